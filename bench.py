@@ -1,0 +1,604 @@
+#!/usr/bin/env python3
+"""Benchmark of the ReplaySSM cached decode step on GB300; prints one JSON line.
+
+Workload (default): one Mamba-2 layer at Nemotron-3-Super shapes -- batch 256,
+128 heads, d_v = 64, d_k = 128, fp32 checkpoint (4 MiB per row), bf16 v/k/q,
+fp32 alpha = sigmoid(N(3, 1)), L = 16, staggered per-row cursors so about 16
+rows flush on every step.  A step is one decode step of the layer: the host
+plan (cursor and flush flag per row) and one launch of the cached-decode
+kernel over the batch; the timed region replays K such steps as one CUDA
+graph, with every input already in HBM.  The checkpoint and rings (1.2 GiB)
+exceed the 129 MB L2, so every step streams its state from HBM.
+
+Reported beside it, on the same inputs: the conventional load-update-store
+kernel, the Gated DeltaNet layer (32 value heads of 128 x 128, fp16 d/k
+rings) and its conventional kernel, an end-to-end figure through the C ABI
+with pinned host buffers, and the CPU oracle timed on the host cores.
+
+``--impl reference`` times the CPU oracle instead (the reference arm).
+Under torchrun every rank runs its own batch of 256 rows on its own GPU (rows
+are independent: weak scaling, no collective on the data path).
+"""
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ReplaySSM decode tokens/s per layer at bs256; achieved HBM GB/s vs roofline"
+UNIT = "tokens/s/layer"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "mamba2_bs256": dict(variant="mamba2", B=256, H=128, d_v=64, d_k=128, L=16, ckpt="f32", inp="bf16",
+                         ring="bf16",
+                         desc="Mamba-2 layer, Nemotron-3-Super shapes: batch 256, 128 heads, d_v 64, d_k 128, "
+                              "fp32 checkpoint, bf16 v/k/q, fp32 alpha=sigmoid(N(3,1)), L 16, staggered cursors"),
+    "gdn_bs256": dict(variant="gdn", B=256, H=32, d_v=128, d_k=128, L=16, ckpt="f32", inp="bf16", ring="f16",
+                      desc="Gated DeltaNet layer: batch 256, 32 value heads of 128 x 128, fp32 checkpoint, "
+                           "fp16 d/k rings, fp32 g ring, L 16, staggered cursors"),
+}
+N_INPUT_SETS = 16  # distinct per-step input sets cycled through the timed steps
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (runs in spawned workers, before any CUDA call)
+# ---------------------------------------------------------------------------
+def _oracle_worker(job):
+    """Time oracle.exact_step on one row of ``heads`` heads for warmup + steps."""
+    variant, heads, d_v, d_k, warmup, steps, seed = job
+    import numpy as np
+
+    import oracle
+
+    r = np.random.default_rng(seed)
+    S = r.standard_normal((1, heads, d_v, d_k)) / math.sqrt(d_k)
+    st = oracle.ExactState(variant, S)
+    slots = np.zeros(1, dtype=np.int32)
+    n_sets = 16  # input sets cycled through the steps
+    v = r.standard_normal((n_sets, 1, heads, d_v)) / math.sqrt(d_k)
+    k = r.standard_normal((n_sets, 1, heads, d_k)) / math.sqrt(d_k)
+    q = r.standard_normal((n_sets, 1, heads, d_k)) / math.sqrt(d_k)
+    a = 1.0 / (1.0 + np.exp(-r.normal(3.0, 1.0, (n_sets, 1, heads))))
+    beta = 1.0 / (1.0 + np.exp(-r.standard_normal((n_sets, 1, heads)))) if variant == "gdn" else [None] * n_sets
+    if variant == "gdn":
+        a = np.log(a)
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+        q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    for t in range(warmup):
+        i = t % n_sets
+        oracle.exact_step(st, slots, v[i], k[i], q[i], a[i], beta[i])
+    t0 = time.perf_counter()
+    for t in range(steps):
+        i = t % n_sets
+        oracle.exact_step(st, slots, v[i], k[i], q[i], a[i], beta[i])
+    return time.perf_counter() - t0
+
+
+def oracle_throughput(spec, budget_s, warmup=1, steps=None):
+    """Tokens/s/layer of the CPU oracle on the host cores.
+
+    Every core runs one row of the layer in a spawned process (BLAS limited to
+    one thread per process); the sample is sized to about ``budget_s`` of work.
+    Returns (tokens_per_s, cores, sample description).
+    """
+    import multiprocessing as mp
+
+    cores = os.cpu_count() or 1
+    H = spec["H"]
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(cores) as pool:
+            # calibrate: one step of one row of all heads
+            t1 = pool.map(_oracle_worker, [(spec["variant"], H, spec["d_v"], spec["d_k"], 1, 1, 99)])[0]
+            heads = H
+            if steps is None:
+                steps = max(1, min(4096, int(budget_s / max(t1, 1e-6))))
+            else:
+                # fixed step count: shrink the per-step sample to fit the budget
+                heads = max(1, min(H, int(H * budget_s / max(t1 * (steps + warmup), 1e-9))))
+            jobs = [(spec["variant"], heads, spec["d_v"], spec["d_k"], warmup, steps, 1000 + i) for i in range(cores)]
+            t0 = time.perf_counter()
+            elapsed = pool.map(_oracle_worker, jobs)
+            wall = time.perf_counter() - t0
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    t_max = max(elapsed)
+    tokens = cores * steps * heads / H  # rows x steps, scaled to all heads
+    sample = (f"{cores} processes x 1 row x {heads}/{H} heads x {steps} steps of the {spec['variant']} layer "
+              f"(float64 NumPy, exact conventional recurrence), {t_max:.1f} s; wall {wall:.1f} s")
+    return tokens / t_max, cores, sample
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed regions
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.windows = []
+        try:
+            import torch
+
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            ident = str(device_index)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+        time.sleep(0.2)
+        self.proc.terminate()
+        out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[4:8]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if any(a <= r[0] <= b for a, b in self.windows)]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        use = inside or rows
+        reasons = sorted({n for r in use for n, v in zip(names, r[4]) if v.lower().startswith("active")})
+        return {
+            "sm_mhz": statistics.median(r[1] for r in use) if use else None,
+            "sm_max_mhz": max(r[2] for r in use) if use else None,
+            "reasons": reasons,
+            "samples_in_timed_regions": len(inside),
+            "power_w_max": max((float(r[3]) for r in use if r[3].replace(".", "", 1).isdigit()), default=None),
+        }
+
+
+# ---------------------------------------------------------------------------
+# GPU side
+# ---------------------------------------------------------------------------
+def _peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_traffic(kernel, workload):
+    """ncu DRAM bytes per launch for ``kernel`` if its sources are unchanged
+    since the counters were taken (profiles/ncu_traffic.json), else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, ValueError, KeyError):
+        return None
+    if rec.get("workload") != workload or rec.get("source_sha256") != source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def source_hash(kernel):
+    files = {"mamba2_replay": ["mamba2.cu"], "gdn_replay": ["gdn.cu"], "conventional": ["conventional.cu"]}[kernel]
+    h = hashlib.sha256()
+    for name in files + ["common.cuh"]:
+        with open(os.path.join(ROOT, "linear_attention_decode_replayssm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+class Layer:
+    """Device state, inputs and per-step plans for one synthetic layer."""
+
+    def __init__(self, lib, spec, device, seed, n_steps):
+        import numpy as np
+        import torch
+
+        self.lib, self.spec, self.device = lib, spec, device
+        B, H, dv, dk, L = (spec[k] for k in ("B", "H", "d_v", "d_k", "L"))
+        td = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        gdn = spec["variant"] == "gdn"
+
+        def randn(*shape):
+            return torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+
+        def unit(x):
+            return x / x.norm(dim=-1, keepdim=True)
+
+        def decay(*shape):
+            a = torch.sigmoid(3.0 + randn(*shape))
+            return torch.log(a) if gdn else a
+
+        sk = math.sqrt(dk)
+        self.ckpt = (randn(B, H, dv, dk) / sk).to(td[spec["ckpt"]])
+        self.state = self.ckpt.clone()  # for the conventional kernel
+        self.ring_v = (randn(B, H, L, dv) / sk).to(td[spec["ring"]])
+        self.ring_k = (unit(randn(B, H, L, dk)) if gdn else randn(B, H, L, dk) / sk).to(td[spec["ring"]])
+        self.ring_a = decay(B, H, L)
+        self.slot_idx = torch.arange(B, device=device, dtype=torch.int32)
+        self.out = torch.empty(B, H, dv, device=device)
+        self.inputs = []
+        for _ in range(N_INPUT_SETS):
+            x = dict(v=(randn(B, H, dv) / sk).to(td[spec["inp"]]))
+            if gdn:
+                x.update(k=unit(randn(B, H, dk)).to(td[spec["inp"]]), q=unit(randn(B, H, dk)).to(td[spec["inp"]]),
+                         alpha=decay(B, H), beta=torch.sigmoid(randn(B, H)))
+            else:
+                x.update(k=(randn(B, H, dk) / sk).to(td[spec["inp"]]), q=(randn(B, H, dk) / sk).to(td[spec["inp"]]),
+                         alpha=decay(B, H), beta=None)
+            self.inputs.append(x)
+        rng = np.random.default_rng(seed)
+        self.decode_step0 = rng.integers(0, L, size=B).astype(np.int64)
+        wps, fls = [], []
+        for t in range(n_steps):
+            wp, fl = lib.replayssm_plan_step(self.decode_step0 + t, L)
+            wps.append(wp)
+            fls.append(fl)
+        self.wp_host, self.fl_host = np.stack(wps), np.stack(fls)
+        self.wp = torch.from_numpy(self.wp_host).to(device)
+        self.fl = torch.from_numpy(self.fl_host).to(device)
+        self.variant_code = lib.RS_GDN if gdn else lib.RS_MAMBA2
+
+    def replay_step(self, t, stream=None, x=None, wp=None, fl=None, out=None):
+        x = self.inputs[t % N_INPUT_SETS] if x is None else x
+        kw = dict(ckpt=self.ckpt, ring_v=self.ring_v, ring_k=self.ring_k, ring_a=self.ring_a,
+                  slot_idx=self.slot_idx, write_pos=self.wp[t] if wp is None else wp,
+                  is_flush=self.fl[t] if fl is None else fl, v=x["v"], k=x["k"], q=x["q"], alpha=x["alpha"],
+                  out=self.out if out is None else out, stream=stream)
+        if self.spec["variant"] == "gdn":
+            self.lib.replayssm_decode_gdn(beta=x["beta"], **kw)
+        else:
+            self.lib.replayssm_decode_mamba2(**kw)
+
+    def conventional_step(self, t, stream=None):
+        x = self.inputs[t % N_INPUT_SETS]
+        self.lib.conventional_decode(variant=self.variant_code, state=self.state, slot_idx=self.slot_idx, v=x["v"],
+                                     k=x["k"], q=x["q"], alpha=x["alpha"], beta=x["beta"], out=self.out,
+                                     stream=stream)
+
+    def bytes_per_step(self, t0, t1, replay=True):
+        from linear_attention_decode_replayssm_gb300 import traffic
+
+        s = self.spec
+        slot = self.slot_idx.cpu().numpy()
+        tot = 0
+        for t in range(t0, t1):
+            tot += traffic.step_bytes(variant=s["variant"], H=s["H"], d_v=s["d_v"], d_k=s["d_k"],
+                                      ckpt_dtype=s["ckpt"], in_dtype=s["inp"], ring_dtype=s["ring"],
+                                      slot_idx=slot, write_pos=self.wp_host[t], is_flush=self.fl_host[t],
+                                      replay=replay)
+        return tot / (t1 - t0)
+
+
+def _timed_graph(torch, fn, t0, t1, stream, eager, dist, sampler):
+    """Run steps t0..t1-1 (captured as one CUDA graph unless ``eager``) in a
+    timed region on ``stream``; returns the max over ranks of the elapsed ms."""
+    graph = None
+    if not eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for t in range(t0, t1):
+                    fn(t, stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    w0 = time.time()
+    start.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for t in range(t0, t1):
+            fn(t, stream)
+    end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    if sampler is not None:
+        sampler.mark(w0, w1)
+    ms = start.elapsed_time(end)
+    if dist is not None:
+        tt = torch.tensor([ms], device=torch.cuda.current_device())
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    del graph
+    return ms
+
+
+def measure_layer(lib, torch, spec, device, args, dist, sampler, seed):
+    """Device-timed ReplaySSM and conventional steps of one layer."""
+    K, W = args.steps, args.warmup
+    layer = Layer(lib, spec, device, seed, W + K)
+    stream = torch.cuda.Stream(device=device)
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for t in range(W):
+            layer.replay_step(t, stream)
+    ms = _timed_graph(torch, layer.replay_step, W, W + K, stream, args.eager, dist, sampler)
+    res = dict(ms_per_step=ms / K, bytes_per_step=layer.bytes_per_step(W, W + K))
+    with torch.cuda.stream(stream):
+        for t in range(W):
+            layer.conventional_step(t, stream)
+    cms = _timed_graph(torch, layer.conventional_step, W, W + K, stream, args.eager, dist, sampler)
+    res.update(conv_ms_per_step=cms / K, conv_bytes_per_step=layer.bytes_per_step(W, W + 1, replay=False))
+    return layer, res
+
+
+def measure_e2e(lib, torch, layer, steps, dist):
+    """Tokens/s through the public API with host buffers: every step copies its
+    inputs from pinned host memory, plans the step on the host, launches the
+    decode, and reads the output back to host memory."""
+    import numpy as np
+
+    dev = layer.device
+    B = layer.spec["B"]
+    host_in = []
+    for x in layer.inputs:
+        host_in.append({n: (t.cpu().pin_memory() if t is not None else None) for n, t in x.items()})
+    d_in = {n: (t.clone() if t is not None else None) for n, t in layer.inputs[0].items()}
+    wp_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    fl_h = torch.empty(B, dtype=torch.uint8).pin_memory()
+    wp_d = torch.empty(B, dtype=torch.int32, device=dev)
+    fl_d = torch.empty(B, dtype=torch.uint8, device=dev)
+    o_h = torch.empty(layer.out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0].values() if t is not None)
+    h2d += wp_h.numel() * 4 + fl_h.numel()
+    d2h = o_h.numel() * 4
+    stream = torch.cuda.Stream(device=dev)
+    wp_np, fl_np = wp_h.numpy(), fl_h.numpy()
+    ds = layer.decode_step0.copy()
+
+    def one(t):
+        x = host_in[t % N_INPUT_SETS]
+        with torch.cuda.stream(stream):
+            for n, t_h in x.items():
+                if t_h is not None:
+                    d_in[n].copy_(t_h, non_blocking=True)
+            lib.replayssm_plan_step(ds + t, layer.spec["L"], write_pos=wp_np, is_flush=fl_np)
+            wp_d.copy_(wp_h, non_blocking=True)
+            fl_d.copy_(fl_h, non_blocking=True)
+            layer.replay_step(t, stream, x=d_in, wp=wp_d, fl=fl_d)
+            o_h.copy_(layer.out, non_blocking=True)
+        stream.synchronize()  # the host holds this step's output
+        return float(o_h[0, 0, 0])
+
+    for t in range(3):
+        one(t)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for t in range(steps):
+        one(t)
+    el = time.perf_counter() - t0
+    if dist is not None:
+        tt = torch.tensor([el], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        el = float(tt.item())
+    return el, h2d, d2h
+
+
+def run_native(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    spec = WORKLOADS[args.workload]
+
+    # CPU baseline first: spawned oracle workers start before any CUDA call
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        val, cores, sample = oracle_throughput(spec, args.cpu_seconds)
+        cpu = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    from linear_attention_decode_replayssm_gb300 import _lib, build
+
+    if rank == 0:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    _lib.load()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    layer, main = measure_layer(_lib, torch, spec, device, args, dist, sampler, seed=rank)
+    extra = {}
+    if not args.no_extras:
+        other = "gdn_bs256" if args.workload == "mamba2_bs256" else "mamba2_bs256"
+        del layer
+        torch.cuda.empty_cache()
+        _, o = measure_layer(_lib, torch, WORKLOADS[other], device, args, dist, sampler, seed=100 + rank)
+        extra[other] = o
+        torch.cuda.empty_cache()
+        layer = Layer(_lib, spec, device, rank, args.warmup + args.e2e_steps + 4)
+    clocks = sampler.finish() if sampler is not None else None
+
+    e2e_el, h2d, d2h = measure_e2e(_lib, torch, layer, args.e2e_steps, dist)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    K, B = args.steps, spec["B"]
+    peak, peak_kind = _peak()
+    ms = main["ms_per_step"]
+    value = world * B / (ms / 1e3)
+    achieved = main["bytes_per_step"] / (ms / 1e3) / 1e9
+    conv_ms = main["conv_ms_per_step"]
+    conv_gbs = main["conv_bytes_per_step"] / (conv_ms / 1e3) / 1e9
+    kernel = "gdn_replay" if spec["variant"] == "gdn" else "mamba2_replay"
+    traffic = _kernel_traffic(kernel, args.workload)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; no model weights or datasets)",
+        "config": {
+            "workload": spec["desc"],
+            "global_batch": world * B,
+            "layers": 1,
+            "l2": "inputs larger than L2: 1.2 GiB of checkpoint and rings streamed every step (L2 is 129 MB)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "timing": "CUDA graph of K steps, CUDA events on the launching stream",
+        },
+        "hbm_gbs": achieved,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": kernel,
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": main["bytes_per_step"],
+        },
+        "conventional": {
+            "ms_per_step": conv_ms,
+            "value": world * B / (conv_ms / 1e3),
+            "hbm_gbs": conv_gbs,
+            "frac": conv_gbs / peak,
+            "algorithmic_bytes_per_launch": main["conv_bytes_per_step"],
+        },
+        "speedup_vs_conventional": conv_ms / ms,
+        "modelled_traffic_ratio": main["bytes_per_step"] / main["conv_bytes_per_step"],
+        "cpu_baseline": cpu,
+        "e2e": {
+            "value": world * B * args.e2e_steps / e2e_el,
+            "unit": UNIT,
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "steps": args.e2e_steps,
+            "how": "C ABI with pinned host buffers: H2D of v/k/q/alpha and the host plan, decode, D2H of o, "
+                   "stream sync per step",
+        },
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    for name, o in extra.items():
+        s = WORKLOADS[name]
+        line[name] = {
+            "workload": s["desc"],
+            "ms_per_step": o["ms_per_step"],
+            "value": world * s["B"] / (o["ms_per_step"] / 1e3),
+            "hbm_gbs": o["bytes_per_step"] / (o["ms_per_step"] / 1e3) / 1e9,
+            "frac": o["bytes_per_step"] / (o["ms_per_step"] / 1e3) / 1e9 / peak,
+            "conventional_ms_per_step": o["conv_ms_per_step"],
+            "conventional_hbm_gbs": o["conv_bytes_per_step"] / (o["conv_ms_per_step"] / 1e3) / 1e9,
+            "speedup_vs_conventional": o["conv_ms_per_step"] / o["ms_per_step"],
+            "modelled_traffic_ratio": o["bytes_per_step"] / o["conv_bytes_per_step"],
+        }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    spec = WORKLOADS[args.workload]
+    val, cores, sample = oracle_throughput(spec, args.ref_seconds, warmup=args.warmup, steps=args.steps)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": val,
+        "unit": UNIT,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": spec["B"] / val * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": spec["desc"], "global_batch": spec["B"], "layers": 1,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": val, "unit": UNIT, "kind": "oracle", "cores": cores, "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4096)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mamba2_bs256")
+    ap.add_argument("--eager", action="store_true", help="launch steps one by one instead of a CUDA graph")
+    ap.add_argument("--no-extras", action="store_true", help="skip the second layer type")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle timing")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--e2e-steps", type=int, default=256)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native" and not args.eager:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+/*
+ * replayssm.h -- C ABI of libreplayssm.so, the GB300 (sm_103a) ReplaySSM
+ * cached SSM decode step.
+ *
+ * Sources, cited below by short name:
+ *   [Ghana]   S. Ghana, "ReplaySSM: an SSM decoder that writes its state once
+ *             every 16 tokens".
+ *   [PR48792] vLLM pull request 48792, "[Kernel] ReplaySSM: cache SSM inputs
+ *             for faster Gated DeltaNet standard decode".
+ *   [NV]      NVIDIA technical blog, "ReplaySSM: Rethinking State Storage for
+ *             Faster Hybrid Model Decoding".
+ *
+ * What a decode step computes (per batch row b and head h, p = write_pos[b]
+ * records already in the row's ring, the current token being record p + 1):
+ *
+ *   Mamba-2 non-flush ([Ghana] §Output without a state):
+ *     o = gamma_{p+1} S_ckpt q + sum_{j=1..p+1} gamma_{j+1:p+1} v_j (k_j . q),
+ *     then the record (alpha, v, k) is appended at ring slot p.
+ *   Mamba-2 flush ([Ghana] §The identity):
+ *     S_new = gamma_{p+1} S_ckpt + sum_j gamma_{j+1:p+1} v_j k_j^T,
+ *     o = S_new q (unrounded), S_ckpt <- S_new cast to the checkpoint type;
+ *     no record is appended and the ring is logically empty afterwards.
+ *   Gated DeltaNet ([Ghana] §The delta-rule wrinkle; [PR48792] §Core concept
+ *   and the review comment on S_{t-1} q and S_{t-1} k): the ring holds the
+ *   corrected value d, the key k and the log-gate g; with
+ *     G_j = exp(sum_{l=j+1..p} g_l), Gamma = exp(sum_{l<=p} g_l),
+ *     S_{t-1} x = Gamma S_ckpt x + sum_{j<=p} G_j (k_j . x) d_j  (x = k_t, q_t),
+ *     alpha_t = exp(g_t), d_t = beta_t (v_t - alpha_t S_{t-1} k_t),
+ *     o = alpha_t S_{t-1} q_t + d_t (k_t . q_t);
+ *   non-flush appends (d_t, k_t, g_t) rounded to the ring type; flush stores
+ *   S_new = alpha_t S_{t-1} + d_t k_t^T (from the unrounded d_t) and outputs
+ *   S_new q_t.
+ *   Conventional baseline ([Ghana] §Why a fixed-size state is not cheap to
+ *   decode): load the state, S <- alpha S + v k^T (delta rule for GDN),
+ *   o = S q, store the state, every step.
+ *
+ * Memory and ownership: every pointer in rs_step_args is a DEVICE pointer
+ * owned by the caller (PyTorch allocates and frees everything).  The library
+ * never allocates, frees or synchronises, and never reads device memory on
+ * the host, so a call is asynchronous on `stream` and can be captured in a
+ * CUDA graph ([PR48792] §CUDA graphs and continuous batching).  Checkpoint and
+ * rings are updated in place.  Two rows of one call must not name the same
+ * slot (their updates would race).
+ *
+ * Errors: arguments are validated on the host before anything is launched; an
+ * invalid call returns a negative rs_status and launches nothing.  A failed
+ * launch returns RS_ECUDA.  Values only the device sees (slot_idx, write_pos)
+ * are range-checked in the kernel: a row with an out-of-range slot or cursor
+ * is skipped (its output row is zero-filled, no state is touched) and the
+ * matching RS_DERR_* bit is OR-ed into *dev_err when dev_err is not NULL.  The
+ * kernels never trap.
+ */
+#ifndef REPLAYSSM_H_
+#define REPLAYSSM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *rs_stream_t;
+
+#define RS_ABI_VERSION 1
+#define RS_MAX_L 64 /* largest supported buffer length */
+
+typedef enum {
+  RS_OK = 0,
+  RS_EINVAL = -1,       /* a null pointer, a bad size or an inconsistent argument */
+  RS_EUNSUPPORTED = -2, /* shape / dtype combination not built into the library */
+  RS_EALIGN = -3,       /* a pointer or row stride breaks the 16-byte rule below */
+  RS_ECUDA = -4         /* the CUDA runtime reported an error at launch */
+} rs_status;
+
+typedef enum { RS_F32 = 0, RS_F16 = 1, RS_BF16 = 2 } rs_dtype;
+
+typedef enum { RS_MAMBA2 = 0, RS_GDN = 1 } rs_variant;
+
+/* Bits the kernels OR into *dev_err. */
+typedef enum {
+  RS_DERR_SLOT = 1,      /* slot_idx[b] >= num_slots */
+  RS_DERR_WRITE_POS = 2  /* write_pos[b] outside [0, L) */
+} rs_dev_error;
+
+/*
+ * One decode step of a batch over a paged state pool ([PR48792] §Paged cache
+ * layout: checkpoint and ring caches live in the per-request state block;
+ * the block table becomes slot_idx here).
+ *
+ * Layouts (row-major, last dimension contiguous):
+ *   ckpt    [num_slots, H, d_v, d_k]  ckpt_dtype (RS_F32 or RS_F16)
+ *   ring_v  [num_slots, H, L, d_v]    ring_dtype: Mamba-2 v records (must equal
+ *                                     in_dtype: records are the inputs verbatim);
+ *                                     GDN corrected values d (RS_F16 or RS_F32)
+ *   ring_k  [num_slots, H, L, d_k]    ring_dtype: key records
+ *   ring_a  [num_slots, H, L]         fp32: Mamba-2 decay alpha / GDN log-gate g
+ *   v       [B, .. H, d_v]            in_dtype (RS_BF16 or RS_F32); row b starts
+ *   k, q    [B, .. H, d_k]            at b * stride_*_row elements, heads packed
+ *   alpha   [B, H]                    fp32, packed: Mamba-2 decay in (0,1), or
+ *                                     GDN log-gate g (alpha_t = exp(g) )
+ *   beta    [B, H]                    fp32, packed; GDN only (NULL for Mamba-2)
+ *   out     [B, .. H, d_v]            fp32 output
+ *   slot_idx  [B] int32: slot of row b; a negative value marks a padded row,
+ *             which touches no state and gets a zero output row.
+ *   write_pos [B] int32 in [0, L): records already held by the row's ring.
+ *   is_flush  [B] uint8: nonzero = fold the ring and write the checkpoint.
+ * Alignment: ckpt, ring_v, ring_k, v, k, q must be 16-byte aligned, and each
+ * row stride times the element size a multiple of 16 bytes.
+ * Cursor and flag come from replayssm_plan_step (host) each step.
+ */
+typedef struct rs_step_args {
+  int32_t B;          /* rows in the batch (0 = nothing to do) */
+  int32_t H;          /* heads per row */
+  int32_t d_v, d_k;   /* head dimensions (see replayssm_supported) */
+  int32_t L;          /* buffer length, 2 <= L <= RS_MAX_L */
+  int32_t num_slots;  /* slots in the paged pools */
+  int32_t ckpt_dtype; /* rs_dtype */
+  int32_t in_dtype;   /* rs_dtype of v, k, q */
+  int32_t ring_dtype; /* rs_dtype of ring_v, ring_k */
+  int32_t reserved;   /* must be 0 */
+  const int32_t *slot_idx;
+  const int32_t *write_pos;
+  const uint8_t *is_flush;
+  const void *v;
+  const void *k;
+  const void *q;
+  const float *alpha;
+  const float *beta;
+  void *ckpt;
+  void *ring_v;
+  void *ring_k;
+  float *ring_a;
+  float *out;
+  int64_t stride_v_row, stride_k_row, stride_q_row, stride_out_row; /* elements */
+  int32_t *dev_err; /* optional device int32, see rs_dev_error */
+} rs_step_args;
+
+/* RS_ABI_VERSION of the loaded library. */
+int replayssm_abi_version(void);
+
+/* 1 if (variant, d_v, d_k, ckpt_dtype) is built into the library, else 0. */
+int replayssm_supported(int variant, int d_v, int d_k, int ckpt_dtype);
+
+/*
+ * Host-side step plan ([PR48792] §CUDA graphs and continuous batching):
+ *   write_pos[b] = decode_step[b] mod L,
+ *   is_flush[b]  = (write_pos[b] == L - 1) or force_flush[b] != 0.
+ * decode_step [B] >= 0 (tokens the row has decoded), force_flush [B] or NULL;
+ * outputs write_pos [B], is_flush [B].  All HOST memory.  After a forced flush
+ * the caller re-anchors decode_step so the next cursor is 0 (align mode).
+ * Returns RS_OK, or RS_EINVAL (null pointer, B < 0, L outside [1, RS_MAX_L],
+ * negative decode_step: outputs untouched).
+ */
+int replayssm_plan_step(const int64_t *decode_step, const uint8_t *force_flush,
+                        int32_t B, int32_t L, int32_t *write_pos, uint8_t *is_flush);
+
+/* ReplaySSM Mamba-2 cached decode step, non-flush and flush rows in one
+ * launch (beta unused). */
+int replayssm_decode_mamba2(const rs_step_args *args, rs_stream_t stream);
+
+/* ReplaySSM Gated DeltaNet cached decode step (alpha = log-gate g, beta used). */
+int replayssm_decode_gdn(const rs_step_args *args, rs_stream_t stream);
+
+/* Conventional load-update-store step on the same state tensor (ckpt is the
+ * state; ring_*, write_pos and is_flush are ignored and may be NULL).
+ * variant is RS_MAMBA2 or RS_GDN. */
+int conventional_decode(const rs_step_args *args, int variant, rs_stream_t stream);
+
+/* Static string naming an rs_status value. */
+const char *replayssm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REPLAYSSM_H_ */

@@ -1,0 +1,276 @@
+"""Thin ctypes binding of libreplayssm.so (same entry-point names as the C ABI).
+
+Argument marshalling only: tensors are checked for device, dtype and layout,
+their ``data_ptr()`` and strides go into an ``rs_step_args`` struct, and the
+call runs on the current torch CUDA stream (or the one given).  Every step of
+the computation runs in the library's CUDA kernels; there is no CPU fallback,
+and loading fails loudly when the library has not been built.
+
+C declarations and their documentation: include/replayssm.h.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+RS_OK, RS_EINVAL, RS_EUNSUPPORTED, RS_EALIGN, RS_ECUDA = 0, -1, -2, -3, -4
+RS_F32, RS_F16, RS_BF16 = 0, 1, 2
+RS_MAMBA2, RS_GDN = 0, 1
+RS_DERR_SLOT, RS_DERR_WRITE_POS = 1, 2
+RS_ABI_VERSION = 1
+RS_MAX_L = 64
+
+# every symbol include/replayssm.h declares
+EXPORTS = (
+    "replayssm_abi_version",
+    "replayssm_supported",
+    "replayssm_plan_step",
+    "replayssm_decode_mamba2",
+    "replayssm_decode_gdn",
+    "conventional_decode",
+    "replayssm_status_string",
+)
+
+
+class StepArgs(ctypes.Structure):
+    """Mirror of ``rs_step_args``."""
+
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("d_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
+        ("L", ctypes.c_int32), ("num_slots", ctypes.c_int32), ("ckpt_dtype", ctypes.c_int32),
+        ("in_dtype", ctypes.c_int32), ("ring_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("slot_idx", ctypes.c_void_p), ("write_pos", ctypes.c_void_p), ("is_flush", ctypes.c_void_p),
+        ("v", ctypes.c_void_p), ("k", ctypes.c_void_p), ("q", ctypes.c_void_p),
+        ("alpha", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("ckpt", ctypes.c_void_p), ("ring_v", ctypes.c_void_p), ("ring_k", ctypes.c_void_p),
+        ("ring_a", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("stride_v_row", ctypes.c_int64), ("stride_k_row", ctypes.c_int64),
+        ("stride_q_row", ctypes.c_int64), ("stride_out_row", ctypes.c_int64),
+        ("dev_err", ctypes.c_void_p),
+    ]
+
+
+_LIB = None
+
+
+def load():
+    """Load the library (once).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (linear_attention_decode_replayssm_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    lib.replayssm_abi_version.restype = ctypes.c_int
+    lib.replayssm_abi_version.argtypes = []
+    lib.replayssm_supported.restype = ctypes.c_int
+    lib.replayssm_supported.argtypes = [ctypes.c_int] * 4
+    lib.replayssm_plan_step.restype = ctypes.c_int
+    lib.replayssm_plan_step.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_void_p, ctypes.c_void_p]
+    for name in ("replayssm_decode_mamba2", "replayssm_decode_gdn"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = [P(StepArgs), ctypes.c_void_p]
+    lib.conventional_decode.restype = ctypes.c_int
+    lib.conventional_decode.argtypes = [P(StepArgs), ctypes.c_int, ctypes.c_void_p]
+    lib.replayssm_status_string.restype = ctypes.c_char_p
+    lib.replayssm_status_string.argtypes = [ctypes.c_int]
+    got = lib.replayssm_abi_version()
+    if got != RS_ABI_VERSION:
+        raise RuntimeError(f"libreplayssm ABI version {got}, binding expects {RS_ABI_VERSION}")
+    _LIB = lib
+    return lib
+
+
+def status_string(status):
+    return load().replayssm_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status != RS_OK:
+        raise RuntimeError(f"{what}: {status_string(status)}")
+    return status
+
+
+def replayssm_abi_version():
+    return load().replayssm_abi_version()
+
+
+def replayssm_supported(variant, d_v, d_k, ckpt_dtype):
+    return bool(load().replayssm_supported(int(variant), int(d_v), int(d_k), int(ckpt_dtype)))
+
+
+# --------------------------------------------------------------------------
+# host step plan
+# --------------------------------------------------------------------------
+def replayssm_plan_step(decode_step, L, force_flush=None, write_pos=None, is_flush=None):
+    """Per-row cursor and flush flag on the host (NumPy arrays; optional
+    preallocated outputs, e.g. pinned-memory views)."""
+    ds = np.ascontiguousarray(decode_step, dtype=np.int64)
+    B = ds.shape[0]
+    if write_pos is None:
+        write_pos = np.empty(B, dtype=np.int32)
+    if is_flush is None:
+        is_flush = np.empty(B, dtype=np.uint8)
+    ff = None
+    if force_flush is not None:
+        ff = np.ascontiguousarray(force_flush, dtype=np.uint8)
+        if ff.shape != (B,):
+            raise ValueError("force_flush must have shape [B]")
+    if write_pos.dtype != np.int32 or is_flush.dtype != np.uint8 or not (
+            write_pos.flags.c_contiguous and is_flush.flags.c_contiguous):
+        raise ValueError("write_pos must be contiguous int32 and is_flush contiguous uint8")
+    _check(load().replayssm_plan_step(ds.ctypes.data, None if ff is None else ff.ctypes.data, B, int(L),
+                                      write_pos.ctypes.data, is_flush.ctypes.data), "replayssm_plan_step")
+    return write_pos, is_flush
+
+
+# --------------------------------------------------------------------------
+# decode steps
+# --------------------------------------------------------------------------
+def _torch():
+    import torch
+
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    m = {torch.float32: RS_F32, torch.float16: RS_F16, torch.bfloat16: RS_BF16}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _need(t, name, dtype=None, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    return t
+
+
+def _rows(t, name, H, d):
+    """[B, H, d] with packed heads and a free row stride; returns row stride."""
+    if t.shape[1:] != (H, d) or t.stride(2) != 1 or t.stride(1) != d:
+        raise ValueError(f"{name} must be [B, {H}, {d}] with packed heads (got {tuple(t.shape)}, strides {t.stride()})")
+    return t.stride(0)
+
+
+def _fill(args, *, variant, ckpt, slot_idx, v, k, q, alpha, out, beta=None, ring_v=None, ring_k=None,
+          ring_a=None, write_pos=None, is_flush=None, dev_err=None):
+    torch = _torch()
+    _need(ckpt, "ckpt", ndim=4)
+    if not ckpt.is_contiguous():
+        raise ValueError("ckpt must be contiguous [num_slots, H, d_v, d_k]")
+    S, H, d_v, d_k = ckpt.shape
+    _need(slot_idx, "slot_idx", torch.int32, 1)
+    B = slot_idx.shape[0]
+    for name, t in (("v", v), ("k", k), ("q", q)):
+        _need(t, name, ndim=3)
+        if t.shape[0] != B:
+            raise ValueError(f"{name} has {t.shape[0]} rows, slot_idx has {B}")
+    if not (v.dtype == k.dtype == q.dtype):
+        raise TypeError("v, k, q must share one dtype")
+    _need(alpha, "alpha", torch.float32, 2)
+    _need(out, "out", torch.float32, 3)
+    if alpha.shape != (B, H) or not alpha.is_contiguous():
+        raise ValueError("alpha must be contiguous [B, H]")
+    if out.shape[0] != B:
+        raise ValueError("out must have B rows")
+    args.B, args.H, args.d_v, args.d_k, args.num_slots = B, H, d_v, d_k, S
+    args.ckpt_dtype, args.in_dtype = _dtype_code(ckpt), _dtype_code(v)
+    args.reserved = 0
+    args.slot_idx, args.ckpt = slot_idx.data_ptr(), ckpt.data_ptr()
+    args.v, args.k, args.q = v.data_ptr(), k.data_ptr(), q.data_ptr()
+    args.alpha, args.out = alpha.data_ptr(), out.data_ptr()
+    args.stride_v_row = _rows(v, "v", H, d_v)
+    args.stride_k_row = _rows(k, "k", H, d_k)
+    args.stride_q_row = _rows(q, "q", H, d_k)
+    args.stride_out_row = _rows(out, "out", H, d_v)
+    if variant == RS_GDN:
+        _need(beta, "beta", torch.float32, 2)
+        if beta.shape != (B, H) or not beta.is_contiguous():
+            raise ValueError("beta must be contiguous [B, H]")
+        args.beta = beta.data_ptr()
+    else:
+        args.beta = None
+    if ring_v is not None:
+        for name, t, shp in (("ring_v", ring_v, (S, H, None, d_v)), ("ring_k", ring_k, (S, H, None, d_k)),
+                             ("ring_a", ring_a, (S, H, None))):
+            _need(t, name)
+            if not t.is_contiguous() or t.dim() != len(shp) or any(
+                    want is not None and got != want for got, want in zip(t.shape, shp)):
+                raise ValueError(f"{name} must be contiguous with shape {shp} (None = L)")
+        L = ring_a.shape[2]
+        if ring_v.shape[2] != L or ring_k.shape[2] != L:
+            raise ValueError("ring_v, ring_k and ring_a disagree on L")
+        if ring_v.dtype != ring_k.dtype or ring_a.dtype != torch.float32:
+            raise TypeError("ring_v and ring_k share a dtype; ring_a is float32")
+        _need(write_pos, "write_pos", torch.int32, 1)
+        _need(is_flush, "is_flush", torch.uint8, 1)
+        if write_pos.shape[0] != B or is_flush.shape[0] != B:
+            raise ValueError("write_pos and is_flush must have B entries")
+        args.L = L
+        args.ring_dtype = _dtype_code(ring_v)
+        args.ring_v, args.ring_k, args.ring_a = ring_v.data_ptr(), ring_k.data_ptr(), ring_a.data_ptr()
+        args.write_pos, args.is_flush = write_pos.data_ptr(), is_flush.data_ptr()
+    else:
+        args.L, args.ring_dtype = 0, args.in_dtype
+        args.ring_v = args.ring_k = args.ring_a = args.write_pos = args.is_flush = None
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+        args.dev_err = dev_err.data_ptr()
+    else:
+        args.dev_err = None
+    return args
+
+
+def _stream(stream):
+    if stream is None:
+        return _torch().cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def replayssm_decode_mamba2(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos, is_flush, v, k, q, alpha,
+                            out, dev_err=None, stream=None):
+    """One ReplaySSM Mamba-2 decode step in place on ckpt and the rings; o in ``out``."""
+    args = _fill(StepArgs(), variant=RS_MAMBA2, ckpt=ckpt, slot_idx=slot_idx, v=v, k=k, q=q, alpha=alpha,
+                 out=out, ring_v=ring_v, ring_k=ring_k, ring_a=ring_a, write_pos=write_pos,
+                 is_flush=is_flush, dev_err=dev_err)
+    return _check(load().replayssm_decode_mamba2(ctypes.byref(args), _stream(stream)), "replayssm_decode_mamba2")
+
+
+def replayssm_decode_gdn(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos, is_flush, v, k, q, alpha, beta,
+                         out, dev_err=None, stream=None):
+    """One ReplaySSM Gated DeltaNet decode step (alpha holds the log-gate g)."""
+    args = _fill(StepArgs(), variant=RS_GDN, ckpt=ckpt, slot_idx=slot_idx, v=v, k=k, q=q, alpha=alpha,
+                 beta=beta, out=out, ring_v=ring_v, ring_k=ring_k, ring_a=ring_a, write_pos=write_pos,
+                 is_flush=is_flush, dev_err=dev_err)
+    return _check(load().replayssm_decode_gdn(ctypes.byref(args), _stream(stream)), "replayssm_decode_gdn")
+
+
+def conventional_decode(*, variant, state, slot_idx, v, k, q, alpha, out, beta=None, dev_err=None, stream=None):
+    """One conventional load-update-store step on ``state`` [num_slots, H, d_v, d_k]."""
+    args = _fill(StepArgs(), variant=variant, ckpt=state, slot_idx=slot_idx, v=v, k=k, q=q, alpha=alpha,
+                 beta=beta, out=out, dev_err=dev_err)
+    return _check(load().conventional_decode(ctypes.byref(args), int(variant), _stream(stream)),
+                  "conventional_decode")
+
+
+def raw_call(name, args, *extra):
+    """Call an entry point with a prepared StepArgs and return the status
+    (no exception).  Used to exercise the C-side validation."""
+    fn = getattr(load(), name)
+    return fn(ctypes.byref(args), *extra)

@@ -1,0 +1,175 @@
+// C ABI of libreplayssm.so: argument validation, the host step plan and
+// dispatch to the kernels.  Declarations and their documentation are in
+// include/replayssm.h.
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "../../include/replayssm.h"
+#include "launch.h"
+
+namespace rs {
+
+cudaError_t ensure_smem(const void *kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  static std::mutex mu;
+  static std::set<std::pair<int, const void *>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({dev, kernel})) return cudaSuccess;
+  // allow the largest opt-in size once, so later, larger L need no new call
+  int max_optin = 0;
+  e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if ((size_t)max_optin < bytes) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+  if (e == cudaSuccess) done.insert({dev, kernel});
+  return e;
+}
+
+}  // namespace rs
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+size_t esize(int dt) { return dt == RS_F32 ? 4 : 2; }
+
+bool shape_supported(int d_v, int d_k) {
+  return (d_v == 16 && d_k == 32) || (d_v == 64 && d_k == 128) || (d_v == 128 && d_k == 128);
+}
+
+// Validation shared by every decode entry point.  `replay` adds the ring and
+// cursor arguments; `gdn` adds beta and the GDN ring rule.
+int validate(const rs_step_args *a, bool replay, bool gdn) {
+  if (!a) return RS_EINVAL;
+  if (a->reserved != 0) return RS_EINVAL;
+  if (a->B < 0 || a->H < 1 || a->num_slots < 1 || a->d_v < 1 || a->d_k < 1) return RS_EINVAL;
+  if (replay && (a->L < 2 || a->L > RS_MAX_L)) return RS_EINVAL;
+  if (a->ckpt_dtype != RS_F32 && a->ckpt_dtype != RS_F16) return RS_EUNSUPPORTED;
+  if (a->in_dtype != RS_F32 && a->in_dtype != RS_BF16) return RS_EUNSUPPORTED;
+  if (!shape_supported(a->d_v, a->d_k)) return RS_EUNSUPPORTED;
+  if (replay) {
+    if (gdn) {
+      if (a->ring_dtype != RS_F16 && a->ring_dtype != RS_F32) return RS_EUNSUPPORTED;
+    } else if (a->ring_dtype != a->in_dtype) {
+      return RS_EUNSUPPORTED;  // Mamba-2 records are the inputs verbatim
+    }
+  }
+  if (a->B == 0) return RS_OK;
+  if (!a->slot_idx || !a->v || !a->k || !a->q || !a->alpha || !a->ckpt || !a->out) return RS_EINVAL;
+  if (gdn && !a->beta) return RS_EINVAL;
+  if (replay && (!a->write_pos || !a->is_flush || !a->ring_v || !a->ring_k || !a->ring_a)) return RS_EINVAL;
+  const int64_t H = a->H;
+  if (a->stride_v_row < H * a->d_v || a->stride_k_row < H * a->d_k || a->stride_q_row < H * a->d_k ||
+      a->stride_out_row < H * a->d_v)
+    return RS_EINVAL;
+  const size_t ie = esize(a->in_dtype);
+  if (!aligned16(a->ckpt) || !aligned16(a->v) || !aligned16(a->k) || !aligned16(a->q)) return RS_EALIGN;
+  if ((a->stride_v_row * ie) % 16 || (a->stride_k_row * ie) % 16 || (a->stride_q_row * ie) % 16) return RS_EALIGN;
+  if (!aligned4(a->out) || !aligned4(a->alpha) || !aligned4(a->slot_idx)) return RS_EALIGN;
+  if (gdn && !aligned4(a->beta)) return RS_EALIGN;
+  if (replay) {
+    if (!aligned16(a->ring_v) || !aligned16(a->ring_k) || !aligned4(a->ring_a) || !aligned4(a->write_pos))
+      return RS_EALIGN;
+  }
+  if ((int64_t)a->B * a->H > 0x7fffffffLL) return RS_EINVAL;
+  return RS_OK;
+}
+
+rs::KArgs to_kargs(const rs_step_args *a) {
+  rs::KArgs k;
+  k.B = a->B;
+  k.H = a->H;
+  k.L = a->L;
+  k.num_slots = a->num_slots;
+  k.in_dtype = a->in_dtype;
+  k.ring_dtype = a->ring_dtype;
+  k.slot_idx = a->slot_idx;
+  k.write_pos = a->write_pos;
+  k.is_flush = a->is_flush;
+  k.v = a->v;
+  k.k = a->k;
+  k.q = a->q;
+  k.alpha = a->alpha;
+  k.beta = a->beta;
+  k.ckpt = a->ckpt;
+  k.ring_v = a->ring_v;
+  k.ring_k = a->ring_k;
+  k.ring_a = a->ring_a;
+  k.out = a->out;
+  k.sv = a->stride_v_row;
+  k.sk = a->stride_k_row;
+  k.sq = a->stride_q_row;
+  k.so = a->stride_out_row;
+  k.dev_err = a->dev_err;
+  return k;
+}
+
+int run(rs::LaunchFn fn, const rs_step_args *a, rs_stream_t stream) {
+  if (!fn) return RS_EUNSUPPORTED;
+  const cudaError_t e = fn(to_kargs(a), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RS_OK : RS_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int replayssm_abi_version(void) { return RS_ABI_VERSION; }
+
+int replayssm_supported(int variant, int d_v, int d_k, int ckpt_dtype) {
+  if (variant != RS_MAMBA2 && variant != RS_GDN) return 0;
+  if (variant == RS_MAMBA2) return rs::find_mamba2(d_v, d_k, ckpt_dtype) != nullptr;
+  return rs::find_gdn(d_v, d_k, ckpt_dtype) != nullptr;
+}
+
+int replayssm_plan_step(const int64_t *decode_step, const uint8_t *force_flush, int32_t B, int32_t L,
+                        int32_t *write_pos, uint8_t *is_flush) {
+  if (B < 0 || L < 1 || L > RS_MAX_L) return RS_EINVAL;
+  if (B == 0) return RS_OK;
+  if (!decode_step || !write_pos || !is_flush) return RS_EINVAL;
+  for (int32_t b = 0; b < B; ++b)
+    if (decode_step[b] < 0) return RS_EINVAL;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t wp = (int32_t)(decode_step[b] % L);
+    write_pos[b] = wp;
+    is_flush[b] = (uint8_t)((wp == L - 1) || (force_flush && force_flush[b]));
+  }
+  return RS_OK;
+}
+
+int replayssm_decode_mamba2(const rs_step_args *args, rs_stream_t stream) {
+  const int st = validate(args, /*replay=*/true, /*gdn=*/false);
+  if (st != RS_OK || args->B == 0) return st;
+  return run(rs::find_mamba2(args->d_v, args->d_k, args->ckpt_dtype), args, stream);
+}
+
+int replayssm_decode_gdn(const rs_step_args *args, rs_stream_t stream) {
+  const int st = validate(args, /*replay=*/true, /*gdn=*/true);
+  if (st != RS_OK || args->B == 0) return st;
+  return run(rs::find_gdn(args->d_v, args->d_k, args->ckpt_dtype), args, stream);
+}
+
+int conventional_decode(const rs_step_args *args, int variant, rs_stream_t stream) {
+  if (variant != RS_MAMBA2 && variant != RS_GDN) return RS_EINVAL;
+  const int st = validate(args, /*replay=*/false, /*gdn=*/variant == RS_GDN);
+  if (st != RS_OK || args->B == 0) return st;
+  return run(rs::find_conventional(variant, args->d_v, args->d_k, args->ckpt_dtype), args, stream);
+}
+
+const char *replayssm_status_string(int status) {
+  switch (status) {
+    case RS_OK: return "RS_OK";
+    case RS_EINVAL: return "RS_EINVAL: invalid argument";
+    case RS_EUNSUPPORTED: return "RS_EUNSUPPORTED: shape or dtype not built into the library";
+    case RS_EALIGN: return "RS_EALIGN: pointer or row stride not aligned";
+    case RS_ECUDA: return "RS_ECUDA: CUDA launch error";
+    default: return "unknown rs_status";
+  }
+}
+
+}  // extern "C"

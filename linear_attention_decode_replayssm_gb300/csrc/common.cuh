@@ -1,0 +1,225 @@
+// Device helpers shared by the ReplaySSM kernels (sm_103a).
+//
+// Memory layout conventions (all row-major, last dimension contiguous):
+//   checkpoint / state  [num_slots, H, d_v, d_k]  fp32 or fp16
+//   ring_v              [num_slots, H, L, d_v]
+//   ring_k              [num_slots, H, L, d_k]
+//   ring_a              [num_slots, H, L]          fp32
+// A CTA owns one (row, head) unit.  Its threads tile the d_v x d_k block in
+// 16-byte vectors: G = d_k * sizeof(T) / 16 consecutive lanes cover one state
+// row, so every warp-wide load instruction reads whole 512-byte (fp32) or
+// 256-byte (fp16) rows, fully coalesced.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rs {
+
+constexpr int kF32 = 0;
+constexpr int kF16 = 1;
+constexpr int kBF16 = 2;
+
+// Kernel arguments, copied by value into the launch (mirrors rs_step_args).
+struct KArgs {
+  int B, H, L, num_slots, in_dtype, ring_dtype;
+  const int32_t *slot_idx;
+  const int32_t *write_pos;
+  const uint8_t *is_flush;
+  const void *v, *k, *q;
+  const float *alpha, *beta;
+  void *ckpt, *ring_v, *ring_k;
+  float *ring_a, *out;
+  long long sv, sk, sq, so;  // row strides in elements
+  int32_t *dev_err;
+};
+
+// ---------------------------------------------------------------------------
+// 16-byte checkpoint vectors
+// ---------------------------------------------------------------------------
+template <typename TC>
+struct CkVec;
+
+template <>
+struct CkVec<float> {
+  static constexpr int E = 4;  // elements per 16-byte vector
+  __device__ __forceinline__ static void unpack(const uint4 &r, float (&f)[4]) {
+    f[0] = __uint_as_float(r.x);
+    f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z);
+    f[3] = __uint_as_float(r.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+template <>
+struct CkVec<__half> {
+  static constexpr int E = 8;
+  __device__ __forceinline__ static float2 h2f(uint32_t w) {
+    __half2 h = *reinterpret_cast<__half2 *>(&w);
+    return __half22float2(h);
+  }
+  __device__ __forceinline__ static uint32_t f2h(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+  __device__ __forceinline__ static void unpack(const uint4 &r, float (&f)[8]) {
+    float2 a = h2f(r.x), b = h2f(r.y), c = h2f(r.z), d = h2f(r.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+  __device__ __forceinline__ static uint4 pack(const float (&f)[8]) {
+    return make_uint4(f2h(f[0], f[1]), f2h(f[2], f[3]), f2h(f[4], f[5]), f2h(f[6], f[7]));
+  }
+};
+
+// Streaming read of data used once: read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_vec(void *p, const uint4 &v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// 8-element staging of inputs and ring records with a runtime element type
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void bf16x2_to_f(uint32_t w, float &a, float &b) {
+  a = __uint_as_float(w << 16);
+  b = __uint_as_float(w & 0xffff0000u);
+}
+
+// Load 8 consecutive elements starting at element offset `off` (16-byte
+// aligned for 16-bit types, 32-byte aligned for fp32) and widen to fp32.
+__device__ __forceinline__ void load8(const void *base, size_t off, int dt, float (&f)[8]) {
+  if (dt == kF32) {
+    const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + off);
+    float4 a = __ldg(p), b = __ldg(p + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  } else {
+    uint4 r = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + off));
+    if (dt == kBF16) {
+      bf16x2_to_f(r.x, f[0], f[1]);
+      bf16x2_to_f(r.y, f[2], f[3]);
+      bf16x2_to_f(r.z, f[4], f[5]);
+      bf16x2_to_f(r.w, f[6], f[7]);
+    } else {
+      float tmp[8];
+      CkVec<__half>::unpack(r, tmp);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = tmp[i];
+    }
+  }
+}
+
+// Copy 8 elements verbatim (same element type on both sides).
+__device__ __forceinline__ void copy8(void *dst, size_t doff, const void *src, size_t soff, int dt) {
+  if (dt == kF32) {
+    const float4 *s = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + soff);
+    float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(dst) + doff);
+    d[0] = __ldg(s);
+    d[1] = __ldg(s + 1);
+  } else {
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dst) + doff) =
+        __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(src) + soff));
+  }
+}
+
+// Store 8 fp32 values as fp32 or fp16 (round to nearest even).
+__device__ __forceinline__ void store8(void *dst, size_t off, int dt, const float (&f)[8]) {
+  if (dt == kF32) {
+    float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(dst) + off);
+    d[0] = make_float4(f[0], f[1], f[2], f[3]);
+    d[1] = make_float4(f[4], f[5], f[6], f[7]);
+  } else {
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dst) + off) = CkVec<__half>::pack(f);
+  }
+}
+
+// Store one fp32 value as fp32 or fp16 (round to nearest even).
+__device__ __forceinline__ void store1(void *dst, size_t off, int dt, float x) {
+  if (dt == kF32)
+    static_cast<float *>(dst)[off] = x;
+  else
+    static_cast<__half *>(dst)[off] = __float2half_rn(x);
+}
+
+// ---------------------------------------------------------------------------
+// Transposed group reduction.
+// Each lane holds N partial sums; lanes are grouped G at a time (G a power of
+// two dividing 32, groups contiguous in the warp).  Every halving stage trades
+// half of the values with the partner lane `G/2` away, so after log2(N)
+// stages each lane holds one fully combined value instead of N; the remaining
+// G/N lanes finish with a plain butterfly.  Costs N-1 + log2(G/N) shuffles
+// instead of N*log2(G).  Requires N <= G.
+// ---------------------------------------------------------------------------
+template <int N, int G>
+__device__ __forceinline__ void group_reduce(float *v, int lane) {
+  static_assert(N <= G, "group_reduce needs N <= G");
+  if constexpr (N > 1) {
+    constexpr int off = G / 2;
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      const float send = upper ? v[i] : v[i + N / 2];
+      const float keep = upper ? v[i + N / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+    group_reduce<N / 2, off>(v, lane);
+  } else {
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+  }
+}
+
+// Which of the N original values a lane holds after group_reduce<N, G>.
+template <int N, int G>
+__device__ __forceinline__ int group_reduce_index(int lane) {
+  if constexpr (N > 1) {
+    constexpr int off = G / 2;
+    return ((lane & off) ? N / 2 : 0) + group_reduce_index<N / 2, off>(lane);
+  } else {
+    return 0;
+  }
+}
+
+// Lanes that hold a distinct result after group_reduce<N, G> (one per value).
+template <int N, int G>
+__device__ __forceinline__ bool group_reduce_writer(int lane) {
+  constexpr int rem = G / N;  // lanes sharing one result
+  return (lane & (rem - 1)) == 0;
+}
+
+// Warp-wide inclusive suffix scan over 64 entries held two per lane
+// (entry `lane` in x0, entry `lane + 32` in x1), combining with op.
+template <typename Op>
+__device__ __forceinline__ void suffix_scan64(float &x0, float &x1, int lane, Op op) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y0 = __shfl_down_sync(0xffffffffu, x0, off);
+    const float y1 = __shfl_down_sync(0xffffffffu, x1, off);
+    if (lane + off < 32) {
+      x0 = op(x0, y0);
+      x1 = op(x1, y1);
+    }
+  }
+  x0 = op(x0, __shfl_sync(0xffffffffu, x1, 0));
+}
+
+__device__ __forceinline__ void report(int32_t *dev_err, int bit) {
+  if (dev_err) atomicOr(dev_err, bit);
+}
+
+}  // namespace rs

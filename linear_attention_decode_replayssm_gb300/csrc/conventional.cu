@@ -1,0 +1,146 @@
+// Conventional load-update-store decode step (the baseline ReplaySSM is judged against).
+//
+// Sources:
+//   [Ghana] S. Ghana, "ReplaySSM: an SSM decoder that writes its state once
+//           every 16 tokens", §Why a fixed-size state is not cheap to decode
+//           (Mamba-2: S_t = alpha_t S_{t-1} + v_t k_t^T, o_t = S_t q_t; every
+//           step loads the state, updates it and stores it back) and §The
+//           delta-rule wrinkle (S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T)
+//           + beta_t v_t k_t^T, written as alpha_t S_{t-1} + u_t k_t^T with
+//           u_t = beta_t (v_t - alpha_t S_{t-1} k_t)).
+//
+// Same tiling and streaming loads as the ReplaySSM kernels, so the two differ
+// only in the bytes they move: this one reads and writes the whole state on
+// every step.
+#include "common.cuh"
+#include "launch.h"
+
+namespace rs {
+
+template <int DV, int DK, typename TC, int NT, bool DELTA>
+__global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
+  using V = CkVec<TC>;
+  constexpr int E = V::E;
+  constexpr int G = DK / E;
+  constexpr int RPP = NT / G;
+  constexpr int VPT = DV / RPP;
+  static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
+  static_assert(NT % G == 0 && DV % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
+
+  __shared__ float sK[DK], sQ[DK], sV[DV], sU[DV], sC[DV];
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int b = blockIdx.x / a.H;
+  const int h = blockIdx.x - b * a.H;
+  float *orow = a.out + (size_t)b * a.so + (size_t)h * DV;
+  const int slot = __ldg(a.slot_idx + b);
+  if (slot < 0) {
+    for (int i = tid; i < DV; i += NT) orow[i] = 0.f;
+    return;
+  }
+  if (slot >= a.num_slots) {
+    if (tid == 0) report(a.dev_err, 1);
+    for (int i = tid; i < DV; i += NT) orow[i] = 0.f;
+    return;
+  }
+  const size_t unit = (size_t)slot * a.H + h;
+  TC *st = static_cast<TC *>(a.ckpt) + unit * (size_t)(DV * DK);
+  const int row0 = tid / G, cv = tid - (tid / G) * G;
+
+  uint4 raw[VPT];
+#pragma unroll
+  for (int r = 0; r < VPT; ++r) raw[r] = ld_stream(st + (size_t)(row0 + r * RPP) * DK + cv * E);
+
+  for (int idx = tid; idx < DK / 8; idx += NT) {
+    float f[8], g[8];
+    load8(a.k, (size_t)b * a.sk + (size_t)h * DK + idx * 8, a.in_dtype, f);
+    load8(a.q, (size_t)b * a.sq + (size_t)h * DK + idx * 8, a.in_dtype, g);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sK[idx * 8 + e] = f[e];
+      sQ[idx * 8 + e] = g[e];
+    }
+  }
+  for (int idx = tid; idx < DV / 8; idx += NT) {
+    float f[8];
+    load8(a.v, (size_t)b * a.sv + (size_t)h * DV + idx * 8, a.in_dtype, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sV[idx * 8 + e] = f[e];
+  }
+  const float a_in = __ldg(a.alpha + (size_t)b * a.H + h);
+  const float alpha = DELTA ? expf(a_in) : a_in;
+  __syncthreads();
+
+  float kv[E], qv[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    kv[e] = sK[cv * E + e];
+    qv[e] = sQ[cv * E + e];
+  }
+  float f[VPT][E];
+#pragma unroll
+  for (int r = 0; r < VPT; ++r) V::unpack(raw[r], f[r]);
+
+  if (DELTA) {
+    // u = beta (v - alpha S k): needs the full row dot S k first
+    float part[VPT];
+#pragma unroll
+    for (int r = 0; r < VPT; ++r) {
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) s = fmaf(f[r][e], kv[e], s);
+      part[r] = s;
+    }
+    group_reduce<VPT, G>(part, lane);
+    if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
+    __syncthreads();
+    const float beta = __ldg(a.beta + (size_t)b * a.H + h);
+    for (int i = tid; i < DV; i += NT) sU[i] = beta * (sV[i] - alpha * sC[i]);
+    __syncthreads();
+  }
+
+  const float *upd = DELTA ? sU : sV;
+  float part[VPT];
+#pragma unroll
+  for (int r = 0; r < VPT; ++r) {
+    const float vv = upd[row0 + r * RPP];
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      f[r][e] = fmaf(alpha, f[r][e], vv * kv[e]);
+      s = fmaf(f[r][e], qv[e], s);
+    }
+    part[r] = s;
+    st_vec(st + (size_t)(row0 + r * RPP) * DK + cv * E, V::pack(f[r]));
+  }
+  group_reduce<VPT, G>(part, lane);
+  if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
+  __syncthreads();
+  for (int i = tid; i < DV; i += NT) orow[i] = sC[i];
+}
+
+template <int DV, int DK, typename TC, int NT, bool DELTA>
+static cudaError_t launch_conv(const KArgs &a, cudaStream_t s) {
+  conventional_kernel<DV, DK, TC, NT, DELTA><<<(unsigned)((size_t)a.B * a.H), NT, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <bool DELTA>
+static LaunchFn find_conv_t(int d_v, int d_k, int ckpt_dtype) {
+  if (ckpt_dtype == kF32) {
+    if (d_v == 16 && d_k == 32) return launch_conv<16, 32, float, 128, DELTA>;
+    if (d_v == 64 && d_k == 128) return launch_conv<64, 128, float, 256, DELTA>;
+    if (d_v == 128 && d_k == 128) return launch_conv<128, 128, float, 512, DELTA>;
+  } else if (ckpt_dtype == kF16) {
+    if (d_v == 16 && d_k == 32) return launch_conv<16, 32, __half, 64, DELTA>;
+    if (d_v == 64 && d_k == 128) return launch_conv<64, 128, __half, 256, DELTA>;
+    if (d_v == 128 && d_k == 128) return launch_conv<128, 128, __half, 256, DELTA>;
+  }
+  return nullptr;
+}
+
+LaunchFn find_conventional(int variant, int d_v, int d_k, int ckpt_dtype) {
+  return variant == 1 ? find_conv_t<true>(d_v, d_k, ckpt_dtype) : find_conv_t<false>(d_v, d_k, ckpt_dtype);
+}
+
+}  // namespace rs

@@ -1,0 +1,55 @@
+"""Algorithmic bytes of one decode-step launch (for the roofline figure).
+
+The count is what the step must move at minimum, per row of the batch:
+  every live row, every head:  the inputs v, k, q (+ alpha, + beta for GDN),
+                               the fp32 output row, and the state read once;
+  ReplaySSM:                   plus the p ring records the row holds, and then
+                               either one appended record (non-flush) or the
+                               state written once (flush);
+  conventional:                plus the state written back every step;
+  per row:                     slot index, cursor and flag (9 bytes);
+  padded rows:                 the slot index and a zero output row.
+A ring record is (d_v + d_k) ring elements plus the 4-byte decay/gate, the
+per-head record of "ReplaySSM: an SSM decoder that writes its state once every
+16 tokens", §The identity (2 d_v + 2 d_k + 4 bytes with 16-bit records).
+"""
+
+import numpy as np
+
+ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
+
+
+def step_bytes(*, variant, H, d_v, d_k, ckpt_dtype, in_dtype, ring_dtype, slot_idx, write_pos=None,
+               is_flush=None, replay=True):
+    """Bytes one launch moves for the given per-row cursors (NumPy arrays [B])."""
+    slot_idx = np.asarray(slot_idx)
+    live = slot_idx >= 0
+    n_live = int(live.sum())
+    n_pad = int((~live).sum())
+    state = d_v * d_k * ESIZE[ckpt_dtype]
+    io = (d_v + 2 * d_k) * ESIZE[in_dtype] + 4 + (4 if variant == "gdn" else 0) + 4 * d_v
+    meta = 4 + (5 if replay else 0)
+    total = n_live * (H * (state + io) + meta) + n_pad * (4 + H * 4 * d_v)
+    if not replay:
+        return total + n_live * H * state
+    rec = (d_v + d_k) * ESIZE[ring_dtype] + 4
+    p = np.asarray(write_pos, dtype=np.int64)[live]
+    fl = np.asarray(is_flush)[live] != 0
+    total += int(p.sum()) * H * rec
+    total += int(fl.sum()) * H * state + int((~fl).sum()) * H * rec
+    return total
+
+
+def step_flops(*, variant, H, d_v, d_k, slot_idx, write_pos=None, is_flush=None, replay=True):
+    """Floating-point operations of one launch (multiply-add = 2), for context."""
+    live = np.asarray(slot_idx) >= 0
+    mn = d_v * d_k
+    if not replay:
+        per = (5 if variant == "mamba2" else 7) * mn
+        return int(live.sum()) * H * per
+    p = np.asarray(write_pos, dtype=np.int64)[live]
+    fl = np.asarray(is_flush)[live] != 0
+    dots = 2 if variant == "gdn" else 1
+    nonflush = dots * 2 * mn + (p + 1) * (2 * d_k * dots + 2 * d_v * dots)
+    flush = 2 * mn + (p + 1) * 2 * mn + 2 * mn + (2 * mn if variant == "gdn" else 0)
+    return int(H * np.where(fl, flush, nonflush).sum())
