@@ -320,13 +320,14 @@ def _timed_graph(torch, fn, t0, t1, stream, eager, dist, sampler):
     if dist is not None:
         dist.barrier()
     w0 = time.time()
-    start.record(stream)
-    if graph is not None:
-        graph.replay()
-    else:
-        for t in range(t0, t1):
-            fn(t, stream)
-    end.record(stream)
+    with torch.cuda.stream(stream):  # graph.replay() launches on the current stream
+        start.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            for t in range(t0, t1):
+                fn(t, stream)
+        end.record(stream)
     end.synchronize()
     torch.cuda.synchronize()
     w1 = time.time()

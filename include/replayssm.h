@@ -81,7 +81,10 @@ typedef enum { RS_MAMBA2 = 0, RS_GDN = 1 } rs_variant;
 /* Bits the kernels OR into *dev_err. */
 typedef enum {
   RS_DERR_SLOT = 1,      /* slot_idx[b] >= num_slots */
-  RS_DERR_WRITE_POS = 2  /* write_pos[b] outside [0, L) */
+  RS_DERR_WRITE_POS = 2, /* write_pos[b] outside [0, L) */
+  RS_DERR_TIMEOUT = 4    /* a pipeline wait gave up after 2 s: outputs of the
+                            call are incomplete (never expected; reported
+                            instead of hanging the GPU) */
 } rs_dev_error;
 
 /*

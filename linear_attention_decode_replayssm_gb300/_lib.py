@@ -19,7 +19,7 @@ from . import build as _build
 RS_OK, RS_EINVAL, RS_EUNSUPPORTED, RS_EALIGN, RS_ECUDA = 0, -1, -2, -3, -4
 RS_F32, RS_F16, RS_BF16 = 0, 1, 2
 RS_MAMBA2, RS_GDN = 0, 1
-RS_DERR_SLOT, RS_DERR_WRITE_POS = 1, 2
+RS_DERR_SLOT, RS_DERR_WRITE_POS, RS_DERR_TIMEOUT = 1, 2, 4
 RS_ABI_VERSION = 1
 RS_MAX_L = 64
 

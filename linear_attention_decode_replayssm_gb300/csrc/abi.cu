@@ -1,12 +1,16 @@
 // C ABI of libreplayssm.so: argument validation, the host step plan and
 // dispatch to the kernels.  Declarations and their documentation are in
 // include/replayssm.h.
+#include <map>
 #include <mutex>
 #include <set>
+#include <tuple>
 #include <utility>
 
 #include "../../include/replayssm.h"
 #include "launch.h"
+
+#include <algorithm>
 
 namespace rs {
 
@@ -27,6 +31,80 @@ cudaError_t ensure_smem(const void *kernel, size_t bytes) {
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
   if (e == cudaSuccess) done.insert({dev, kernel});
   return e;
+}
+
+namespace {
+
+struct DevInfo {
+  int sms = 0, smem_sm = 0, smem_block = 0;
+};
+
+cudaError_t dev_info(int dev, DevInfo *out) {
+  static std::mutex mu;
+  static std::map<int, DevInfo> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  DevInfo d;
+  cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.smem_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  cache[dev] = d;
+  *out = d;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t plan_pipe(const void *kernel, int threads, size_t stage_bytes, HeadFn head, int max_stages, int units,
+                      PipePlan *out) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void *, size_t>, PipePlan> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_tuple(dev, kernel, stage_bytes);
+  PipePlan plan{};
+  bool hit = false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      plan = it->second;
+      hit = true;
+    }
+  }
+  if (!hit) {
+    DevInfo d;
+    e = dev_info(dev, &d);
+    if (e != cudaSuccess) return e;
+    int ctas = 0, ns = 0;
+    for (int c = 2; c >= 1 && ns < 2; --c) {
+      const long budget = std::min<long>(d.smem_sm / c - 1024, d.smem_block);
+      const long n = (budget - (long)head(max_stages)) / (long)stage_bytes;
+      ns = (int)std::min<long>(n, max_stages);
+      ctas = c;
+    }
+    if (ns < 2) return cudaErrorInvalidValue;  // one stage would not overlap copies with compute
+    plan.nstage = ns;
+    plan.smem = head(ns) + (size_t)ns * stage_bytes;
+    e = ensure_smem(kernel, plan.smem);
+    if (e != cudaSuccess) return e;
+    int fit = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kernel, threads, plan.smem);
+    if (e != cudaSuccess) return e;
+    if (fit < 1) return cudaErrorInvalidConfiguration;
+    plan.grid = (unsigned)(d.sms * std::min(ctas, fit));
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = plan;
+  }
+  plan.grid = std::min<unsigned>(plan.grid, (unsigned)units);
+  *out = plan;
+  return cudaSuccess;
 }
 
 }  // namespace rs

@@ -223,3 +223,128 @@ __device__ __forceinline__ void report(int32_t *dev_err, int bit) {
 }
 
 }  // namespace rs
+
+// ---------------------------------------------------------------------------
+// Bulk-copy (TMA) pipeline primitives: mbarriers in shared memory, 1-D
+// cp.async.bulk global -> shared with transaction-count completion, and waits
+// bounded by the global timer so a lost arrival ends in an error code instead
+// of a hung GPU.
+// ---------------------------------------------------------------------------
+namespace rs {
+
+constexpr int kDerrTimeout = 4;                       // RS_DERR_TIMEOUT
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// make barrier initialisation visible to the async (bulk copy) proxy
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the barrier phase with the given parity; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` on the barrier's
+// transaction count.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_addr(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// barrier among the consumer warps only (the producer warp does not take part)
+template <int NTHREADS>
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
+}
+
+// widen E consecutive 16-bit or fp32 elements from shared memory
+template <int E>
+__device__ __forceinline__ void lds_cols(const unsigned char *base, int elem, int dt, float (&f)[E]) {
+  if (dt == kF32) {
+    const float4 *p = reinterpret_cast<const float4 *>(base + (size_t)elem * 4);
+#pragma unroll
+    for (int i = 0; i < E / 4; ++i) {
+      const float4 x = p[i];
+      f[4 * i] = x.x; f[4 * i + 1] = x.y; f[4 * i + 2] = x.z; f[4 * i + 3] = x.w;
+    }
+  } else {
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(base + (size_t)elem * 2);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      const uint32_t w = p[i];
+      if (dt == kBF16) {
+        bf16x2_to_f(w, f[2 * i], f[2 * i + 1]);
+      } else {
+        const float2 x = CkVec<__half>::h2f(w);
+        f[2 * i] = x.x; f[2 * i + 1] = x.y;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float lds_elem(const unsigned char *base, int elem, int dt) {
+  if (dt == kF32) return reinterpret_cast<const float *>(base)[elem];
+  const uint16_t h = reinterpret_cast<const uint16_t *>(base)[elem];
+  if (dt == kBF16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  return __half2float(__ushort_as_half(h));
+}
+
+}  // namespace rs

@@ -6,8 +6,16 @@ head's vector or matrix)):
     the inputs verbatim, so only fp32 arithmetic order differs).
   * fp16 checkpoint: 2e-2 against the exact recurrence, and 2e-3 against the
     storage-emulating oracle (same roundings as the method).
-  * Gated DeltaNet with fp16 d/k rings: 1e-4 against the storage-emulating
-    oracle (the fp16 d ring alone moves outputs by ~1e-3 against exact).
+  * Gated DeltaNet with an fp32 ring: 1e-4 against the exact recurrence (the
+    arithmetic of the GDN kernel at fp32 accuracy).
+  * Gated DeltaNet with fp16 d/k rings, against the storage-emulating oracle:
+    the corrected value d_t is computed (fp32 on the GPU, fp64 in the oracle)
+    and then rounded to fp16, so where d_t lies near an fp16 rounding midpoint
+    the two sides store codes one ulp apart, and later outputs of the window
+    inherit that difference: up to ~|k_c| * ulp(d) / rms, about 5e-4 relative
+    on a checkpoint element.  The gate is the pages' own fp32 tolerance (the
+    vLLM PR's tests: output rtol = atol = 1e-4, state rtol 1e-3 / atol 2e-3),
+    plus a max relative error of 2e-3 derived from one fp16 ulp.
   * Cursors, flags, Mamba-2 ring records, GDN key and gate records: bit-exact.
     GDN corrected values (fp16, rounded on both sides from slightly different
     fp32/fp64 values): within one fp16 rounding, 1e-3.
@@ -27,6 +35,9 @@ TOL_F32 = 1e-4
 TOL_F16 = 2e-2
 TOL_F16_EMU = 2e-3
 TOL_D_RING = 1e-3
+TOL_F16_RING = 2e-3            # derived bound for GDN with fp16 d/k rings
+PR_OUT = (1e-4, 1e-4)          # (rtol, atol) on outputs
+PR_STATE = (1e-3, 2e-3)        # (rtol, atol) on the checkpoint
 
 
 @pytest.fixture(scope="module")
@@ -47,7 +58,7 @@ def run_parity(lib, w, steps, heads=None, replay=True, exact=True, conventional=
                   exact_state_dtype=exact_state_dtype)
     hs = o.heads
     hs_t = torch.as_tensor(hs, device="cuda")
-    res = dict(o_exact=0.0, o_replay=0.0, ck_exact=0.0, ck_replay=0.0, flush_rows=0)
+    res = dict(o_exact=0.0, o_replay=0.0, ck_exact=0.0, ck_replay=0.0, flush_rows=0, pr_out=0.0, pr_state=0.0)
     for t in range(steps):
         x = w.inputs(t)
         ds = w.decode_step(t)
@@ -64,6 +75,7 @@ def run_parity(lib, w, steps, heads=None, replay=True, exact=True, conventional=
             res["o_exact"] = max(res["o_exact"], rel_err(og, o_e))
         if o_r is not None:
             res["o_replay"] = max(res["o_replay"], rel_err(og, o_r))
+            res["pr_out"] = max(res["pr_out"], _allclose_excess(og, o_r, *PR_OUT))
         flushed = (fl != 0) & ~pad
         if conventional:
             flushed = ~pad
@@ -75,10 +87,29 @@ def run_parity(lib, w, steps, heads=None, replay=True, exact=True, conventional=
                 res["ck_exact"] = max(res["ck_exact"], rel_err(ck, o.ex.S[slots], nd=2))
             if o.rs is not None:
                 res["ck_replay"] = max(res["ck_replay"], rel_err(ck, o.rs.ckpt[slots], nd=2))
+                res["pr_state"] = max(res["pr_state"], _allclose_excess(ck, o.rs.ckpt[slots], *PR_STATE))
     assert int(g.dev_err.item()) == 0
     if check_rings and not conventional and o.rs is not None:
         res["ring"] = compare_rings(g, o, w, steps)
     return res
+
+
+def same_bits(a, b):
+    """Bitwise tensor equality (NaN-poisoned stale ring slots compare equal)."""
+    import torch
+
+    ints = {4: torch.int32, 2: torch.int16, 1: torch.uint8}
+    return torch.equal(a.view(ints[a.element_size()]), b.view(ints[b.element_size()]))
+
+
+def _allclose_excess(x, y, rtol, atol):
+    """max(|x - y| - rtol |y|) / atol: <= 1 exactly when allclose(x, y, rtol, atol)."""
+    return float(np.max(np.abs(x - y) - rtol * np.abs(y)) / atol) if np.size(y) else 0.0
+
+
+def assert_gdn_f16_ring(r):
+    assert r["pr_out"] <= 1.0 and r["pr_state"] <= 1.0, r
+    assert r["o_replay"] <= TOL_F16_RING and r["ck_replay"] <= TOL_F16_RING, r
 
 
 def compare_rings(g, o, w, steps):
@@ -174,8 +205,7 @@ def test_mamba2_bs256_full_size_sampled(cuda):
 def test_tiny_gdn(cuda):
     w = synth.make_workload("tiny", variant="gdn", ring_dtype="f16", alpha_mu=3.0, alpha_sd=1.0)
     r = run_parity(cuda, w, w.steps)
-    assert r["o_replay"] <= TOL_F32, r
-    assert r["ck_replay"] <= TOL_F32, r
+    assert_gdn_f16_ring(r)
 
 
 def test_gdn_fp32_ring_matches_exact(cuda):
@@ -190,7 +220,7 @@ def test_gdn_paged_padded(cuda, ckpt_dtype):
                             ckpt_dtype=ckpt_dtype, seed=11)
     r = run_parity(cuda, w, w.steps)
     if ckpt_dtype == "f32":
-        assert r["o_replay"] <= TOL_F32 and r["ck_replay"] <= TOL_F32, r
+        assert_gdn_f16_ring(r)
     else:
         assert r["o_exact"] <= TOL_F16 and r["o_replay"] <= TOL_F16_EMU, r
 
@@ -199,7 +229,10 @@ def test_gdn_paged_padded(cuda, ckpt_dtype):
 def test_gdn_buffer_lengths(cuda, L):
     w = synth.make_workload("gdn_bs256", B=3, H=2, L=L, steps=2 * L + 1, seed=L)
     r = run_parity(cuda, w, w.steps)
-    assert r["o_replay"] <= TOL_F32, r
+    assert_gdn_f16_ring(r)
+    w32 = synth.make_workload("gdn_bs256", B=3, H=2, L=L, steps=2 * L + 1, seed=L, ring_dtype="f32")
+    r32 = run_parity(cuda, w32, w32.steps)
+    assert r32["o_exact"] <= TOL_F32 and r32["ck_exact"] <= TOL_F32, r32
 
 
 def test_gdn_bs256_full_size_sampled(cuda):
@@ -207,8 +240,8 @@ def test_gdn_bs256_full_size_sampled(cuda):
     # fp32 g ring, L = 16 staggered, 256 steps; the oracle follows two heads
     w = synth.make_workload("gdn_bs256")
     r = run_parity(cuda, w, w.steps, heads=[0, 31], exact=False)
-    assert r["o_replay"] <= TOL_F32, r
-    assert r["ck_replay"] <= TOL_F32, r
+    assert_gdn_f16_ring(r)
+    assert r["flush_rows"] == 256 * 16
 
 
 # --------------------------------------------------------------------------
@@ -220,8 +253,12 @@ def test_conventional(cuda, variant, ckpt_dtype):
     name = "mamba2_bs256" if variant == "mamba2" else "gdn_bs256"
     w = synth.make_workload(name, B=5, H=3, steps=30, ckpt_dtype=ckpt_dtype, num_slots=8, permute_slots=True,
                             pad_rows=1, stagger=False, seed=13)
+    # the oracle rounds the state to its storage type after every step, as the
+    # kernel does; with an fp16 state the two sides' roundings diverge on
+    # near-midpoint elements and compound step by step, so that case takes the
+    # fp16-state tolerance
     r = run_parity(cuda, w, w.steps, conventional=True, exact_state_dtype=ckpt_dtype)
-    tol = TOL_F32 if ckpt_dtype == "f32" else TOL_F16_EMU
+    tol = TOL_F32 if ckpt_dtype == "f32" else TOL_F16
     assert r["o_exact"] <= tol and r["ck_exact"] <= tol, r
 
 
@@ -263,7 +300,7 @@ def test_device_range_checks(cuda):
     assert int(g.dev_err.item()) == lib.RS_DERR_WRITE_POS
     assert torch.all(g.out[2] == 0)
     s2 = int(w.slot_idx[2])
-    assert torch.equal(g.ckpt[s2], ck0[s2]) and torch.equal(g.ring_a[s2], ra0[s2])
+    assert same_bits(g.ckpt[s2], ck0[s2]) and same_bits(g.ring_a[s2], ra0[s2])
 
 
 def test_strided_rows_match_packed(cuda):
@@ -317,5 +354,5 @@ def test_cuda_graph_replay_matches_eager(cuda):
     for t in range(w.steps):
         o_e, _, _ = eager.step(w.inputs(t), w.decode_step(t))
         np.testing.assert_array_equal(outs[t].double().cpu().numpy(), o_e)
-    assert torch.equal(eager.ckpt, graphed.ckpt)
-    assert torch.equal(eager.ring_v, graphed.ring_v)
+    for name in ("ckpt", "ring_v", "ring_k", "ring_a"):
+        assert same_bits(getattr(eager, name), getattr(graphed, name)), name
