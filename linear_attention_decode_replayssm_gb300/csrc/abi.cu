@@ -7,7 +7,7 @@
 #include <tuple>
 #include <utility>
 
-#include "../../include/replayssm.h"
+#include "replayssm.h"
 #include "launch.h"
 
 #include <algorithm>
@@ -60,8 +60,8 @@ cudaError_t dev_info(int dev, DevInfo *out) {
 
 }  // namespace
 
-cudaError_t plan_pipe(const void *kernel, int threads, size_t stage_bytes, HeadFn head, int max_stages, int units,
-                      PipePlan *out) {
+cudaError_t plan_pipe(const void *kernel, int threads, size_t stage_bytes, HeadFn head, int max_stages,
+                      int ctas_per_sm, int units, PipePlan *out) {
   static std::mutex mu;
   static std::map<std::tuple<int, const void *, size_t>, PipePlan> cache;
   int dev = 0;
@@ -83,7 +83,7 @@ cudaError_t plan_pipe(const void *kernel, int threads, size_t stage_bytes, HeadF
     e = dev_info(dev, &d);
     if (e != cudaSuccess) return e;
     int ctas = 0, ns = 0;
-    for (int c = 2; c >= 1 && ns < 2; --c) {
+    for (int c = ctas_per_sm; c >= 1 && ns < 2; --c) {
       const long budget = std::min<long>(d.smem_sm / c - 1024, d.smem_block);
       const long n = (budget - (long)head(max_stages)) / (long)stage_bytes;
       ns = (int)std::min<long>(n, max_stages);
@@ -92,6 +92,60 @@ cudaError_t plan_pipe(const void *kernel, int threads, size_t stage_bytes, HeadF
     if (ns < 2) return cudaErrorInvalidValue;  // one stage would not overlap copies with compute
     plan.nstage = ns;
     plan.smem = head(ns) + (size_t)ns * stage_bytes;
+    e = ensure_smem(kernel, plan.smem);
+    if (e != cudaSuccess) return e;
+    int fit = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kernel, threads, plan.smem);
+    if (e != cudaSuccess) return e;
+    if (fit < 1) return cudaErrorInvalidConfiguration;
+    plan.grid = (unsigned)(d.sms * std::min(ctas, fit));
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = plan;
+  }
+  plan.grid = std::min<unsigned>(plan.grid, (unsigned)units);
+  *out = plan;
+  return cudaSuccess;
+}
+
+cudaError_t plan_rings(const void *kernel, int threads, size_t ck_bytes, size_t rec_bytes, RingHeadFn head,
+                       int units, RingPlan *out) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void *, size_t, size_t>, RingPlan> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_tuple(dev, kernel, ck_bytes, rec_bytes);
+  RingPlan plan{};
+  bool hit = false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      plan = it->second;
+      hit = true;
+    }
+  }
+  if (!hit) {
+    DevInfo d;
+    e = dev_info(dev, &d);
+    if (e != cudaSuccess) return e;
+    auto need = [&](int nsr, int nsc) { return (size_t)head(nsr, nsc) + nsc * ck_bytes + nsr * rec_bytes; };
+    // preferred shapes, best first: two CTAs per SM each with two
+    // checkpoint slots (two producers per SM keep bulk-copy issue off the
+    // critical path), then one CTA per SM with fewer or more slots
+    static const int shapes[][3] = {{2, 2, 4}, {2, 2, 3}, {1, 4, 8}, {1, 3, 6}, {1, 2, 4}, {1, 2, 3}, {1, 1, 2}};
+    int ctas = 0;
+    for (const auto &sh : shapes) {
+      const size_t budget = (size_t)std::min<long>(d.smem_sm / sh[0] - 1024, d.smem_block);
+      if (need(sh[2], sh[1]) <= budget) {
+        ctas = sh[0];
+        plan.nsc = sh[1];
+        plan.nsr = sh[2];
+        break;
+      }
+    }
+    if (!ctas) return cudaErrorInvalidValue;
+    plan.smem = need(plan.nsr, plan.nsc);
     e = ensure_smem(kernel, plan.smem);
     if (e != cudaSuccess) return e;
     int fit = 0;
@@ -201,7 +255,7 @@ int replayssm_abi_version(void) { return RS_ABI_VERSION; }
 
 int replayssm_supported(int variant, int d_v, int d_k, int ckpt_dtype) {
   if (variant != RS_MAMBA2 && variant != RS_GDN) return 0;
-  if (variant == RS_MAMBA2) return rs::find_mamba2(d_v, d_k, ckpt_dtype) != nullptr;
+  if (variant == RS_MAMBA2) return rs::find_mamba2(d_v, d_k, ckpt_dtype, RS_BF16) != nullptr;
   return rs::find_gdn(d_v, d_k, ckpt_dtype) != nullptr;
 }
 
@@ -223,7 +277,7 @@ int replayssm_plan_step(const int64_t *decode_step, const uint8_t *force_flush, 
 int replayssm_decode_mamba2(const rs_step_args *args, rs_stream_t stream) {
   const int st = validate(args, /*replay=*/true, /*gdn=*/false);
   if (st != RS_OK || args->B == 0) return st;
-  return run(rs::find_mamba2(args->d_v, args->d_k, args->ckpt_dtype), args, stream);
+  return run(rs::find_mamba2(args->d_v, args->d_k, args->ckpt_dtype, args->in_dtype), args, stream);
 }
 
 int replayssm_decode_gdn(const rs_step_args *args, rs_stream_t stream) {

@@ -15,17 +15,21 @@
 //   flush:     S_new = gamma * S_ckpt + sum_{j<=p} w_j v_j k_j^T, o = S_new q
 //              from the fp32 registers, S_new stored (cast) over S_ckpt.
 //
-// Persistent, warp-specialised kernel.  One producer warp streams each unit's
-// checkpoint, ring records and inputs into a ring of shared-memory stages with
-// 1-D bulk copies (cp.async.bulk, completion counted on an mbarrier); the
-// decays come in with 4-byte cp.async.  The per-row slot, cursor and flag are
-// prefetched 32 units ahead by the producer's lanes, so no dependent global
-// load sits on the streaming path.  Eight consumer warps wait on a stage,
-// compute from shared memory and release it.  The units a CTA owns are
+// Persistent, warp-specialised kernel, two CTAs per SM.  A producer warp
+// streams each unit's checkpoint into a checkpoint slot with one 1-D bulk
+// copy (cp.async.bulk, completion counted on an mbarrier) and its ring
+// records, this token's k, v, q and the decays into a record slot with
+// per-lane cp.async.  It prefetches the per-row slot, cursor and flag 32
+// units ahead, so no dependent global load sits on the streaming path.
+// Eight consumer warps wait for a unit, take their share of the checkpoint
+// into registers (freeing that slot for the next load at once), compute from
+// the record slot and release it.  The units a CTA owns are
 // strided across the batch, so the ~1/L flush rows (which also write their
 // state) spread evenly over the CTAs.  Every wait is bounded: on a timeout
 // the kernel reports RS_DERR_TIMEOUT, drains its own copies and returns.
 // No tensor cores: the step is a bandwidth-bound GEMV (about 0.6 FLOP/byte).
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -34,6 +38,10 @@ namespace rs {
 namespace {
 
 constexpr int kStatusOk = 0, kStatusPad = 1, kStatusBadSlot = 2, kStatusBadPos = 3;
+
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
 
 __device__ __forceinline__ void cp_async4(void *dst_smem, const void *src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
@@ -44,26 +52,24 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ void bulk_load_plain(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_addr(dst_smem)),
-               "l"(src), "r"(bytes), "r"(smem_addr(bar))
-               : "memory");
-}
 
 }  // namespace
 
-// Byte offsets of one pipeline stage (host and device agree on this layout).
-struct M2Stage {
-  uint32_t ck, k, v, q, a, meta, scr, bytes;
+// Shared memory holds two rings: checkpoint slots (the 32 KiB-class state
+// block of a unit, released as soon as the consumers hold it in registers)
+// and record slots (ring records, query, decays, per-unit metadata and
+// scratch, released when the unit is done).  Small record slots are cheap, so
+// there are more of them, and the checkpoint slots turn over at the speed of
+// the memory system rather than of the arithmetic.
+struct M2Rec {
+  uint32_t k, v, q, a, meta, scr, bytes;
 };
 
 __host__ __device__ inline uint32_t align128(uint32_t x) { return (x + 127u) & ~127u; }
 
-__host__ __device__ inline M2Stage m2_stage(int DV, int DK, int ck_es, int rec_es, int L) {
-  M2Stage s;
+__host__ __device__ inline M2Rec m2_rec(int DV, int DK, int rec_es, int L) {
+  M2Rec s;
   uint32_t o = 0;
-  s.ck = o;   o = align128(o + DV * DK * ck_es);
   s.k = o;    o = align128(o + L * DK * rec_es);   // records 0..p, current token at p
   s.v = o;    o = align128(o + L * DV * rec_es);
   s.q = o;    o = align128(o + DK * rec_es);
@@ -74,47 +80,67 @@ __host__ __device__ inline M2Stage m2_stage(int DV, int DK, int ck_es, int rec_e
   return s;
 }
 
-// barriers (full[ns], empty[ns]) and the abort flag precede the stages
-__host__ __device__ inline uint32_t m2_head(int nstage) { return align128(16 * nstage + 16); }
+// barriers full/rec_empty[nsr], ck_empty[nsc] and the abort flag
+__host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(8 * (2 * nsr + nsc) + 16); }
 
-template <int DV, int DK, typename TC, int NCW>
-__global__ void __launch_bounds__(NCW * 32 + 32) mamba2_replay_kernel(const KArgs a, int nstage) {
+// Element type of the ring records and inputs (they are the same for Mamba-2).
+template <typename RT>
+struct Rec;
+template <>
+struct Rec<float> {
+  static constexpr int kDtype = kF32;
+};
+template <>
+struct Rec<__nv_bfloat16> {
+  static constexpr int kDtype = kBF16;
+};
+
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP>
+__global__ void __launch_bounds__(NGRP * NCW * 32 + 32) mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr int E = V::E;
   constexpr int G = DK / E;          // lanes per state row
-  constexpr int NC = NCW * 32;       // consumer threads
-  constexpr int RPP = NC / G;        // state rows per pass of the consumers
+  constexpr int NC = NCW * 32;       // consumer threads per group
+  constexpr int RPP = NC / G;        // state rows per pass of a group
   constexpr int VPT = DV / RPP;      // state rows per consumer thread
+  constexpr int RPW = DV / NCW;      // output rows per warp in the output phase
+  constexpr int JG = 32 / RPW;       // lanes sharing one output row (split over records)
+  constexpr int RDT = Rec<RT>::kDtype;
+  constexpr int RES = (int)sizeof(RT);
+  constexpr int PROD = NGRP * NCW;   // warp index of the producer
+  constexpr uint32_t CKB = DV * DK * (uint32_t)sizeof(TC);
   static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && DV % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
+  static_assert(DV % NCW == 0 && 32 % RPW == 0 && JG >= 1, "bad output tiling");
   static_assert(DK % 8 == 0 && DV % 8 == 0, "head dims must be multiples of 8");
 
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-  uint64_t *empty = full + nstage;
-  int *s_abort = reinterpret_cast<int *>(smem + 16 * nstage);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // per record slot: all bytes of a unit landed
+  uint64_t *rec_empty = full + nsr;                     // per record slot: the unit is done
+  uint64_t *ck_empty = rec_empty + nsr;                 // per checkpoint slot: consumers hold it in registers
+  int *s_abort = reinterpret_cast<int *>(ck_empty + nsc);
   const int L = a.L;
-  const int rdt = a.in_dtype;  // records are the inputs verbatim
-  const int res = rdt == kF32 ? 4 : 2;
-  const M2Stage lay = m2_stage(DV, DK, (int)sizeof(TC), res, L);
-  unsigned char *stages = smem + m2_head(nstage);
+  const M2Rec lay = m2_rec(DV, DK, RES, L);
+  unsigned char *ck_slots = smem + m2_head(nsr, nsc);
+  unsigned char *rec_slots = ck_slots + (size_t)nsc * CKB;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_units = a.B * a.H;
   const int stride = gridDim.x;
 
   if (tid == 0) {
-    for (int s = 0; s < nstage; ++s) {
-      mbar_init(&full[s], 33);   // 32 producer-lane cp.async arrivals + 1 expect_tx
-      mbar_init(&empty[s], NC);  // every consumer thread
+    for (int s = 0; s < nsr; ++s) {
+      mbar_init(&full[s], 33);       // 32 producer-lane cp.async arrivals + lane 0 (+ bulk bytes)
+      mbar_init(&rec_empty[s], NC);  // every thread of the consuming group
     }
+    for (int c = 0; c < nsc; ++c) mbar_init(&ck_empty[c], NC);
     *s_abort = 0;
     mbar_init_fence();
   }
   __syncthreads();
 
-  if (warp == NCW) {
-    // ---------------------------------------------------------------- producer
+  if (warp == PROD) {
+    // ----------------------------------------------------------------- producer
     const uint64_t pol_stream = policy_evict_first();
     int it = 0;
     auto fetch = [&](int ub, int &sl, int &wp, int &fl) {
@@ -140,11 +166,13 @@ __global__ void __launch_bounds__(NCW * 32 + 32) mamba2_replay_kernel(const KArg
         const int slot = __shfl_sync(0xffffffffu, c_sl, j);
         const int p = __shfl_sync(0xffffffffu, c_wp, j);
         const int fl = __shfl_sync(0xffffffffu, c_fl, j);
-        const int s = it % nstage;
-        const uint32_t par = (uint32_t)(it / nstage) & 1u;
-        if (it >= nstage) {
+        const int s = it % nsr, c = it % nsc;
+        if (it >= nsr || it >= nsc) {
           int w = 1;
-          if (lane == 0) w = mbar_wait(&empty[s], par ^ 1u) ? 1 : 0;
+          if (lane == 0) {
+            if (it >= nsr) w = mbar_wait(&rec_empty[s], ((uint32_t)(it / nsr) & 1u) ^ 1u) ? 1 : 0;
+            if (w && it >= nsc) w = mbar_wait(&ck_empty[c], ((uint32_t)(it / nsc) & 1u) ^ 1u) ? 1 : 0;
+          }
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w || *(volatile int *)s_abort) {
             if (lane == 0) *(volatile int *)s_abort = 1;
@@ -153,42 +181,48 @@ __global__ void __launch_bounds__(NCW * 32 + 32) mamba2_replay_kernel(const KArg
           }
         }
         __syncwarp();
-        unsigned char *st = stages + (size_t)s * lay.bytes;
         const int b = u / a.H, h = u - (u / a.H) * a.H;
         const int status = slot < 0 ? kStatusPad
                            : slot >= a.num_slots ? kStatusBadSlot
                            : (p < 0 || p >= L) ? kStatusBadPos
                            : kStatusOk;
+        unsigned char *st = rec_slots + (size_t)s * lay.bytes;
+        int *meta = reinterpret_cast<int *>(st + lay.meta);
         if (status == kStatusOk) {
+          // The checkpoint, the only large operand, is one bulk copy from lane
+          // 0.  The small pieces -- ring records, this token's k, v, q and the
+          // decays -- go as 16- and 4-byte cp.async over the 32 lanes: a bulk
+          // copy carries a fixed cost of ~0.2 us that five small copies per
+          // unit would pay five times.
           const size_t unit = (size_t)slot * a.H + h;
+          if (lane == 0) {
+            meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
+            mbar_expect_tx(&full[s], CKB);
+            bulk_load(ck_slots + (size_t)c * CKB, static_cast<const TC *>(a.ckpt) + unit * (DV * DK), CKB,
+                      &full[s], pol_stream);
+          }
+          constexpr uint32_t kb = DK * RES, vb = DV * RES;
+          constexpr int KC = kb / 16, VC = vb / 16;  // 16-byte chunks per k / v record
+          const unsigned char *rk = static_cast<const unsigned char *>(a.ring_k) + unit * L * kb;
+          const unsigned char *rv = static_cast<const unsigned char *>(a.ring_v) + unit * L * vb;
+          const unsigned char *kin =
+              static_cast<const unsigned char *>(a.k) + ((size_t)b * a.sk + (size_t)h * DK) * RES;
+          const unsigned char *vin =
+              static_cast<const unsigned char *>(a.v) + ((size_t)b * a.sv + (size_t)h * DV) * RES;
+          const unsigned char *qin =
+              static_cast<const unsigned char *>(a.q) + ((size_t)b * a.sq + (size_t)h * DK) * RES;
+          for (int cc = lane; cc < (p + 1) * KC; cc += 32)
+            cp_async16(st + lay.k + cc * 16, (cc < p * KC ? rk + cc * 16 : kin + (cc - p * KC) * 16));
+          for (int cc = lane; cc < (p + 1) * VC; cc += 32)
+            cp_async16(st + lay.v + cc * 16, (cc < p * VC ? rv + cc * 16 : vin + (cc - p * VC) * 16));
+          for (int cc = lane; cc < KC; cc += 32) cp_async16(st + lay.q + cc * 16, qin + cc * 16);
           float *sa = reinterpret_cast<float *>(st + lay.a);
           for (int jj = lane; jj < p; jj += 32) cp_async4(sa + jj, a.ring_a + unit * L + jj);
-          if (lane == 0) cp_async4(sa + p, a.alpha + (size_t)b * a.H + h);
-          if (lane == 0) {
-            int *meta = reinterpret_cast<int *>(st + lay.meta);
-            meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
-            const uint32_t ckb = DV * DK * (uint32_t)sizeof(TC);
-            const uint32_t kb = DK * res, vb = DV * res;
-            mbar_arrive_expect_tx(&full[s], ckb + (uint32_t)(p + 1) * (kb + vb) + kb);
-            bulk_load(st + lay.ck, static_cast<const TC *>(a.ckpt) + unit * (DV * DK), ckb, &full[s], pol_stream);
-            if (p > 0) {
-              bulk_load_plain(st + lay.k, static_cast<const unsigned char *>(a.ring_k) + unit * L * kb,
-                              (uint32_t)p * kb, &full[s]);
-              bulk_load_plain(st + lay.v, static_cast<const unsigned char *>(a.ring_v) + unit * L * vb,
-                              (uint32_t)p * vb, &full[s]);
-            }
-            const unsigned char *kin = static_cast<const unsigned char *>(a.k);
-            const unsigned char *vin = static_cast<const unsigned char *>(a.v);
-            const unsigned char *qin = static_cast<const unsigned char *>(a.q);
-            bulk_load_plain(st + lay.k + p * kb, kin + ((size_t)b * a.sk + (size_t)h * DK) * res, kb, &full[s]);
-            bulk_load_plain(st + lay.v + p * vb, vin + ((size_t)b * a.sv + (size_t)h * DV) * res, vb, &full[s]);
-            bulk_load_plain(st + lay.q, qin + ((size_t)b * a.sq + (size_t)h * DK) * res, kb, &full[s]);
-          }
+          if (lane == 31) cp_async4(sa + p, a.alpha + (size_t)b * a.H + h);
         } else if (lane == 0) {
-          int *meta = reinterpret_cast<int *>(st + lay.meta);
           meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
-          mbar_arrive(&full[s]);
         }
+        if (lane == 0) mbar_arrive(&full[s]);  // releases the meta words
         cp_async_arrive(&full[s]);
         ++it;
       }
@@ -196,24 +230,31 @@ __global__ void __launch_bounds__(NCW * 32 + 32) mamba2_replay_kernel(const KArg
     }
     // drain: every copy this warp issued has landed before the CTA may exit
     if (lane == 0) {
-      for (int k = it > nstage ? it - nstage : 0; k < it; ++k) mbar_wait(&full[k % nstage], (uint32_t)(k / nstage) & 1u);
+      for (int k = it > nsr ? it - nsr : 0; k < it; ++k) mbar_wait(&full[k % nsr], (uint32_t)(k / nsr) & 1u);
     }
     __syncwarp();
     return;
   }
 
   // ------------------------------------------------------------------ consumers
-  const int ctid = tid;  // 0 .. NC-1
+  // group g takes the CTA's units g, g + NGRP, ...; each group has its own
+  // named barrier, so the groups run independently of each other
+  const int grp = warp / NCW;
+  const int lw = warp - grp * NCW;  // warp within the group
+  const int ctid = tid - grp * NC;  // 0 .. NC-1
   const int row0 = ctid / G, cv = ctid - (ctid / G) * G;
-  int it = 0;
-  for (int u = blockIdx.x; u < n_units; u += stride, ++it) {
-    const int s = it % nstage;
-    const uint32_t par = (uint32_t)(it / nstage) & 1u;
-    if (lane == 0 && !mbar_wait(&full[s], par)) *(volatile int *)s_abort = 1;
-    consumer_sync<NC>();
+  const int orow_l = lw * RPW + lane / JG;  // output row of this lane in the output phase
+  const int jg = lane - (lane / JG) * JG;   // its share of the records
+  auto gsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(NC) : "memory"); };
+  for (int it = grp; ; it += NGRP) {
+    const int u = blockIdx.x + it * stride;
+    if (u >= n_units) break;
+    const int s = it % nsr, c = it % nsc;
+    if (lane == 0 && !mbar_wait(&full[s], (uint32_t)(it / nsr) & 1u)) *(volatile int *)s_abort = 1;
+    gsync();
     if (*(volatile int *)s_abort) break;
 
-    const unsigned char *st = stages + (size_t)s * lay.bytes;
+    const unsigned char *st = rec_slots + (size_t)s * lay.bytes;
     const int *meta = reinterpret_cast<const int *>(st + lay.meta);
     const int slot = meta[0], p = meta[1], flush = meta[2], status = meta[3];
     const int b = u / a.H, h = u - (u / a.H) * a.H;
@@ -221,18 +262,27 @@ __global__ void __launch_bounds__(NCW * 32 + 32) mamba2_replay_kernel(const KArg
     if (status != kStatusOk) {
       for (int i = ctid; i < DV; i += NC) orow[i] = 0.f;
       if (ctid == 0 && status != kStatusPad) report(a.dev_err, status == kStatusBadSlot ? 1 : 2);
-      mbar_arrive(&empty[s]);
+      mbar_arrive(&ck_empty[c]);
+      mbar_arrive(&rec_empty[s]);
       continue;
     }
+    // take this thread's share of the checkpoint into registers and hand the
+    // slot straight back to the producer
+    uint4 raw[VPT];
+    {
+      const uint4 *ck = reinterpret_cast<const uint4 *>(ck_slots + (size_t)c * CKB);
+#pragma unroll
+      for (int r = 0; r < VPT; ++r) raw[r] = ck[(row0 + r * RPP) * G + cv];
+    }
+    mbar_arrive(&ck_empty[c]);
     const size_t unit = (size_t)slot * a.H + h;
     const float *sa = reinterpret_cast<const float *>(st + lay.a);
     float *scr = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + lay.scr);
     float *sW = scr, *sS = scr + L, *sC = scr + 2 * L, *sGam = scr + 2 * L + DV;
     const unsigned char *sk = st + lay.k, *sv = st + lay.v;
-    const uint4 *ck = reinterpret_cast<const uint4 *>(st + lay.ck);
 
     // window weights w_j (suffix products of the decays) and gamma
-    if (warp == 0) {
+    if (lw == 0) {
       float x0 = lane <= p ? sa[lane] : 1.f;
       float x1 = lane + 32 <= p ? sa[lane + 32] : 1.f;
       suffix_scan64(x0, x1, lane, [](float x, float y) { return x * y; });
@@ -244,17 +294,17 @@ __global__ void __launch_bounds__(NCW * 32 + 32) mamba2_replay_kernel(const KArg
       if (lane == 0) sGam[0] = x0;
     }
     float qv[E];
-    lds_cols<E>(st + lay.q, cv * E, rdt, qv);
+    lds_cols<E>(st + lay.q, cv * E, RDT, qv);
 
     float part[VPT];
     if (!flush) {
-      // k_j . q for every record of the window
-      for (int j = warp; j <= p; j += NCW) {
+      // k_j . q for every record of the window, one warp per record
+      for (int j = lw; j <= p; j += NCW) {
         float acc = 0.f;
         for (int c = lane * 4; c < DK; c += 128) {
           float kk[4], qq[4];
-          lds_cols<4>(sk, j * DK + c, rdt, kk);
-          lds_cols<4>(st + lay.q, c, rdt, qq);
+          lds_cols<4>(sk, j * DK + c, RDT, kk);
+          lds_cols<4>(st + lay.q, c, RDT, qq);
           acc += kk[0] * qq[0] + kk[1] * qq[1] + kk[2] * qq[2] + kk[3] * qq[3];
         }
 #pragma unroll
@@ -265,7 +315,7 @@ __global__ void __launch_bounds__(NCW * 32 + 32) mamba2_replay_kernel(const KArg
 #pragma unroll
       for (int r = 0; r < VPT; ++r) {
         float f[E];
-        V::unpack(ck[(row0 + r * RPP) * G + cv], f);
+        V::unpack(raw[r], f);
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) acc = fmaf(f[e], qv[e], acc);
@@ -273,45 +323,46 @@ __global__ void __launch_bounds__(NCW * 32 + 32) mamba2_replay_kernel(const KArg
       }
       group_reduce<VPT, G>(part, lane);
       if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
-      consumer_sync<NC>();
+      gsync();
 
-      const float gam = sGam[0];
-      for (int i = ctid; i < DV; i += NC) {
-        float acc = gam * sC[i];
-        for (int j = 0; j <= p; ++j) acc = fmaf(sW[j] * sS[j], lds_elem(sv, j * DV + i, rdt), acc);
-        orow[i] = acc;
+      // o_i = gamma c_i + sum_j w_j s_j v_j[i]: JG lanes per row split the records
+      {
+        float acc = 0.f;
+        for (int j = jg; j <= p; j += JG) acc = fmaf(sW[j] * sS[j], lds_elem(sv, j * DV + orow_l, RDT), acc);
+#pragma unroll
+        for (int off = JG / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (jg == 0) orow[orow_l] = fmaf(sGam[0], sC[orow_l], acc);
       }
       // append the current record (k, v verbatim, alpha) at ring slot p
-      constexpr int KCH = DK / 8, VCH = DV / 8;  // 16-byte chunks at bf16; doubled at fp32
-      const int kch = KCH * (res / 2), vch = VCH * (res / 2);
-      for (int c = ctid; c < kch + vch; c += NC) {
-        if (c < kch) {
-          const uint4 x = reinterpret_cast<const uint4 *>(sk + (size_t)p * DK * res)[c];
-          reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.ring_k) + (unit * L + p) * DK * res)[c] = x;
+      constexpr int KCH = DK * RES / 16, VCH = DV * RES / 16;
+      for (int c = ctid; c < KCH + VCH; c += NC) {
+        if (c < KCH) {
+          const uint4 x = reinterpret_cast<const uint4 *>(sk + (size_t)p * DK * RES)[c];
+          reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.ring_k) + (unit * L + p) * DK * RES)[c] = x;
         } else {
-          const uint4 x = reinterpret_cast<const uint4 *>(sv + (size_t)p * DV * res)[c - kch];
-          reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.ring_v) + (unit * L + p) * DV * res)[c - kch] = x;
+          const uint4 x = reinterpret_cast<const uint4 *>(sv + (size_t)p * DV * RES)[c - KCH];
+          reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.ring_v) + (unit * L + p) * DV * RES)[c - KCH] = x;
         }
       }
       if (ctid == 0) a.ring_a[unit * L + p] = sa[p];
     } else {
-      consumer_sync<NC>();  // weights ready
+      gsync();  // weights ready
       const float gam = sGam[0];
       TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK);
       float f[VPT][E];
 #pragma unroll
       for (int r = 0; r < VPT; ++r) {
-        V::unpack(ck[(row0 + r * RPP) * G + cv], f[r]);
+        V::unpack(raw[r], f[r]);
 #pragma unroll
         for (int e = 0; e < E; ++e) f[r][e] *= gam;
       }
       for (int j = 0; j <= p; ++j) {
         float kk[E];
-        lds_cols<E>(sk, j * DK + cv * E, rdt, kk);
+        lds_cols<E>(sk, j * DK + cv * E, RDT, kk);
         const float wj = sW[j];
 #pragma unroll
         for (int r = 0; r < VPT; ++r) {
-          const float vv = wj * lds_elem(sv, j * DV + row0 + r * RPP, rdt);
+          const float vv = wj * lds_elem(sv, j * DV + row0 + r * RPP, RDT);
 #pragma unroll
           for (int e = 0; e < E; ++e) f[r][e] = fmaf(vv, kk[e], f[r][e]);
         }
@@ -326,38 +377,44 @@ __global__ void __launch_bounds__(NCW * 32 + 32) mamba2_replay_kernel(const KArg
       }
       group_reduce<VPT, G>(part, lane);
       if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
-      consumer_sync<NC>();
+      gsync();
       for (int i = ctid; i < DV; i += NC) orow[i] = sC[i];
     }
-    mbar_arrive(&empty[s]);
+    mbar_arrive(&rec_empty[s]);
   }
-  if (ctid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
+  if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
 }
 
-template <int DV, int DK, typename TC, int NCW>
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP>
 static cudaError_t launch_mamba2(const KArgs &a, cudaStream_t s) {
-  auto kern = mamba2_replay_kernel<DV, DK, TC, NCW>;
-  const int res = a.in_dtype == kF32 ? 4 : 2;
-  const M2Stage lay = m2_stage(DV, DK, (int)sizeof(TC), res, a.L);
-  PipePlan plan;
-  cudaError_t e = plan_pipe(reinterpret_cast<const void *>(kern), NCW * 32 + 32, lay.bytes, m2_head, 4,
-                            a.B * a.H, &plan);
+  auto kern = mamba2_replay_kernel<DV, DK, TC, RT, NCW, NGRP>;
+  constexpr int threads = NGRP * NCW * 32 + 32;
+  const size_t ckb = (size_t)DV * DK * sizeof(TC);
+  const size_t rb = m2_rec(DV, DK, (int)sizeof(RT), a.L).bytes;
+  RingPlan plan;
+  cudaError_t e = plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, m2_head, a.B * a.H, &plan);
   if (e != cudaSuccess) return e;
-  kern<<<plan.grid, NCW * 32 + 32, plan.smem, s>>>(a, plan.nstage);
+  kern<<<plan.grid, threads, plan.smem, s>>>(a, plan.nsr, plan.nsc);
   return cudaGetLastError();
 }
 
-LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype) {
+template <typename RT>
+static LaunchFn find_mamba2_t(int d_v, int d_k, int ckpt_dtype) {
   if (ckpt_dtype == kF32) {
-    if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, 4>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, 8>;
-    if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, 8>;
+    if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 8, 1>;
+    if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1>;
   } else if (ckpt_dtype == kF16) {
-    if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, __half, 2>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, __half, 8>;
-    if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, __half, 8>;
+    if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, __half, RT, 2, 1>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, __half, RT, 8, 1>;
+    if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, __half, RT, 8, 1>;
   }
   return nullptr;
+}
+
+LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype) {
+  return in_dtype == kF32 ? find_mamba2_t<float>(d_v, d_k, ckpt_dtype)
+                          : find_mamba2_t<__nv_bfloat16>(d_v, d_k, ckpt_dtype);
 }
 
 }  // namespace rs
