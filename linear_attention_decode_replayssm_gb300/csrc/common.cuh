@@ -314,6 +314,25 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// per-unit status the producer hands to the consumers
+constexpr int kStatusOk = 0, kStatusPad = 1, kStatusBadSlot = 2, kStatusBadPos = 3;
+
+__host__ __device__ inline uint32_t align128(uint32_t x) { return (x + 127u) & ~127u; }
+
+// 16- and 4-byte asynchronous global -> shared copies (per thread)
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
+
+// arrive on the barrier once this thread's earlier cp.async copies have landed
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // barrier among the consumer warps only (the producer warp does not take part)
 template <int NTHREADS>
 __device__ __forceinline__ void consumer_sync() {

@@ -11,7 +11,7 @@
 //           S_{t-1} q_t and S_{t-1} k_t both expand over the checkpoint and the
 //           ring, so the output needs no rebuilt state.
 //
-// One CTA per (row b, head h).  With p ring records (d_j, k_j, g_j), j < p:
+// With p ring records (d_j, k_j, g_j), j < p, of one (row b, head h):
 //   G_j = exp(sum_{l=j+1..p-1} g_l),  Gamma = exp(sum_{l<p} g_l),
 //   a = S_{t-1} k_t = Gamma (S_ckpt k_t) + sum_j G_j (k_j . k_t) d_j,
 //   c = S_{t-1} q_t = Gamma (S_ckpt q_t) + sum_j G_j (k_j . q_t) d_j,
@@ -20,260 +20,413 @@
 //              and k rounded to the ring type;
 //   flush:     S_new = alpha_t (Gamma S_ckpt + sum_j G_j d_j k_j^T) + d_t k_t^T
 //              with the unrounded d_t, o = S_new q_t, S_new stored.
-// One streaming pass over the checkpoint yields S_ckpt k_t and S_ckpt q_t
-// together: both partial-dot sets go through one transposed group reduction.
+// Every row of the state is independent given the dot products, so a work
+// unit is a block of RB state rows of one head (a 128 x 128 fp32 head is two
+// 32 KiB units); both halves compute the (cheap) key dot products.
+//
+// Same pipeline as the Mamba-2 kernel: persistent, two CTAs per SM, one
+// producer warp (the unit's checkpoint rows as one bulk copy into a
+// checkpoint slot, the ring records, this token's inputs and the gates as
+// per-lane cp.async into a record slot), eight consumer warps that take the
+// checkpoint into registers, free its slot at once and compute from the
+// record slot.  One streaming pass over the checkpoint yields S_ckpt k_t and
+// S_ckpt q_t together through one transposed group reduction.  All waits are
+// bounded and report RS_DERR_TIMEOUT instead of hanging.
 #include "common.cuh"
 #include "launch.h"
 
 namespace rs {
 
-template <int DV, int DK, typename TC, int NT, int MINB>
-__global__ void __launch_bounds__(NT, MINB) gdn_replay_kernel(const KArgs a) {
-  using V = CkVec<TC>;
-  constexpr int E = V::E;
-  constexpr int G = DK / E;
-  constexpr int RPP = NT / G;
-  constexpr int VPT = DV / RPP;
-  constexpr int NW = NT / 32;
-  static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
-  static_assert(NT % G == 0 && DV % RPP == 0 && VPT >= 1 && 2 * VPT <= G, "bad tiling");
-  static_assert(DK % 8 == 0 && DV % 8 == 0, "head dims must be multiples of 8");
+// Byte offsets of one record slot.
+struct GdnRec {
+  uint32_t k, kt, q, d, vt, a, meta, scr, bytes;
+};
 
+__host__ __device__ inline GdnRec gdn_rec(int RB, int DK, int res, int ies, int L) {
+  GdnRec s;
+  uint32_t o = 0;
+  s.k = o;    o = align128(o + L * DK * res);    // key records 0..p-1 (ring type)
+  s.kt = o;   o = align128(o + DK * ies);        // this token's key (input type)
+  s.q = o;    o = align128(o + DK * ies);
+  s.d = o;    o = align128(o + L * RB * res);    // corrected values of this unit's rows
+  s.vt = o;   o = align128(o + RB * ies);
+  s.a = o;    o = align128(o + (L + 4) * 4);     // g_0..g_{p-1}; [L] = g_t, [L+1] = beta_t
+  s.meta = o; o = align128(o + 16);
+  s.scr = o;  o = align128(o + (3 * L + 4 * RB + 4) * 4);  // G_j, k_j.k_t, k_j.q_t, row dots, d_t, o
+  s.bytes = o;
+  return s;
+}
+
+__host__ __device__ inline uint32_t gdn_head(int nsr, int nsc) { return align128(8 * (2 * nsr + nsc) + 16); }
+
+template <int DV, int DK, typename TC, int NCW, int NSPLIT>
+__global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
+  using V = CkVec<TC>;
+  constexpr int RB = DV / NSPLIT;    // state rows per unit
+  constexpr int E = V::E;
+  constexpr int G = DK / E;          // lanes per state row
+  constexpr int NC = NCW * 32;       // consumer threads
+  constexpr int RPP = NC / G;        // state rows per pass
+  constexpr int VPT = RB / RPP;      // state rows per consumer thread
+  constexpr int RPW = RB / NCW;      // rows per warp in the per-row phase
+  constexpr int JG = 32 / RPW;       // lanes sharing a row (split over records)
+  constexpr int PROD = NCW;          // warp index of the producer
+  constexpr uint32_t CKB = RB * DK * (uint32_t)sizeof(TC);
+  static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
+  static_assert(NC % G == 0 && RB % RPP == 0 && VPT >= 1 && 2 * VPT <= G, "bad tiling");
+  static_assert(RB % NCW == 0 && 32 % RPW == 0 && JG >= 1, "bad row tiling");
+  static_assert(DK % 8 == 0 && RB % 8 == 0, "head dims must be multiples of 8");
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *rec_empty = full + nsr;
+  uint64_t *ck_empty = rec_empty + nsr;
+  int *s_abort = reinterpret_cast<int *>(ck_empty + nsc);
   const int L = a.L;
-  extern __shared__ float smem[];
-  float *sQ = smem;            // [DK] q_t
-  float *sK = sQ + DK;         // [L][DK] keys: records 0..p-1, current k_t at p
-  float *sD = sK + L * DK;     // [L][DV] corrected values; d_t at p (flush)
-  float *sVt = sD + L * DV;    // [DV] v_t
-  float *sG = sVt + DV;        // [L] log-gates of records
-  float *sW = sG + L;          // [L] G_j
-  float *sDk = sW + L;         // [L] k_j . k_t
-  float *sDq = sDk + L;        // [L] k_j . q_t
-  float *sAk = sDq + L;        // [DV] S_ckpt k_t
-  float *sAq = sAk + DV;       // [DV] S_ckpt q_t
-  float *sC = sAq + DV;        // [DV] flush output
-  float *sScal = sC + DV;      // [0] Gamma, [1] k_t . q_t
+  const int rdt = a.ring_dtype, idt = a.in_dtype;
+  const int res = rdt == kF32 ? 4 : 2, ies = idt == kF32 ? 4 : 2;
+  const GdnRec lay = gdn_rec(RB, DK, res, ies, L);
+  unsigned char *ck_slots = smem + gdn_head(nsr, nsc);
+  unsigned char *rec_slots = ck_slots + (size_t)nsc * CKB;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.x / a.H;
-  const int h = blockIdx.x - b * a.H;
-  float *orow = a.out + (size_t)b * a.so + (size_t)h * DV;
+  const int per_row = a.H * NSPLIT;
+  const int n_units = a.B * per_row;
+  const int stride = gridDim.x;
 
-  const int slot = __ldg(a.slot_idx + b);
-  if (slot < 0) {
-    for (int i = tid; i < DV; i += NT) orow[i] = 0.f;
-    return;
-  }
-  const int p = __ldg(a.write_pos + b);
-  const bool flush = __ldg(a.is_flush + b) != 0;
-  if (slot >= a.num_slots || p < 0 || p >= L) {
-    if (tid == 0) report(a.dev_err, slot >= a.num_slots ? 1 : 2);
-    for (int i = tid; i < DV; i += NT) orow[i] = 0.f;
-    return;
-  }
-  const size_t unit = (size_t)slot * a.H + h;
-  TC *ck = static_cast<TC *>(a.ckpt) + unit * (size_t)(DV * DK);
-  const int row0 = tid / G, cv = tid - (tid / G) * G;
-
-  uint4 raw[VPT];
-#pragma unroll
-  for (int r = 0; r < VPT; ++r) raw[r] = ld_stream(ck + (size_t)(row0 + r * RPP) * DK + cv * E);
-
-  // stage the ring records and the current token; append k_t and g_t now
-  const size_t ring_rec = unit * (size_t)L;
-  const int n = p + 1;
-  for (int idx = tid; idx < n * (DK / 8); idx += NT) {
-    const int j = idx / (DK / 8), c = (idx - j * (DK / 8)) * 8;
-    float f[8];
-    if (j < p) {
-      load8(a.ring_k, (ring_rec + j) * DK + c, a.ring_dtype, f);
-    } else {
-      load8(a.k, (size_t)b * a.sk + (size_t)h * DK + c, a.in_dtype, f);
-      if (!flush) store8(a.ring_k, (ring_rec + p) * DK + c, a.ring_dtype, f);
+  if (tid == 0) {
+    for (int s = 0; s < nsr; ++s) {
+      mbar_init(&full[s], 33);
+      mbar_init(&rec_empty[s], NC);
     }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sK[j * DK + c + e] = f[e];
+    for (int c = 0; c < nsc; ++c) mbar_init(&ck_empty[c], NC);
+    *s_abort = 0;
+    mbar_init_fence();
   }
-  for (int idx = tid; idx < p * (DV / 8); idx += NT) {
-    const int j = idx / (DV / 8), c = (idx - j * (DV / 8)) * 8;
-    float f[8];
-    load8(a.ring_v, (ring_rec + j) * DV + c, a.ring_dtype, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sD[j * DV + c + e] = f[e];
-  }
-  for (int idx = tid; idx < DV / 8; idx += NT) {
-    float f[8];
-    load8(a.v, (size_t)b * a.sv + (size_t)h * DV + idx * 8, a.in_dtype, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sVt[idx * 8 + e] = f[e];
-  }
-  for (int idx = tid; idx < DK / 8; idx += NT) {
-    float f[8];
-    load8(a.q, (size_t)b * a.sq + (size_t)h * DK + idx * 8, a.in_dtype, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sQ[idx * 8 + e] = f[e];
-  }
-  for (int j = tid; j < p; j += NT) sG[j] = __ldg(a.ring_a + ring_rec + j);
-  const float g_t = __ldg(a.alpha + (size_t)b * a.H + h);
-  const float beta_t = __ldg(a.beta + (size_t)b * a.H + h);
-  if (!flush && tid == 0) a.ring_a[ring_rec + p] = g_t;
   __syncthreads();
 
-  // decay weights over the p held records (warp 0); dot products (all warps)
-  if (warp == 0) {
-    float x0 = lane < p ? sG[lane] : 0.f;
-    float x1 = lane + 32 < p ? sG[lane + 32] : 0.f;
-    suffix_scan64(x0, x1, lane, [](float u, float w) { return u + w; });
-    const float n0 = __shfl_down_sync(0xffffffffu, x0, 1);
-    const float n1 = __shfl_down_sync(0xffffffffu, x1, 1);
-    const float hi0 = __shfl_sync(0xffffffffu, x1, 0);
-    const float e0 = lane == 31 ? hi0 : n0;
-    const float e1 = lane == 31 ? 0.f : n1;
-    if (lane < p) sW[lane] = expf(e0);
-    if (lane + 32 < p) sW[lane + 32] = expf(e1);
-    if (lane == 0) sScal[0] = expf(x0);
-  }
-  for (int j = warp; j <= p; j += NW) {  // j == p gives k_t . q_t
-    float sk = 0.f, sq = 0.f;
-    for (int c = lane; c < DK; c += 32) {
-      const float kj = sK[j * DK + c];
-      sk = fmaf(kj, sK[p * DK + c], sk);
-      sq = fmaf(kj, sQ[c], sq);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      sk += __shfl_xor_sync(0xffffffffu, sk, off);
-      sq += __shfl_xor_sync(0xffffffffu, sq, off);
+  if (warp == PROD) {
+    // ----------------------------------------------------------------- producer
+    const uint64_t pol_stream = policy_evict_first();
+    int it = 0;
+    auto fetch = [&](int ub, int &sl, int &wp, int &fl) {
+      const int u = ub + lane * stride;
+      if (u < n_units) {
+        const int b = u / per_row;
+        sl = __ldg(a.slot_idx + b);
+        wp = __ldg(a.write_pos + b);
+        fl = __ldg(a.is_flush + b);
+      } else {
+        sl = -1; wp = 0; fl = 0;
+      }
+    };
+    int c_sl, c_wp, c_fl;
+    fetch(blockIdx.x, c_sl, c_wp, c_fl);
+    bool ok = true;
+    for (int ub = blockIdx.x; ok && ub < n_units; ub += 32 * stride) {
+      int n_sl, n_wp, n_fl;
+      fetch(ub + 32 * stride, n_sl, n_wp, n_fl);
+      for (int j = 0; j < 32; ++j) {
+        const int u = ub + j * stride;
+        if (u >= n_units) break;
+        const int slot = __shfl_sync(0xffffffffu, c_sl, j);
+        const int p = __shfl_sync(0xffffffffu, c_wp, j);
+        const int fl = __shfl_sync(0xffffffffu, c_fl, j);
+        const int s = it % nsr, c = it % nsc;
+        if (it >= nsr || it >= nsc) {
+          int w = 1;
+          if (lane == 0) {
+            if (it >= nsr) w = mbar_wait(&rec_empty[s], ((uint32_t)(it / nsr) & 1u) ^ 1u) ? 1 : 0;
+            if (w && it >= nsc) w = mbar_wait(&ck_empty[c], ((uint32_t)(it / nsc) & 1u) ^ 1u) ? 1 : 0;
+          }
+          w = __shfl_sync(0xffffffffu, w, 0);
+          if (!w || *(volatile int *)s_abort) {
+            if (lane == 0) *(volatile int *)s_abort = 1;
+            ok = false;
+            break;
+          }
+        }
+        __syncwarp();
+        const int b = u / per_row;
+        const int rem = u - b * per_row;
+        const int h = rem / NSPLIT, row_off = (rem - h * NSPLIT) * RB;
+        const int status = slot < 0 ? kStatusPad
+                           : slot >= a.num_slots ? kStatusBadSlot
+                           : (p < 0 || p >= L) ? kStatusBadPos
+                           : kStatusOk;
+        unsigned char *st = rec_slots + (size_t)s * lay.bytes;
+        int *meta = reinterpret_cast<int *>(st + lay.meta);
+        if (status == kStatusOk) {
+          const size_t unit = (size_t)slot * a.H + h;
+          if (lane == 0) {
+            meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
+            mbar_expect_tx(&full[s], CKB);
+            bulk_load(ck_slots + (size_t)c * CKB,
+                      static_cast<const TC *>(a.ckpt) + unit * (DV * DK) + (size_t)row_off * DK, CKB, &full[s],
+                      pol_stream);
+          }
+          const int KC = DK * res / 16, DC = RB * res / 16, ITC = DK * ies / 16, VTC = RB * ies / 16;
+          const unsigned char *rk = static_cast<const unsigned char *>(a.ring_k) + unit * L * DK * res;
+          const unsigned char *rd = static_cast<const unsigned char *>(a.ring_v);
+          for (int cc = lane; cc < p * KC; cc += 32) cp_async16(st + lay.k + cc * 16, rk + cc * 16);
+          for (int cc = lane; cc < p * DC; cc += 32) {
+            const int jj = cc / DC;
+            cp_async16(st + lay.d + cc * 16,
+                       rd + ((unit * L + jj) * DV + row_off) * res + (size_t)(cc - jj * DC) * 16);
+          }
+          const unsigned char *kin =
+              static_cast<const unsigned char *>(a.k) + ((size_t)b * a.sk + (size_t)h * DK) * ies;
+          const unsigned char *qin =
+              static_cast<const unsigned char *>(a.q) + ((size_t)b * a.sq + (size_t)h * DK) * ies;
+          const unsigned char *vin =
+              static_cast<const unsigned char *>(a.v) + ((size_t)b * a.sv + (size_t)h * DV + row_off) * ies;
+          for (int cc = lane; cc < ITC; cc += 32) {
+            cp_async16(st + lay.kt + cc * 16, kin + cc * 16);
+            cp_async16(st + lay.q + cc * 16, qin + cc * 16);
+          }
+          for (int cc = lane; cc < VTC; cc += 32) cp_async16(st + lay.vt + cc * 16, vin + cc * 16);
+          float *sa = reinterpret_cast<float *>(st + lay.a);
+          for (int jj = lane; jj < p; jj += 32) cp_async4(sa + jj, a.ring_a + unit * L + jj);
+          if (lane == 30) cp_async4(sa + L, a.alpha + (size_t)b * a.H + h);
+          if (lane == 31) cp_async4(sa + L + 1, a.beta + (size_t)b * a.H + h);
+        } else if (lane == 0) {
+          meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
+        }
+        if (lane == 0) mbar_arrive(&full[s]);
+        cp_async_arrive(&full[s]);
+        ++it;
+      }
+      c_sl = n_sl; c_wp = n_wp; c_fl = n_fl;
     }
     if (lane == 0) {
-      if (j < p) {
-        sDk[j] = sk;
-        sDq[j] = sq;
-      } else {
-        sScal[1] = sq;
+      for (int k = it > nsr ? it - nsr : 0; k < it; ++k) mbar_wait(&full[k % nsr], (uint32_t)(k / nsr) & 1u);
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int lw = warp, ctid = tid;
+  const int row0 = ctid / G, cv = ctid - (ctid / G) * G;
+  const int prow = lw * RPW + lane / JG;  // row of this lane in the per-row phase
+  const int jg = lane - (lane / JG) * JG;
+  for (int it = 0; ; ++it) {
+    const int u = blockIdx.x + it * stride;
+    if (u >= n_units) break;
+    const int s = it % nsr, c = it % nsc;
+    if (lane == 0 && !mbar_wait(&full[s], (uint32_t)(it / nsr) & 1u)) *(volatile int *)s_abort = 1;
+    consumer_sync<NC>();
+    if (*(volatile int *)s_abort) break;
+
+    const unsigned char *st = rec_slots + (size_t)s * lay.bytes;
+    const int *meta = reinterpret_cast<const int *>(st + lay.meta);
+    const int slot = meta[0], p = meta[1], flush = meta[2], status = meta[3];
+    const int b = u / per_row;
+    const int rem = u - b * per_row;
+    const int h = rem / NSPLIT, half = rem - h * NSPLIT, row_off = half * RB;
+    float *orow = a.out + (size_t)b * a.so + (size_t)h * DV + row_off;
+    if (status != kStatusOk) {
+      for (int i = ctid; i < RB; i += NC) orow[i] = 0.f;
+      if (ctid == 0 && status != kStatusPad) report(a.dev_err, status == kStatusBadSlot ? 1 : 2);
+      mbar_arrive(&ck_empty[c]);
+      mbar_arrive(&rec_empty[s]);
+      continue;
+    }
+    uint4 raw[VPT];
+    {
+      const uint4 *ck = reinterpret_cast<const uint4 *>(ck_slots + (size_t)c * CKB);
+#pragma unroll
+      for (int r = 0; r < VPT; ++r) raw[r] = ck[(row0 + r * RPP) * G + cv];
+    }
+    mbar_arrive(&ck_empty[c]);
+
+    const size_t unit = (size_t)slot * a.H + h;
+    const float *sa = reinterpret_cast<const float *>(st + lay.a);
+    float *scr = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + lay.scr);
+    float *sW = scr, *sDk = scr + L, *sDq = scr + 2 * L;
+    float *sAk = scr + 3 * L, *sAq = sAk + RB, *sDt = sAq + RB, *sC = sDt + RB, *sScal = sC + RB;
+    const unsigned char *sk = st + lay.k, *skt = st + lay.kt, *sq = st + lay.q, *sd = st + lay.d;
+
+    // decay weights over the held records (warp 0)
+    if (lw == 0) {
+      float x0 = lane < p ? sa[lane] : 0.f;
+      float x1 = lane + 32 < p ? sa[lane + 32] : 0.f;
+      suffix_scan64(x0, x1, lane, [](float x, float y) { return x + y; });
+      const float n0 = __shfl_down_sync(0xffffffffu, x0, 1);
+      const float n1 = __shfl_down_sync(0xffffffffu, x1, 1);
+      const float hi0 = __shfl_sync(0xffffffffu, x1, 0);
+      if (lane < p) sW[lane] = expf(lane == 31 ? hi0 : n0);
+      if (lane + 32 < p) sW[lane + 32] = expf(lane == 31 ? 0.f : n1);
+      if (lane == 0) sScal[0] = expf(x0);
+    }
+    // k_j . k_t and k_j . q_t for the held records, k_t . q_t at j == p
+    for (int j = lw; j <= p; j += NCW) {
+      float dk = 0.f, dq = 0.f;
+      for (int cc = lane * 4; cc < DK; cc += 128) {
+        float kk[4], kt4[4], q4[4];
+        if (j < p)
+          lds_cols<4>(sk, j * DK + cc, rdt, kk);
+        else
+          lds_cols<4>(skt, cc, idt, kk);
+        lds_cols<4>(skt, cc, idt, kt4);
+        lds_cols<4>(sq, cc, idt, q4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          dk = fmaf(kk[e], kt4[e], dk);
+          dq = fmaf(kk[e], q4[e], dq);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        dk += __shfl_xor_sync(0xffffffffu, dk, off);
+        dq += __shfl_xor_sync(0xffffffffu, dq, off);
+      }
+      if (lane == 0) {
+        if (j < p) {
+          sDk[j] = dk;
+          sDq[j] = dq;
+        } else {
+          sScal[1] = dq;
+        }
       }
     }
-  }
-
-  // S_ckpt k_t and S_ckpt q_t from the registers: 2 * VPT partials per lane
-  float part[2 * VPT];
-  {
-    float kt[E], qt[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      kt[e] = sK[p * DK + cv * E + e];
-      qt[e] = sQ[cv * E + e];
-    }
-#pragma unroll
-    for (int r = 0; r < VPT; ++r) {
-      float f[E];
-      V::unpack(raw[r], f);
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        s0 = fmaf(f[e], kt[e], s0);
-        s1 = fmaf(f[e], qt[e], s1);
-      }
-      part[r] = s0;
-      part[VPT + r] = s1;
-    }
-  }
-  group_reduce<2 * VPT, G>(part, lane);
-  if (group_reduce_writer<2 * VPT, G>(lane)) {
-    const int vi = group_reduce_index<2 * VPT, G>(lane);
-    if (vi < VPT)
-      sAk[row0 + vi * RPP] = part[0];
-    else
-      sAq[row0 + (vi - VPT) * RPP] = part[0];
-  }
-  __syncthreads();
-
-  // per value row: rebuild S_{t-1} k_t and S_{t-1} q_t, then d_t
-  const float alpha_t = expf(g_t);
-  const float Gam = sScal[0];
-  for (int i = tid; i < DV; i += NT) {
-    float ak = Gam * sAk[i], aq = Gam * sAq[i];
-    for (int j = 0; j < p; ++j) {
-      const float dj = sW[j] * sD[j * DV + i];
-      ak = fmaf(sDk[j], dj, ak);
-      aq = fmaf(sDq[j], dj, aq);
-    }
-    const float d_t = beta_t * (sVt[i] - alpha_t * ak);
-    if (!flush) {
-      orow[i] = fmaf(alpha_t, aq, d_t * sScal[1]);
-      store1(a.ring_v, (ring_rec + p) * DV + i, a.ring_dtype, d_t);
-    } else {
-      sD[p * DV + i] = d_t;
-    }
-  }
-  if (!flush) return;
-  __syncthreads();
-
-  // flush: S_new = alpha_t (Gamma S_ckpt + sum_j G_j d_j k_j^T) + d_t k_t^T
-  {
-    float f[VPT][E];
-    const float scale0 = alpha_t * Gam;
-#pragma unroll
-    for (int r = 0; r < VPT; ++r) {
-      V::unpack(raw[r], f[r]);
-#pragma unroll
-      for (int e = 0; e < E; ++e) f[r][e] *= scale0;
-    }
-    for (int j = 0; j <= p; ++j) {
-      float kk[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) kk[e] = sK[j * DK + cv * E + e];
-      const float wj = j < p ? alpha_t * sW[j] : 1.f;
+    // S_ckpt k_t and S_ckpt q_t for this thread's rows
+    float ktc[E], qc[E];
+    lds_cols<E>(skt, cv * E, idt, ktc);
+    lds_cols<E>(sq, cv * E, idt, qc);
+    {
+      float part[2 * VPT];
 #pragma unroll
       for (int r = 0; r < VPT; ++r) {
-        const float dd = wj * sD[j * DV + row0 + r * RPP];
+        float f[E];
+        V::unpack(raw[r], f);
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) f[r][e] = fmaf(dd, kk[e], f[r][e]);
+        for (int e = 0; e < E; ++e) {
+          s0 = fmaf(f[e], ktc[e], s0);
+          s1 = fmaf(f[e], qc[e], s1);
+        }
+        part[r] = s0;
+        part[VPT + r] = s1;
+      }
+      group_reduce<2 * VPT, G>(part, lane);
+      if (group_reduce_writer<2 * VPT, G>(lane)) {
+        const int vi = group_reduce_index<2 * VPT, G>(lane);
+        if (vi < VPT)
+          sAk[row0 + vi * RPP] = part[0];
+        else
+          sAq[row0 + (vi - VPT) * RPP] = part[0];
       }
     }
-    float qv[E];
+    consumer_sync<NC>();
+
+    // per row: S_{t-1} k_t, S_{t-1} q_t, then d_t (JG lanes split the records)
+    const float gam = sScal[0], kq = sScal[1];
+    const float g_t = sa[L], beta_t = sa[L + 1];
+    const float alpha_t = expf(g_t);
+    {
+      float ak = 0.f, aq = 0.f;
+      for (int j = jg; j < p; j += JG) {
+        const float dj = sW[j] * lds_elem(sd, j * RB + prow, rdt);
+        ak = fmaf(sDk[j], dj, ak);
+        aq = fmaf(sDq[j], dj, aq);
+      }
 #pragma unroll
-    for (int e = 0; e < E; ++e) qv[e] = sQ[cv * E + e];
-    float po[VPT];
-#pragma unroll
-    for (int r = 0; r < VPT; ++r) {
-      float s = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) s = fmaf(f[r][e], qv[e], s);
-      po[r] = s;
-      st_vec(ck + (size_t)(row0 + r * RPP) * DK + cv * E, V::pack(f[r]));
+      for (int off = JG / 2; off > 0; off >>= 1) {
+        ak += __shfl_xor_sync(0xffffffffu, ak, off);
+        aq += __shfl_xor_sync(0xffffffffu, aq, off);
+      }
+      if (jg == 0) {
+        ak = fmaf(gam, sAk[prow], ak);
+        aq = fmaf(gam, sAq[prow], aq);
+        const float d_t = beta_t * (lds_elem(st + lay.vt, prow, idt) - alpha_t * ak);
+        if (!flush) {
+          orow[prow] = fmaf(alpha_t, aq, d_t * kq);
+          store1(a.ring_v, (unit * L + p) * DV + row_off + prow, rdt, d_t);
+        } else {
+          sDt[prow] = d_t;
+        }
+      }
     }
-    group_reduce<VPT, G>(po, lane);
-    if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = po[0];
+    if (!flush) {
+      if (half == 0) {
+        // append this token's key (rounded to the ring type) and gate
+        for (int cc = ctid; cc < DK / 8; cc += NC) {
+          float f[8];
+          lds_cols<8>(skt, cc * 8, idt, f);
+          store8(a.ring_k, (unit * L + p) * DK + cc * 8, rdt, f);
+        }
+        if (ctid == 0) a.ring_a[unit * L + p] = g_t;
+      }
+    } else {
+      consumer_sync<NC>();  // d_t of every row ready
+      TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK) + (size_t)row_off * DK;
+      const float scale0 = alpha_t * gam;
+      float f[VPT][E];
+#pragma unroll
+      for (int r = 0; r < VPT; ++r) {
+        V::unpack(raw[r], f[r]);
+#pragma unroll
+        for (int e = 0; e < E; ++e) f[r][e] *= scale0;
+      }
+      for (int j = 0; j < p; ++j) {
+        float kk[E];
+        lds_cols<E>(sk, j * DK + cv * E, rdt, kk);
+        const float wj = alpha_t * sW[j];
+#pragma unroll
+        for (int r = 0; r < VPT; ++r) {
+          const float dd = wj * lds_elem(sd, j * RB + row0 + r * RPP, rdt);
+#pragma unroll
+          for (int e = 0; e < E; ++e) f[r][e] = fmaf(dd, kk[e], f[r][e]);
+        }
+      }
+      float po[VPT];
+#pragma unroll
+      for (int r = 0; r < VPT; ++r) {
+        const float dd = sDt[row0 + r * RPP];
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          f[r][e] = fmaf(dd, ktc[e], f[r][e]);
+          acc = fmaf(f[r][e], qc[e], acc);
+        }
+        po[r] = acc;
+        st_vec(ckg + (size_t)(row0 + r * RPP) * DK + cv * E, V::pack(f[r]));
+      }
+      group_reduce<VPT, G>(po, lane);
+      if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = po[0];
+      consumer_sync<NC>();
+      for (int i = ctid; i < RB; i += NC) orow[i] = sC[i];
+    }
+    mbar_arrive(&rec_empty[s]);
   }
-  __syncthreads();
-  for (int i = tid; i < DV; i += NT) orow[i] = sC[i];
+  if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
 }
 
-template <int DV, int DK>
-static size_t gdn_smem(int L) {
-  return sizeof(float) * (size_t)(DK + L * (DK + DV) + DV + 4 * L + 3 * DV + 4);
-}
-
-template <int DV, int DK, typename TC, int NT, int MINB = 1>
+template <int DV, int DK, typename TC, int NCW, int NSPLIT>
 static cudaError_t launch_gdn(const KArgs &a, cudaStream_t s) {
-  auto kern = gdn_replay_kernel<DV, DK, TC, NT, MINB>;
-  const size_t smem = gdn_smem<DV, DK>(a.L);
-  cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kern), smem);
+  auto kern = gdn_replay_kernel<DV, DK, TC, NCW, NSPLIT>;
+  constexpr int threads = NCW * 32 + 32;
+  const size_t ckb = (size_t)(DV / NSPLIT) * DK * sizeof(TC);
+  const int res = a.ring_dtype == kF32 ? 4 : 2, ies = a.in_dtype == kF32 ? 4 : 2;
+  const size_t rb = gdn_rec(DV / NSPLIT, DK, res, ies, a.L).bytes;
+  RingPlan plan;
+  cudaError_t e =
+      plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, gdn_head, a.B * a.H * NSPLIT, &plan);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)((size_t)a.B * a.H), NT, smem, s>>>(a);
+  kern<<<plan.grid, threads, plan.smem, s>>>(a, plan.nsr, plan.nsc);
   return cudaGetLastError();
 }
 
 LaunchFn find_gdn(int d_v, int d_k, int ckpt_dtype) {
   if (ckpt_dtype == kF32) {
-    if (d_v == 16 && d_k == 32) return launch_gdn<16, 32, float, 128>;
-    if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, float, 256>;
-    if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, float, 512, 2>;
+    if (d_v == 16 && d_k == 32) return launch_gdn<16, 32, float, 4, 1>;
+    if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, float, 8, 1>;
+    if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, float, 8, 2>;
   } else if (ckpt_dtype == kF16) {
-    if (d_v == 16 && d_k == 32) return launch_gdn<16, 32, __half, 64>;
-    if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, __half, 256>;
-    if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, __half, 256>;
+    if (d_v == 16 && d_k == 32) return launch_gdn<16, 32, __half, 2, 1>;
+    if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, __half, 8, 1>;
+    if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, __half, 8, 1>;
   }
   return nullptr;
 }

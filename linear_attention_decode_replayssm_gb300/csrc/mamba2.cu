@@ -35,25 +35,6 @@
 
 namespace rs {
 
-namespace {
-
-constexpr int kStatusOk = 0, kStatusPad = 1, kStatusBadSlot = 2, kStatusBadPos = 3;
-
-__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
-}
-
-// arrive on the barrier once this thread's earlier cp.async copies have landed
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-
-}  // namespace
 
 // Shared memory holds two rings: checkpoint slots (the 32 KiB-class state
 // block of a unit, released as soon as the consumers hold it in registers)
@@ -64,8 +45,6 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
 struct M2Rec {
   uint32_t k, v, q, a, meta, scr, bytes;
 };
-
-__host__ __device__ inline uint32_t align128(uint32_t x) { return (x + 127u) & ~127u; }
 
 __host__ __device__ inline M2Rec m2_rec(int DV, int DK, int rec_es, int L) {
   M2Rec s;
