@@ -225,7 +225,16 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32) mamba2_replay_kernel(con
   const int orow_l = lw * RPW + lane / JG;  // output row of this lane in the output phase
   const int jg = lane - (lane / JG) * JG;   // its share of the records
   auto gsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(NC) : "memory"); };
-  for (int it = grp; ; it += NGRP) {
+  // row and head of the unit, stepped instead of divided
+  const int ustep = NGRP * stride;
+  const int step_b = ustep / a.H, step_h = ustep - (ustep / a.H) * a.H;
+  int b = (int)(blockIdx.x + grp * stride) / a.H;
+  int h = (int)(blockIdx.x + grp * stride) - b * a.H;
+  for (int it = grp; ; it += NGRP, h += step_h, b += step_b) {
+    if (h >= a.H) {
+      h -= a.H;
+      ++b;
+    }
     const int u = blockIdx.x + it * stride;
     if (u >= n_units) break;
     const int s = it % nsr, c = it % nsc;
@@ -234,9 +243,8 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32) mamba2_replay_kernel(con
     if (*(volatile int *)s_abort) break;
 
     const unsigned char *st = rec_slots + (size_t)s * lay.bytes;
-    const int *meta = reinterpret_cast<const int *>(st + lay.meta);
-    const int slot = meta[0], p = meta[1], flush = meta[2], status = meta[3];
-    const int b = u / a.H, h = u - (u / a.H) * a.H;
+    const int4 m = *reinterpret_cast<const int4 *>(st + lay.meta);
+    const int slot = m.x, p = m.y, flush = m.z, status = m.w;
     float *orow = a.out + (size_t)b * a.so + (size_t)h * DV;
     if (status != kStatusOk) {
       for (int i = ctid; i < DV; i += NC) orow[i] = 0.f;
@@ -277,14 +285,23 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32) mamba2_replay_kernel(con
 
     float part[VPT];
     if (!flush) {
-      // k_j . q for every record of the window, one warp per record
+      // k_j . q for every record of the window, one warp per record (q held
+      // in registers across the records)
+      constexpr int QPL = (DK + 127) / 128;  // 4-element chunks of q per lane
+      float qq[QPL][4];
+#pragma unroll
+      for (int i = 0; i < QPL; ++i)
+        if (lane * 4 + i * 128 < DK) lds_cols<4>(st + lay.q, lane * 4 + i * 128, RDT, qq[i]);
       for (int j = lw; j <= p; j += NCW) {
         float acc = 0.f;
-        for (int c = lane * 4; c < DK; c += 128) {
-          float kk[4], qq[4];
-          lds_cols<4>(sk, j * DK + c, RDT, kk);
-          lds_cols<4>(st + lay.q, c, RDT, qq);
-          acc += kk[0] * qq[0] + kk[1] * qq[1] + kk[2] * qq[2] + kk[3] * qq[3];
+#pragma unroll
+        for (int i = 0; i < QPL; ++i) {
+          const int cc = lane * 4 + i * 128;
+          if (cc < DK) {
+            float kk[4];
+            lds_cols<4>(sk, j * DK + cc, RDT, kk);
+            acc = fmaf(kk[0], qq[i][0], fmaf(kk[1], qq[i][1], fmaf(kk[2], qq[i][2], fmaf(kk[3], qq[i][3], acc))));
+          }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
