@@ -256,7 +256,7 @@ int replayssm_abi_version(void) { return RS_ABI_VERSION; }
 int replayssm_supported(int variant, int d_v, int d_k, int ckpt_dtype) {
   if (variant != RS_MAMBA2 && variant != RS_GDN) return 0;
   if (variant == RS_MAMBA2) return rs::find_mamba2(d_v, d_k, ckpt_dtype, RS_BF16) != nullptr;
-  return rs::find_gdn(d_v, d_k, ckpt_dtype) != nullptr;
+  return rs::find_gdn(d_v, d_k, ckpt_dtype, RS_F16, RS_BF16) != nullptr;
 }
 
 int replayssm_plan_step(const int64_t *decode_step, const uint8_t *force_flush, int32_t B, int32_t L,
@@ -283,7 +283,7 @@ int replayssm_decode_mamba2(const rs_step_args *args, rs_stream_t stream) {
 int replayssm_decode_gdn(const rs_step_args *args, rs_stream_t stream) {
   const int st = validate(args, /*replay=*/true, /*gdn=*/true);
   if (st != RS_OK || args->B == 0) return st;
-  return run(rs::find_gdn(args->d_v, args->d_k, args->ckpt_dtype), args, stream);
+  return run(rs::find_gdn(args->d_v, args->d_k, args->ckpt_dtype, args->ring_dtype, args->in_dtype), args, stream);
 }
 
 int conventional_decode(const rs_step_args *args, int variant, rs_stream_t stream) {

@@ -11,6 +11,7 @@
 // 256-byte (fp16) rows, fully coalesced.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -313,6 +314,22 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+
+// element type tag of ring records and inputs, as a compile-time dtype
+template <typename T>
+struct Rec;
+template <>
+struct Rec<float> {
+  static constexpr int kDtype = kF32;
+};
+template <>
+struct Rec<__nv_bfloat16> {
+  static constexpr int kDtype = kBF16;
+};
+template <>
+struct Rec<__half> {
+  static constexpr int kDtype = kF16;
+};
 
 // per-unit status the producer hands to the consumers
 constexpr int kStatusOk = 0, kStatusPad = 1, kStatusBadSlot = 2, kStatusBadPos = 3;

@@ -59,7 +59,7 @@ __host__ __device__ inline GdnRec gdn_rec(int RB, int DK, int res, int ies, int 
 
 __host__ __device__ inline uint32_t gdn_head(int nsr, int nsc) { return align128(8 * (2 * nsr + nsc) + 16); }
 
-template <int DV, int DK, typename TC, int NCW, int NSPLIT>
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT>
 __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr int RB = DV / NSPLIT;    // state rows per unit
@@ -83,8 +83,8 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
   uint64_t *ck_empty = rec_empty + nsr;
   int *s_abort = reinterpret_cast<int *>(ck_empty + nsc);
   const int L = a.L;
-  const int rdt = a.ring_dtype, idt = a.in_dtype;
-  const int res = rdt == kF32 ? 4 : 2, ies = idt == kF32 ? 4 : 2;
+  constexpr int rdt = Rec<RT>::kDtype, idt = Rec<IT>::kDtype;  // ring and input element types
+  constexpr int res = (int)sizeof(RT), ies = (int)sizeof(IT);
   const GdnRec lay = gdn_rec(RB, DK, res, ies, L);
   unsigned char *ck_slots = smem + gdn_head(nsr, nsc);
   unsigned char *rec_slots = ck_slots + (size_t)nsc * CKB;
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
                       static_cast<const TC *>(a.ckpt) + unit * (DV * DK) + (size_t)row_off * DK, CKB, &full[s],
                       pol_stream);
           }
-          const int KC = DK * res / 16, DC = RB * res / 16, ITC = DK * ies / 16, VTC = RB * ies / 16;
+          constexpr int KC = DK * res / 16, DC = RB * res / 16, ITC = DK * ies / 16, VTC = RB * ies / 16;
           const unsigned char *rk = static_cast<const unsigned char *>(a.ring_k) + unit * L * DK * res;
           const unsigned char *rd = static_cast<const unsigned char *>(a.ring_v);
           for (int cc = lane; cc < p * KC; cc += 32) cp_async16(st + lay.k + cc * 16, rk + cc * 16);
@@ -260,20 +260,34 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
       if (lane == 0) sScal[0] = expf(x0);
     }
     // k_j . k_t and k_j . q_t for the held records, k_t . q_t at j == p
+    // (this lane's chunks of k_t and q_t stay in registers across records)
+    constexpr int QPL = (DK + 127) / 128;
+    float kt4[QPL][4], q4[QPL][4];
+#pragma unroll
+    for (int i = 0; i < QPL; ++i) {
+      if (lane * 4 + i * 128 < DK) {
+        lds_cols<4>(skt, lane * 4 + i * 128, idt, kt4[i]);
+        lds_cols<4>(sq, lane * 4 + i * 128, idt, q4[i]);
+      }
+    }
     for (int j = lw; j <= p; j += NCW) {
       float dk = 0.f, dq = 0.f;
-      for (int cc = lane * 4; cc < DK; cc += 128) {
-        float kk[4], kt4[4], q4[4];
-        if (j < p)
-          lds_cols<4>(sk, j * DK + cc, rdt, kk);
-        else
-          lds_cols<4>(skt, cc, idt, kk);
-        lds_cols<4>(skt, cc, idt, kt4);
-        lds_cols<4>(sq, cc, idt, q4);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          dk = fmaf(kk[e], kt4[e], dk);
-          dq = fmaf(kk[e], q4[e], dq);
+      for (int i = 0; i < QPL; ++i) {
+        const int cc = lane * 4 + i * 128;
+        if (cc < DK) {
+          float kk[4];
+          if (j < p) {
+            lds_cols<4>(sk, j * DK + cc, rdt, kk);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) kk[e] = kt4[i][e];
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dk = fmaf(kk[e], kt4[i][e], dk);
+            dq = fmaf(kk[e], q4[i][e], dq);
+          }
         }
       }
 #pragma unroll
@@ -403,13 +417,12 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
   if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
 }
 
-template <int DV, int DK, typename TC, int NCW, int NSPLIT>
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT>
 static cudaError_t launch_gdn(const KArgs &a, cudaStream_t s) {
-  auto kern = gdn_replay_kernel<DV, DK, TC, NCW, NSPLIT>;
+  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT>;
   constexpr int threads = NCW * 32 + 32;
   const size_t ckb = (size_t)(DV / NSPLIT) * DK * sizeof(TC);
-  const int res = a.ring_dtype == kF32 ? 4 : 2, ies = a.in_dtype == kF32 ? 4 : 2;
-  const size_t rb = gdn_rec(DV / NSPLIT, DK, res, ies, a.L).bytes;
+  const size_t rb = gdn_rec(DV / NSPLIT, DK, (int)sizeof(RT), (int)sizeof(IT), a.L).bytes;
   RingPlan plan;
   cudaError_t e =
       plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, gdn_head, a.B * a.H * NSPLIT, &plan);
@@ -418,16 +431,27 @@ static cudaError_t launch_gdn(const KArgs &a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-LaunchFn find_gdn(int d_v, int d_k, int ckpt_dtype) {
-  if (ckpt_dtype == kF32) {
-    if (d_v == 16 && d_k == 32) return launch_gdn<16, 32, float, 4, 1>;
-    if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, float, 8, 1>;
-    if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, float, 8, 2>;
-  } else if (ckpt_dtype == kF16) {
-    if (d_v == 16 && d_k == 32) return launch_gdn<16, 32, __half, 2, 1>;
-    if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, __half, 8, 1>;
-    if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, __half, 8, 1>;
-  }
+template <typename TC, typename RT, typename IT>
+static LaunchFn find_gdn_t(int d_v, int d_k) {
+  constexpr bool f32 = sizeof(TC) == 4;
+  if (d_v == 16 && d_k == 32) return launch_gdn<16, 32, TC, RT, IT, f32 ? 4 : 2, 1>;
+  if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, TC, RT, IT, 8, 1>;
+  if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, TC, RT, IT, 8, f32 ? 2 : 1>;
+  return nullptr;
+}
+
+template <typename TC>
+static LaunchFn find_gdn_c(int d_v, int d_k, int ring_dtype, int in_dtype) {
+  if (ring_dtype == kF16)
+    return in_dtype == kF32 ? find_gdn_t<TC, __half, float>(d_v, d_k) : find_gdn_t<TC, __half, __nv_bfloat16>(d_v, d_k);
+  if (ring_dtype == kF32)
+    return in_dtype == kF32 ? find_gdn_t<TC, float, float>(d_v, d_k) : find_gdn_t<TC, float, __nv_bfloat16>(d_v, d_k);
+  return nullptr;
+}
+
+LaunchFn find_gdn(int d_v, int d_k, int ckpt_dtype, int ring_dtype, int in_dtype) {
+  if (ckpt_dtype == kF32) return find_gdn_c<float>(d_v, d_k, ring_dtype, in_dtype);
+  if (ckpt_dtype == kF16) return find_gdn_c<__half>(d_v, d_k, ring_dtype, in_dtype);
   return nullptr;
 }
 

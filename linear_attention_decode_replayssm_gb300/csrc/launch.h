@@ -11,7 +11,7 @@ using LaunchFn = cudaError_t (*)(const KArgs &, cudaStream_t);
 
 // nullptr when the (d_v, d_k, checkpoint dtype) combination is not built in.
 LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype);
-LaunchFn find_gdn(int d_v, int d_k, int ckpt_dtype);
+LaunchFn find_gdn(int d_v, int d_k, int ckpt_dtype, int ring_dtype, int in_dtype);
 LaunchFn find_conventional(int variant, int d_v, int d_k, int ckpt_dtype);
 
 // Launch shape of a persistent bulk-copy pipeline: CTAs, stages per CTA and

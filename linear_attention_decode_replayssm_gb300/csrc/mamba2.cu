@@ -28,8 +28,6 @@
 // state) spread evenly over the CTAs.  Every wait is bounded: on a timeout
 // the kernel reports RS_DERR_TIMEOUT, drains its own copies and returns.
 // No tensor cores: the step is a bandwidth-bound GEMV (about 0.6 FLOP/byte).
-#include <cuda_bf16.h>
-
 #include "common.cuh"
 #include "launch.h"
 
@@ -62,17 +60,6 @@ __host__ __device__ inline M2Rec m2_rec(int DV, int DK, int rec_es, int L) {
 // barriers full/rec_empty[nsr], ck_empty[nsc] and the abort flag
 __host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(8 * (2 * nsr + nsc) + 16); }
 
-// Element type of the ring records and inputs (they are the same for Mamba-2).
-template <typename RT>
-struct Rec;
-template <>
-struct Rec<float> {
-  static constexpr int kDtype = kF32;
-};
-template <>
-struct Rec<__nv_bfloat16> {
-  static constexpr int kDtype = kBF16;
-};
 
 template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP>
 __global__ void __launch_bounds__(NGRP * NCW * 32 + 32) mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
