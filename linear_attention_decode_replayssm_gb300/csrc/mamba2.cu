@@ -255,8 +255,10 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32) mamba2_replay_kernel(con
     float *sW = scr, *sS = scr + L, *sC = scr + 2 * L, *sGam = scr + 2 * L + DV;
     const unsigned char *sk = st + lay.k, *sv = st + lay.v;
 
-    // window weights w_j (suffix products of the decays) and gamma
-    if (lw == 0) {
+    // window weights w_j (suffix products of the decays) and gamma; a flush
+    // needs them all, so one warp scans them; non-flush rows build their own
+    // below, off the critical path
+    if (flush && lw == 0) {
       float x0 = lane <= p ? sa[lane] : 1.f;
       float x1 = lane + 32 <= p ? sa[lane + 32] : 1.f;
       suffix_scan64(x0, x1, lane, [](float x, float y) { return x * y; });
@@ -308,13 +310,27 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32) mamba2_replay_kernel(con
       if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
       gsync();
 
-      // o_i = gamma c_i + sum_j w_j s_j v_j[i]: JG lanes per row split the records
+      // o_i = gamma c_i + sum_j w_j s_j v_j[i]: JG lanes per row split the
+      // records; each lane walks its records from the newest down, extending
+      // the suffix product w_j = prod_{l=j+1..p} alpha_l as it goes
       {
-        float acc = 0.f;
-        for (int j = jg; j <= p; j += JG) acc = fmaf(sW[j] * sS[j], lds_elem(sv, j * DV + orow_l, RDT), acc);
+        float acc = 0.f, w = 1.f;
+        int j = jg + ((p - jg) / JG) * JG;  // this lane's newest record
+        if (jg <= p) {
+          for (int l = p; l > j; --l) w *= sa[l];
+          for (;;) {
+            acc = fmaf(w * sS[j], lds_elem(sv, j * DV + orow_l, RDT), acc);
+            if (j < JG) break;
+#pragma unroll
+            for (int l = 0; l < JG; ++l) w *= sa[j - l];
+            j -= JG;
+          }
+        }
+        // lane jg = 0 ends at record 0 with w = w_0, so gamma = w_0 * alpha_0
+        const float gam = w * sa[0];
 #pragma unroll
         for (int off = JG / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (jg == 0) orow[orow_l] = fmaf(sGam[0], sC[orow_l], acc);
+        if (jg == 0) orow[orow_l] = fmaf(gam, sC[orow_l], acc);
       }
       // append the current record (k, v verbatim, alpha) at ring slot p
       constexpr int KCH = DK * RES / 16, VCH = DV * RES / 16;
