@@ -21,9 +21,12 @@
 // records, this token's k, v, q and the decays into a record slot with
 // per-lane cp.async.  It prefetches the per-row slot, cursor and flag 32
 // units ahead, so no dependent global load sits on the streaming path.
-// Eight consumer warps wait for a unit, take their share of the checkpoint
-// into registers (freeing that slot for the next load at once), compute from
-// the record slot and release it.  The units a CTA owns are
+// Consumer groups (two groups of four warps for the 64 x 128 fp32 layer)
+// take alternate units: a group waits for its unit, takes its share of the
+// checkpoint into registers (freeing that slot for the next load at once),
+// computes from the record slot and releases it.  The step is bound by
+// instruction issue as much as by bandwidth, so the per-warp fixed costs of a
+// unit are paid by four warps rather than eight.  The units a CTA owns are
 // strided across the batch, so the ~1/L flush rows (which also write their
 // state) spread evenly over the CTAs.  Every wait is bounded: on a timeout
 // the kernel reports RS_DERR_TIMEOUT, drains its own copies and returns.
@@ -62,7 +65,7 @@ __host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(
 
 
 template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP>
-__global__ void __launch_bounds__(NGRP * NCW * 32 + 32) mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
+__global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr int E = V::E;
   constexpr int G = DK / E;          // lanes per state row
@@ -401,7 +404,7 @@ template <typename RT>
 static LaunchFn find_mamba2_t(int d_v, int d_k, int ckpt_dtype) {
   if (ckpt_dtype == kF32) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 8, 1>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1>;
   } else if (ckpt_dtype == kF16) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, __half, RT, 2, 1>;
