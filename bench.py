@@ -223,7 +223,7 @@ def source_hash(kernel):
 class Layer:
     """Device state, inputs and per-step plans for one synthetic layer."""
 
-    def __init__(self, lib, spec, device, seed, n_steps):
+    def __init__(self, lib, spec, device, seed, n_steps, plans=None, with_state=True):
         import numpy as np
         import torch
 
@@ -246,7 +246,7 @@ class Layer:
 
         sk = math.sqrt(dk)
         self.ckpt = (randn(B, H, dv, dk) / sk).to(td[spec["ckpt"]])
-        self.state = self.ckpt.clone()  # for the conventional kernel
+        self.state = self.ckpt.clone() if with_state else None  # for the conventional kernel
         self.ring_v = (randn(B, H, L, dv) / sk).to(td[spec["ring"]])
         self.ring_k = (unit(randn(B, H, L, dk)) if gdn else randn(B, H, L, dk) / sk).to(td[spec["ring"]])
         self.ring_a = decay(B, H, L)
@@ -264,12 +264,14 @@ class Layer:
             self.inputs.append(x)
         rng = np.random.default_rng(seed)
         self.decode_step0 = rng.integers(0, L, size=B).astype(np.int64)
-        wps, fls = [], []
-        for t in range(n_steps):
-            wp, fl = lib.replayssm_plan_step(self.decode_step0 + t, L)
-            wps.append(wp)
-            fls.append(fl)
-        self.wp_host, self.fl_host = np.stack(wps), np.stack(fls)
+        if plans is None:
+            wps, fls = [], []
+            for t in range(n_steps):
+                wp, fl = lib.replayssm_plan_step(self.decode_step0 + t, L)
+                wps.append(wp)
+                fls.append(fl)
+            plans = (np.stack(wps), np.stack(fls))
+        self.wp_host, self.fl_host = plans
         self.wp = torch.from_numpy(self.wp_host).to(device)
         self.fl = torch.from_numpy(self.fl_host).to(device)
         self.variant_code = lib.RS_GDN if gdn else lib.RS_MAMBA2
@@ -417,6 +419,95 @@ def measure_e2e(lib, torch, layer, steps, dist):
     return el, h2d, d2h
 
 
+def measure_layers40(lib, torch, args, device, sampler):
+    """40 independent Mamba-2 layer pools at batch 256 under continuous
+    batching (rows leave and new requests join at random offsets every 8
+    steps; a joining row restarts at decode step 0), one CUDA graph of 40
+    launches per decode step."""
+    import numpy as np
+
+    from linear_attention_decode_replayssm_gb300 import synth
+
+    spec = WORKLOADS["mamba2_bs256"]
+    B, L, n_layers, K = spec["B"], spec["L"], 40, args.layers40_steps
+    W = 4
+    ds0 = np.random.default_rng(5).integers(0, L, B)
+    sched = synth.ChurnSchedule(B, L, W + K, period=8, p_churn=0.25, seed=6, decode_step0=ds0)
+    wps, fls = [], []
+    for t in range(W + K):
+        wp, fl = lib.replayssm_plan_step(sched.decode_step(t), L)
+        wps.append(wp)
+        fls.append(fl)
+    plans = (np.stack(wps), np.stack(fls))
+    layers = [Layer(lib, spec, device, 200 + l, W + K, plans=plans, with_state=False) for l in range(n_layers)]
+    for l in range(1, n_layers):  # one set of 16 input batches serves every layer
+        layers[l].inputs = layers[0].inputs
+        layers[l].wp, layers[l].fl = layers[0].wp, layers[0].fl
+    stream = torch.cuda.Stream(device=device)
+    stream.wait_stream(torch.cuda.current_stream())
+
+    def step(t, st):
+        for l in range(n_layers):
+            layers[l].replay_step(t, st, x=layers[l].inputs[(t + l) % N_INPUT_SETS])
+
+    with torch.cuda.stream(stream):
+        for t in range(W):
+            step(t, stream)
+    ms = _timed_graph(torch, step, W, W + K, stream, args.eager, None, sampler)
+    bytes_step = layers[0].bytes_per_step(W, W + K) * n_layers
+    joins = int(sched.join[W:].sum())
+    del layers
+    torch.cuda.empty_cache()
+    return dict(ms_per_step=ms / K, bytes_per_step=bytes_step, joins=joins, steps=K, layers=n_layers)
+
+
+def run_sweep(args):
+    """Batch x buffer length x checkpoint dtype, ReplaySSM next to the
+    conventional kernel on the same inputs; small batches rotate several state
+    pools so that every step reads its state from HBM (cold L2)."""
+    import numpy as np
+    import torch
+
+    from linear_attention_decode_replayssm_gb300 import _lib, build, traffic
+
+    build.build()
+    _lib.load()
+    device = torch.device("cuda", 0)
+    peak, _ = _peak()
+    base = WORKLOADS["mamba2_bs256"]
+    out = []
+    for ck in ("f32", "f16"):
+        for L in (8, 16, 32):
+            for B in (1, 8, 32, 128, 256, 512):
+                spec = dict(base, B=B, L=L, ckpt=ck)
+                state_bytes = B * spec["H"] * spec["d_v"] * spec["d_k"] * (4 if ck == "f32" else 2)
+                n_pools = max(1, int(np.ceil(3 * 129e6 / state_bytes)))
+                K = 96 if B >= 128 else 256
+                K = (K // n_pools + 1) * n_pools if n_pools > 1 else K
+                pools = [Layer(_lib, spec, device, 300 + i, 8 + K) for i in range(n_pools)]
+                stream = torch.cuda.Stream(device=device)
+                stream.wait_stream(torch.cuda.current_stream())
+                rep = lambda t, st: pools[t % n_pools].replay_step(t, st)
+                con = lambda t, st: pools[t % n_pools].conventional_step(t, st)
+                with torch.cuda.stream(stream):
+                    for t in range(8):
+                        rep(t, stream)
+                        con(t, stream)
+                ms_r = _timed_graph(torch, rep, 8, 8 + K, stream, False, None, None) / K
+                ms_c = _timed_graph(torch, con, 8, 8 + K, stream, False, None, None) / K
+                by_r = np.mean([p.bytes_per_step(8, 8 + K) for p in pools[:1]])
+                by_c = pools[0].bytes_per_step(8, 9, replay=False)
+                row = dict(ckpt=ck, L=L, B=B, pools=n_pools, replay_us=ms_r * 1e3, conventional_us=ms_c * 1e3,
+                           speedup=ms_c / ms_r, replay_frac=by_r / (ms_r / 1e3) / 1e9 / peak,
+                           conventional_frac=by_c / (ms_c / 1e3) / 1e9 / peak,
+                           replay_tok_s=B / (ms_r / 1e3), modelled_ratio=by_r / by_c)
+                out.append(row)
+                print(json.dumps(row), flush=True)
+                del pools
+                torch.cuda.empty_cache()
+    return out
+
+
 def run_native(args):
     import torch
 
@@ -458,6 +549,12 @@ def run_native(args):
         _, o = measure_layer(_lib, torch, WORKLOADS[other], device, args, dist, sampler, seed=100 + rank)
         extra[other] = o
         torch.cuda.empty_cache()
+        layer = Layer(_lib, spec, device, rank, args.warmup + args.e2e_steps + 4)
+    layers40 = None
+    if not args.no_extras and args.layers40_steps > 0:
+        del layer
+        torch.cuda.empty_cache()
+        layers40 = measure_layers40(_lib, torch, args, device, sampler)
         layer = Layer(_lib, spec, device, rank, args.warmup + args.e2e_steps + 4)
     clocks = sampler.finish() if sampler is not None else None
 
@@ -545,6 +642,20 @@ def run_native(args):
             "speedup_vs_conventional": o["conv_ms_per_step"] / o["ms_per_step"],
             "modelled_traffic_ratio": o["bytes_per_step"] / o["conv_bytes_per_step"],
         }
+    if layers40 is not None:
+        ms40 = layers40["ms_per_step"]
+        line["layers40_churn"] = {
+            "workload": "40 independent Mamba-2 layer pools (Nemotron-3-Super shapes), batch 256, fp32 checkpoints, "
+                        "L 16, continuous batching: rows leave and new requests join every 8 steps at random offsets",
+            "ms_per_step": ms40,
+            "ms_per_layer_step": ms40 / layers40["layers"],
+            "tokens_per_s": world * B / (ms40 / 1e3),
+            "tokens_per_s_per_layer": world * B * layers40["layers"] / (ms40 / 1e3),
+            "hbm_gbs": layers40["bytes_per_step"] / (ms40 / 1e3) / 1e9,
+            "frac": layers40["bytes_per_step"] / (ms40 / 1e3) / 1e9 / peak,
+            "steps": layers40["steps"],
+            "joins": layers40["joins"],
+        }
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -592,7 +703,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--e2e-steps", type=int, default=256)
+    ap.add_argument("--layers40-steps", type=int, default=64, help="steps of the 40-layer churn loop (0: skip)")
+    ap.add_argument("--sweep", action="store_true", help="batch x L x checkpoint dtype sweep (JSON lines)")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.warmup < 3 and args.impl == "native" and not args.eager:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

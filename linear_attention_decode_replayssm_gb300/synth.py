@@ -100,6 +100,7 @@ class Workload:
     num_slots: int = 0
     pad_rows: int = 0          # rows (chosen at random) whose slot is -1
     permute_slots: bool = False
+    cursor0: np.ndarray = None  # optional starting decode steps [B] (else drawn)
     # filled by build()
     slot_idx: np.ndarray = field(default=None, repr=False)
     decode_step0: np.ndarray = field(default=None, repr=False)
@@ -121,7 +122,9 @@ class Workload:
         if self.pad_rows:
             slots[r.choice(self.B, self.pad_rows, replace=False)] = -1
         self.slot_idx = slots
-        if self.stagger:
+        if self.cursor0 is not None:
+            self.decode_step0 = np.asarray(self.cursor0, dtype=np.int64).copy()
+        elif self.stagger:
             self.decode_step0 = r.integers(0, self.L, size=self.B).astype(np.int64)
         else:
             self.decode_step0 = np.zeros(self.B, dtype=np.int64)
@@ -207,3 +210,66 @@ def make_workload(name, seed=0, **overrides):
     spec = dict(SPECS[name])
     spec.update(overrides)
     return Workload(seed=seed, **spec).build()
+
+
+# ---------------------------------------------------------------------------
+# continuous batching: rows leave and new requests take their slots
+# ---------------------------------------------------------------------------
+class ChurnSchedule:
+    """Per-row decode-step counters under continuous batching.
+
+    Every ``period`` steps each row, at its own random offset, finishes with
+    probability ``p_churn``; a new request takes the same batch position and
+    slot at decode step 0 with a fresh checkpoint (stand-in for its prefill
+    state).  The slot's ring is left as it was: the cursor restarts at 0, so
+    no stale record is ever read ("[Kernel] ReplaySSM: cache SSM inputs for
+    faster Gated DeltaNet standard decode", §CUDA graphs and continuous
+    batching: recycled blocks need no zero-init).
+    """
+
+    def __init__(self, B, L, steps, period=8, p_churn=0.25, seed=0, decode_step0=None):
+        r = _rng(seed, 7)
+        self.B, self.L, self.steps = B, L, steps
+        self.offset = r.integers(0, period, size=B)
+        churn = np.zeros((steps, B), dtype=bool)
+        for t in range(1, steps):
+            due = (t % period) == self.offset
+            churn[t] = due & (r.random(B) < p_churn)
+        self.join = churn  # [steps, B]: a new request starts at this step
+        ds = np.empty((steps, B), dtype=np.int64)
+        cur = np.zeros(B, dtype=np.int64) if decode_step0 is None else np.asarray(decode_step0, dtype=np.int64).copy()
+        for t in range(steps):
+            cur = np.where(churn[t], 0, cur)
+            ds[t] = cur
+            cur = cur + 1
+        self.decode_steps = ds  # [steps, B]
+
+    def decode_step(self, t):
+        return self.decode_steps[t]
+
+    def joins(self, t):
+        return np.nonzero(self.join[t])[0]
+
+
+# ---------------------------------------------------------------------------
+# the same laws drawn on a CUDA device (for GiB-sized workloads)
+# ---------------------------------------------------------------------------
+def device_draw(shape, law, generator, device="cuda", d_k=None):
+    """Draw a float32 tensor on the device from one of the input laws:
+    'scaled' N(0,1)/sqrt(d_k), 'unit' N(0,1) L2-normalised over the last axis,
+    'sigmoid3' sigmoid(N(3,1)), 'logsigmoid3' log(sigmoid(N(3,1))),
+    'sigmoid0' sigmoid(N(0,1))."""
+    import torch
+
+    x = torch.randn(*shape, generator=generator, device=device, dtype=torch.float32)
+    if law == "scaled":
+        return x / float(np.sqrt(d_k))
+    if law == "unit":
+        return x / x.norm(dim=-1, keepdim=True)
+    if law == "sigmoid3":
+        return torch.sigmoid(x + 3.0)
+    if law == "logsigmoid3":
+        return torch.log(torch.sigmoid(x + 3.0))
+    if law == "sigmoid0":
+        return torch.sigmoid(x)
+    raise ValueError(law)
