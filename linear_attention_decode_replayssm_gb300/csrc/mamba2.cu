@@ -72,15 +72,12 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   constexpr int NC = NCW * 32;       // consumer threads per group
   constexpr int RPP = NC / G;        // state rows per pass of a group
   constexpr int VPT = DV / RPP;      // state rows per consumer thread
-  constexpr int RPW = DV / NCW;      // output rows per warp in the output phase
-  constexpr int JG = 32 / RPW;       // lanes sharing one output row (split over records)
   constexpr int RDT = Rec<RT>::kDtype;
   constexpr int RES = (int)sizeof(RT);
   constexpr int PROD = NGRP * NCW;   // warp index of the producer
   constexpr uint32_t CKB = DV * DK * (uint32_t)sizeof(TC);
   static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && DV % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
-  static_assert(DV % NCW == 0 && 32 % RPW == 0 && JG >= 1, "bad output tiling");
   static_assert(DK % 8 == 0 && DV % 8 == 0, "head dims must be multiples of 8");
 
   extern __shared__ __align__(128) unsigned char smem[];
@@ -212,8 +209,6 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   const int lw = warp - grp * NCW;  // warp within the group
   const int ctid = tid - grp * NC;  // 0 .. NC-1
   const int row0 = ctid / G, cv = ctid - (ctid / G) * G;
-  const int orow_l = lw * RPW + lane / JG;  // output row of this lane in the output phase
-  const int jg = lane - (lane / JG) * JG;   // its share of the records
   auto gsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(NC) : "memory"); };
   // row and head of the unit, stepped instead of divided
   const int ustep = NGRP * stride;
@@ -258,10 +253,8 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
     float *sW = scr, *sS = scr + L, *sC = scr + 2 * L, *sGam = scr + 2 * L + DV;
     const unsigned char *sk = st + lay.k, *sv = st + lay.v;
 
-    // window weights w_j (suffix products of the decays) and gamma; a flush
-    // needs them all, so one warp scans them; non-flush rows build their own
-    // below, off the critical path
-    if (flush && lw == 0) {
+    // window weights w_j (suffix products of the decays) and gamma
+    if (lw == 0) {
       float x0 = lane <= p ? sa[lane] : 1.f;
       float x1 = lane + 32 <= p ? sa[lane + 32] : 1.f;
       suffix_scan64(x0, x1, lane, [](float x, float y) { return x * y; });
@@ -277,27 +270,45 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
 
     float part[VPT];
     if (!flush) {
-      // k_j . q for every record of the window, one warp per record (q held
-      // in registers across the records)
-      constexpr int QPL = (DK + 127) / 128;  // 4-element chunks of q per lane
-      float qq[QPL][4];
-#pragma unroll
-      for (int i = 0; i < QPL; ++i)
-        if (lane * 4 + i * 128 < DK) lds_cols<4>(st + lay.q, lane * 4 + i * 128, RDT, qq[i]);
-      for (int j = lw; j <= p; j += NCW) {
-        float acc = 0.f;
+      // s_j = k_j . q: a warp takes records four at a time; each lane holds
+      // its 4-column chunk of q and accumulates four partial dots, and one
+      // transposed reduction finishes the chunk
+      {
+        constexpr int QPL = (DK + 127) / 128;  // 4-column chunks of q per lane
+        float qq[QPL][4];
 #pragma unroll
         for (int i = 0; i < QPL; ++i) {
-          const int cc = lane * 4 + i * 128;
-          if (cc < DK) {
-            float kk[4];
-            lds_cols<4>(sk, j * DK + cc, RDT, kk);
-            acc = fmaf(kk[0], qq[i][0], fmaf(kk[1], qq[i][1], fmaf(kk[2], qq[i][2], fmaf(kk[3], qq[i][3], acc))));
+          if (lane * 4 + i * 128 < DK) {
+            lds_cols<4>(st + lay.q, lane * 4 + i * 128, RDT, qq[i]);
+          } else {
+            qq[i][0] = qq[i][1] = qq[i][2] = qq[i][3] = 0.f;
           }
         }
+        for (int ch = lw; ch * 4 <= p; ch += NCW) {
+          float part4[4];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) sS[j] = acc;
+          for (int r = 0; r < 4; ++r) {
+            const int j = ch * 4 + r;
+            float acc = 0.f;
+            if (j <= p) {
+#pragma unroll
+              for (int i = 0; i < QPL; ++i) {
+                const int cc = lane * 4 + i * 128;
+                if (cc < DK) {
+                  float kk[4];
+                  lds_cols<4>(sk, j * DK + cc, RDT, kk);
+                  acc = fmaf(kk[0], qq[i][0], fmaf(kk[1], qq[i][1], fmaf(kk[2], qq[i][2], fmaf(kk[3], qq[i][3], acc))));
+                }
+              }
+            }
+            part4[r] = acc;
+          }
+          group_reduce<4, 32>(part4, lane);
+          if (group_reduce_writer<4, 32>(lane)) {
+            const int j = ch * 4 + group_reduce_index<4, 32>(lane);
+            if (j <= p) sS[j] = part4[0];
+          }
+        }
       }
       // checkpoint GEMV partials from the stage
 #pragma unroll
@@ -313,31 +324,39 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
       gsync();
 
-      // o_i = gamma c_i + sum_j w_j s_j v_j[i]: JG lanes per row split the
-      // records; each lane walks its records from the newest down, extending
-      // the suffix product w_j = prod_{l=j+1..p} alpha_l as it goes
-      {
-        float acc = 0.f, w = 1.f;
-        int j = jg + ((p - jg) / JG) * JG;  // this lane's newest record
-        if (jg <= p) {
-          for (int l = p; l > j; --l) w *= sa[l];
-          for (;;) {
-            acc = fmaf(w * sS[j], lds_elem(sv, j * DV + orow_l, RDT), acc);
-            if (j < JG) break;
+      // o = gamma c + sum_j w_j s_j v_j, by one warp: a lane covers 8 output
+      // rows (one 16-byte load of a v record) for every OG-th record, then
+      // lanes sharing rows add up; the other warps append the record
+      if (lw == 0) {
+        constexpr int RG = DV / 8;   // 8-row groups
+        constexpr int OG = 32 / RG;  // record groups
+        static_assert(DV % 8 == 0 && 32 % RG == 0 && OG >= 1, "bad output layout");
+        const int rg = lane % RG, og = lane / RG;
+        float acc[8];
 #pragma unroll
-            for (int l = 0; l < JG; ++l) w *= sa[j - l];
-            j -= JG;
-          }
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int j = og; j <= p; j += OG) {
+          const float cj = sW[j] * sS[j];
+          float vv[8];
+          lds_cols<8>(sv, j * DV + rg * 8, RDT, vv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = fmaf(cj, vv[e], acc[e]);
         }
-        // lane jg = 0 ends at record 0 with w = w_0, so gamma = w_0 * alpha_0
-        const float gam = w * sa[0];
 #pragma unroll
-        for (int off = JG / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (jg == 0) orow[orow_l] = fmaf(gam, sC[orow_l], acc);
+        for (int off = RG; off < 32; off <<= 1) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+        }
+        if (og == 0) {
+          const float gam = sGam[0];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) orow[rg * 8 + e] = fmaf(gam, sC[rg * 8 + e], acc[e]);
+        }
       }
       // append the current record (k, v verbatim, alpha) at ring slot p
       constexpr int KCH = DK * RES / 16, VCH = DV * RES / 16;
-      for (int c = ctid; c < KCH + VCH; c += NC) {
+      constexpr int APP0 = NCW > 1 ? 32 : 0;  // warp 0 is busy with the output
+      for (int c = ctid - APP0; c >= 0 && c < KCH + VCH; c += NC - APP0) {
         if (c < KCH) {
           const uint4 x = reinterpret_cast<const uint4 *>(sk + (size_t)p * DK * RES)[c];
           reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.ring_k) + (unit * L + p) * DK * RES)[c] = x;
@@ -346,7 +365,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
           reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.ring_v) + (unit * L + p) * DV * RES)[c - KCH] = x;
         }
       }
-      if (ctid == 0) a.ring_a[unit * L + p] = sa[p];
+      if (ctid == NC - 1) a.ring_a[unit * L + p] = sa[p];
     } else {
       gsync();  // weights ready
       const float gam = sGam[0];
