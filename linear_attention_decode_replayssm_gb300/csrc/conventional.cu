@@ -17,34 +17,39 @@
 
 namespace rs {
 
-template <int DV, int DK, typename TC, int NT, bool DELTA>
+// A unit is RB = DV / NSPLIT state rows of one (row, head): the rows of the
+// update are independent once the row dots are known, so a 128 x 128 fp32
+// head is two 32 KiB units, the same shape as a 64 x 128 Mamba-2 head.
+template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT>
 __global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
   using V = CkVec<TC>;
+  constexpr int RB = DV / NSPLIT;
   constexpr int E = V::E;
   constexpr int G = DK / E;
   constexpr int RPP = NT / G;
-  constexpr int VPT = DV / RPP;
+  constexpr int VPT = RB / RPP;
   static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
-  static_assert(NT % G == 0 && DV % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
+  static_assert(NT % G == 0 && RB % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
 
-  __shared__ float sK[DK], sQ[DK], sV[DV], sU[DV], sC[DV];
+  __shared__ float sK[DK], sQ[DK], sV[RB], sU[RB], sC[RB];
 
   const int tid = threadIdx.x, lane = tid & 31;
-  const int b = blockIdx.x / a.H;
-  const int h = blockIdx.x - b * a.H;
-  float *orow = a.out + (size_t)b * a.so + (size_t)h * DV;
+  const int b = blockIdx.x / (a.H * NSPLIT);
+  const int rem = blockIdx.x - b * (a.H * NSPLIT);
+  const int h = rem / NSPLIT, row_off = (rem - h * NSPLIT) * RB;
+  float *orow = a.out + (size_t)b * a.so + (size_t)h * DV + row_off;
   const int slot = __ldg(a.slot_idx + b);
   if (slot < 0) {
-    for (int i = tid; i < DV; i += NT) orow[i] = 0.f;
+    for (int i = tid; i < RB; i += NT) orow[i] = 0.f;
     return;
   }
   if (slot >= a.num_slots) {
     if (tid == 0) report(a.dev_err, 1);
-    for (int i = tid; i < DV; i += NT) orow[i] = 0.f;
+    for (int i = tid; i < RB; i += NT) orow[i] = 0.f;
     return;
   }
   const size_t unit = (size_t)slot * a.H + h;
-  TC *st = static_cast<TC *>(a.ckpt) + unit * (size_t)(DV * DK);
+  TC *st = static_cast<TC *>(a.ckpt) + unit * (size_t)(DV * DK) + (size_t)row_off * DK;
   const int row0 = tid / G, cv = tid - (tid / G) * G;
 
   uint4 raw[VPT];
@@ -61,9 +66,9 @@ __global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
       sQ[idx * 8 + e] = g[e];
     }
   }
-  for (int idx = tid; idx < DV / 8; idx += NT) {
+  for (int idx = tid; idx < RB / 8; idx += NT) {
     float f[8];
-    load8(a.v, (size_t)b * a.sv + (size_t)h * DV + idx * 8, a.in_dtype, f);
+    load8(a.v, (size_t)b * a.sv + (size_t)h * DV + row_off + idx * 8, a.in_dtype, f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) sV[idx * 8 + e] = f[e];
   }
@@ -95,7 +100,7 @@ __global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
     if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
     __syncthreads();
     const float beta = __ldg(a.beta + (size_t)b * a.H + h);
-    for (int i = tid; i < DV; i += NT) sU[i] = beta * (sV[i] - alpha * sC[i]);
+    for (int i = tid; i < RB; i += NT) sU[i] = beta * (sV[i] - alpha * sC[i]);
     __syncthreads();
   }
 
@@ -116,12 +121,12 @@ __global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
   group_reduce<VPT, G>(part, lane);
   if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
   __syncthreads();
-  for (int i = tid; i < DV; i += NT) orow[i] = sC[i];
+  for (int i = tid; i < RB; i += NT) orow[i] = sC[i];
 }
 
-template <int DV, int DK, typename TC, int NT, bool DELTA>
+template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT = 1>
 static cudaError_t launch_conv(const KArgs &a, cudaStream_t s) {
-  conventional_kernel<DV, DK, TC, NT, DELTA><<<(unsigned)((size_t)a.B * a.H), NT, 0, s>>>(a);
+  conventional_kernel<DV, DK, TC, NT, DELTA, NSPLIT><<<(unsigned)((size_t)a.B * a.H * NSPLIT), NT, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -130,7 +135,7 @@ static LaunchFn find_conv_t(int d_v, int d_k, int ckpt_dtype) {
   if (ckpt_dtype == kF32) {
     if (d_v == 16 && d_k == 32) return launch_conv<16, 32, float, 128, DELTA>;
     if (d_v == 64 && d_k == 128) return launch_conv<64, 128, float, 256, DELTA>;
-    if (d_v == 128 && d_k == 128) return launch_conv<128, 128, float, 512, DELTA>;
+    if (d_v == 128 && d_k == 128) return launch_conv<128, 128, float, 256, DELTA, 2>;
   } else if (ckpt_dtype == kF16) {
     if (d_v == 16 && d_k == 32) return launch_conv<16, 32, __half, 64, DELTA>;
     if (d_v == 64 && d_k == 128) return launch_conv<64, 128, __half, 256, DELTA>;

@@ -34,6 +34,7 @@
 // bounded and report RS_DERR_TIMEOUT instead of hanging.
 #include "common.cuh"
 #include "launch.h"
+#include "replayssm.h"
 
 namespace rs {
 
@@ -52,29 +53,28 @@ __host__ __device__ inline GdnRec gdn_rec(int RB, int DK, int res, int ies, int 
   s.vt = o;   o = align128(o + RB * ies);
   s.a = o;    o = align128(o + (L + 4) * 4);     // g_0..g_{p-1}; [L] = g_t, [L+1] = beta_t
   s.meta = o; o = align128(o + 16);
-  s.scr = o;  o = align128(o + (3 * L + 4 * RB + 4) * 4);  // G_j, k_j.k_t, k_j.q_t, row dots, d_t, o
+  s.scr = o;  o = align128(o + (3 * L + 5 * RB + 4) * 4);  // G_j, k_j.k_t, k_j.q_t, row dots, d_t, o / row sums
   s.bytes = o;
   return s;
 }
 
 __host__ __device__ inline uint32_t gdn_head(int nsr, int nsc) { return align128(8 * (2 * nsr + nsc) + 16); }
 
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT>
-__global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
+// LMAX bounds the buffer length at compile time (L <= LMAX): loops over a
+// window's records unroll to a fixed count with predicated bodies.
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP, int LMAX>
+__global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr int RB = DV / NSPLIT;    // state rows per unit
   constexpr int E = V::E;
   constexpr int G = DK / E;          // lanes per state row
-  constexpr int NC = NCW * 32;       // consumer threads
+  constexpr int NC = NCW * 32;       // consumer threads per group
   constexpr int RPP = NC / G;        // state rows per pass
   constexpr int VPT = RB / RPP;      // state rows per consumer thread
-  constexpr int RPW = RB / NCW;      // rows per warp in the per-row phase
-  constexpr int JG = 32 / RPW;       // lanes sharing a row (split over records)
-  constexpr int PROD = NCW;          // warp index of the producer
+  constexpr int PROD = NGRP * NCW;   // warp index of the producer
   constexpr uint32_t CKB = RB * DK * (uint32_t)sizeof(TC);
   static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && RB % RPP == 0 && VPT >= 1 && 2 * VPT <= G, "bad tiling");
-  static_assert(RB % NCW == 0 && 32 % RPW == 0 && JG >= 1, "bad row tiling");
   static_assert(DK % 8 == 0 && RB % 8 == 0, "head dims must be multiples of 8");
 
   extern __shared__ __align__(128) unsigned char smem[];
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
   if (tid == 0) {
     for (int s = 0; s < nsr; ++s) {
       mbar_init(&full[s], 33);
-      mbar_init(&rec_empty[s], NC);
+      mbar_init(&rec_empty[s], NC);  // every thread of the consuming group
     }
     for (int c = 0; c < nsc; ++c) mbar_init(&ck_empty[c], NC);
     *s_abort = 0;
@@ -168,11 +168,19 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
           constexpr int KC = DK * res / 16, DC = RB * res / 16, ITC = DK * ies / 16, VTC = RB * ies / 16;
           const unsigned char *rk = static_cast<const unsigned char *>(a.ring_k) + unit * L * DK * res;
           const unsigned char *rd = static_cast<const unsigned char *>(a.ring_v);
-          for (int cc = lane; cc < p * KC; cc += 32) cp_async16(st + lay.k + cc * 16, rk + cc * 16);
-          for (int cc = lane; cc < p * DC; cc += 32) {
-            const int jj = cc / DC;
-            cp_async16(st + lay.d + cc * 16,
-                       rd + ((unit * L + jj) * DV + row_off) * res + (size_t)(cc - jj * DC) * 16);
+#pragma unroll
+          for (int i = 0; i < (LMAX * KC + 31) / 32; ++i) {
+            const int cc = lane + 32 * i;
+            if (cc < p * KC) cp_async16(st + lay.k + cc * 16, rk + cc * 16);
+          }
+#pragma unroll
+          for (int i = 0; i < (LMAX * DC + 31) / 32; ++i) {
+            const int cc = lane + 32 * i;
+            if (cc < p * DC) {
+              const int jj = cc / DC;
+              cp_async16(st + lay.d + cc * 16,
+                         rd + ((unit * L + jj) * DV + row_off) * res + (size_t)(cc - jj * DC) * 16);
+            }
           }
           const unsigned char *kin =
               static_cast<const unsigned char *>(a.k) + ((size_t)b * a.sk + (size_t)h * DK) * ies;
@@ -186,7 +194,11 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
           }
           for (int cc = lane; cc < VTC; cc += 32) cp_async16(st + lay.vt + cc * 16, vin + cc * 16);
           float *sa = reinterpret_cast<float *>(st + lay.a);
-          for (int jj = lane; jj < p; jj += 32) cp_async4(sa + jj, a.ring_a + unit * L + jj);
+#pragma unroll
+          for (int i = 0; i < (LMAX + 31) / 32; ++i) {
+            const int jj = lane + 32 * i;
+            if (jj < p) cp_async4(sa + jj, a.ring_a + unit * L + jj);
+          }
           if (lane == 30) cp_async4(sa + L, a.alpha + (size_t)b * a.H + h);
           if (lane == 31) cp_async4(sa + L + 1, a.beta + (size_t)b * a.H + h);
         } else if (lane == 0) {
@@ -206,16 +218,18 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
   }
 
   // ------------------------------------------------------------------ consumers
-  const int lw = warp, ctid = tid;
+  // group g takes the CTA's units g, g + NGRP, ...; each group has its own
+  // named barrier, so the groups run independently of each other
+  const int grp = warp / NCW;
+  const int lw = warp - grp * NCW, ctid = tid - grp * NC;
   const int row0 = ctid / G, cv = ctid - (ctid / G) * G;
-  const int prow = lw * RPW + lane / JG;  // row of this lane in the per-row phase
-  const int jg = lane - (lane / JG) * JG;
-  for (int it = 0; ; ++it) {
+  auto gsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(NC) : "memory"); };
+  for (int it = grp; ; it += NGRP) {
     const int u = blockIdx.x + it * stride;
     if (u >= n_units) break;
     const int s = it % nsr, c = it % nsc;
     if (lane == 0 && !mbar_wait(&full[s], (uint32_t)(it / nsr) & 1u)) *(volatile int *)s_abort = 1;
-    consumer_sync<NC>();
+    gsync();
     if (*(volatile int *)s_abort) break;
 
     const unsigned char *st = rec_slots + (size_t)s * lay.bytes;
@@ -244,7 +258,7 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
     const float *sa = reinterpret_cast<const float *>(st + lay.a);
     float *scr = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + lay.scr);
     float *sW = scr, *sDk = scr + L, *sDq = scr + 2 * L;
-    float *sAk = scr + 3 * L, *sAq = sAk + RB, *sDt = sAq + RB, *sC = sDt + RB, *sScal = sC + RB;
+    float *sAk = scr + 3 * L, *sAq = sAk + RB, *sDt = sAq + RB, *sC = sDt + RB, *sScal = sC + 2 * RB;
     const unsigned char *sk = st + lay.k, *skt = st + lay.kt, *sq = st + lay.q, *sd = st + lay.d;
 
     // decay weights over the held records (warp 0)
@@ -259,48 +273,64 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
       if (lane + 32 < p) sW[lane + 32] = expf(lane == 31 ? 0.f : n1);
       if (lane == 0) sScal[0] = expf(x0);
     }
-    // k_j . k_t and k_j . q_t for the held records, k_t . q_t at j == p
-    // (this lane's chunks of k_t and q_t stay in registers across records)
-    constexpr int QPL = (DK + 127) / 128;
-    float kt4[QPL][4], q4[QPL][4];
-#pragma unroll
-    for (int i = 0; i < QPL; ++i) {
-      if (lane * 4 + i * 128 < DK) {
-        lds_cols<4>(skt, lane * 4 + i * 128, idt, kt4[i]);
-        lds_cols<4>(sq, lane * 4 + i * 128, idt, q4[i]);
-      }
-    }
-    for (int j = lw; j <= p; j += NCW) {
-      float dk = 0.f, dq = 0.f;
+    // k_j . k_t and k_j . q_t for the held records (k_t . q_t at j == p): a
+    // warp takes records four at a time; each lane holds its 4-column chunks
+    // of k_t and q_t and accumulates 2 x 4 partial dots, and one transposed
+    // reduction finishes the chunk
+    {
+      constexpr int QPL = (DK + 127) / 128;
+      float kt4[QPL][4], q4[QPL][4];
 #pragma unroll
       for (int i = 0; i < QPL; ++i) {
-        const int cc = lane * 4 + i * 128;
-        if (cc < DK) {
-          float kk[4];
-          if (j < p) {
-            lds_cols<4>(sk, j * DK + cc, rdt, kk);
-          } else {
+        if (lane * 4 + i * 128 < DK) {
+          lds_cols<4>(skt, lane * 4 + i * 128, idt, kt4[i]);
+          lds_cols<4>(sq, lane * 4 + i * 128, idt, q4[i]);
+        } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) kk[e] = kt4[i][e];
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            dk = fmaf(kk[e], kt4[i][e], dk);
-            dq = fmaf(kk[e], q4[i][e], dq);
-          }
+          for (int e = 0; e < 4; ++e) kt4[i][e] = q4[i][e] = 0.f;
         }
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        dk += __shfl_xor_sync(0xffffffffu, dk, off);
-        dq += __shfl_xor_sync(0xffffffffu, dq, off);
-      }
-      if (lane == 0) {
-        if (j < p) {
-          sDk[j] = dk;
-          sDq[j] = dq;
-        } else {
-          sScal[1] = dq;
+      for (int ci = 0; ci < (LMAX / 4 + NCW - 1) / NCW; ++ci) {
+        const int ch = lw + ci * NCW;
+        if (ch * 4 > p) break;
+        float part8[8];  // [0..3]: k_j . k_t, [4..7]: k_j . q_t
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int j = ch * 4 + r;
+          float dk = 0.f, dq = 0.f;
+          if (j <= p) {
+#pragma unroll
+            for (int i = 0; i < QPL; ++i) {
+              const int cc = lane * 4 + i * 128;
+              if (cc < DK) {
+                float kk[4];
+                if (j < p) {
+                  lds_cols<4>(sk, j * DK + cc, rdt, kk);
+                } else {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) kk[e] = kt4[i][e];
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  dk = fmaf(kk[e], kt4[i][e], dk);
+                  dq = fmaf(kk[e], q4[i][e], dq);
+                }
+              }
+            }
+          }
+          part8[r] = dk;
+          part8[4 + r] = dq;
+        }
+        group_reduce<8, 32>(part8, lane);
+        if (group_reduce_writer<8, 32>(lane)) {
+          const int vi = group_reduce_index<8, 32>(lane);
+          const int j = ch * 4 + (vi & 3);
+          if (j < p) {
+            if (vi < 4) sDk[j] = part8[0]; else sDq[j] = part8[0];
+          } else if (j == p && vi >= 4) {
+            sScal[1] = part8[0];
+          }
         }
       }
     }
@@ -332,35 +362,51 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
           sAq[row0 + (vi - VPT) * RPP] = part[0];
       }
     }
-    consumer_sync<NC>();
+    gsync();
 
-    // per row: S_{t-1} k_t, S_{t-1} q_t, then d_t (JG lanes split the records)
+    // per row: S_{t-1} k_t, S_{t-1} q_t, then d_t.  Warp lw takes RW rows
+    // (one vector load of a d record); its lanes split the records, one
+    // transposed reduction folds the 2 x RW sums, and lane r finishes row r.
     const float gam = sScal[0], kq = sScal[1];
     const float g_t = sa[L], beta_t = sa[L + 1];
     const float alpha_t = expf(g_t);
     {
-      float ak = 0.f, aq = 0.f;
-      for (int j = jg; j < p; j += JG) {
-        const float dj = sW[j] * lds_elem(sd, j * RB + prow, rdt);
-        ak = fmaf(sDk[j], dj, ak);
-        aq = fmaf(sDq[j], dj, aq);
-      }
+      constexpr int RW = RB / NCW;  // rows per warp
+      static_assert(RB % NCW == 0 && (RW == 4 || RW == 8 || RW == 16), "bad row layout");
+      const int r0 = lw * RW;
+      float acc[2 * RW];  // [0, RW): S_{t-1} k_t terms, [RW, 2 RW): S_{t-1} q_t terms
 #pragma unroll
-      for (int off = JG / 2; off > 0; off >>= 1) {
-        ak += __shfl_xor_sync(0xffffffffu, ak, off);
-        aq += __shfl_xor_sync(0xffffffffu, aq, off);
-      }
-      if (jg == 0) {
-        ak = fmaf(gam, sAk[prow], ak);
-        aq = fmaf(gam, sAq[prow], aq);
-        const float d_t = beta_t * (lds_elem(st + lay.vt, prow, idt) - alpha_t * ak);
-        if (!flush) {
-          orow[prow] = fmaf(alpha_t, aq, d_t * kq);
-          store1(a.ring_v, (unit * L + p) * DV + row_off + prow, rdt, d_t);
-        } else {
-          sDt[prow] = d_t;
+      for (int e = 0; e < 2 * RW; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < (LMAX + 31) / 32; ++jj) {
+        const int j = lane + 32 * jj;
+        if (j >= p) break;
+        const float ck = sW[j] * sDk[j], cq = sW[j] * sDq[j];
+        float dd[RW];
+        lds_cols<RW>(sd, j * RB + r0, rdt, dd);
+#pragma unroll
+        for (int e = 0; e < RW; ++e) {
+          acc[e] = fmaf(ck, dd[e], acc[e]);
+          acc[RW + e] = fmaf(cq, dd[e], acc[RW + e]);
         }
       }
+      group_reduce<2 * RW, 32>(acc, lane);
+      float *sRow = sC + r0 * 2;  // sC (2 RB floats of scratch) holds this warp's sums
+      if (group_reduce_writer<2 * RW, 32>(lane)) sRow[group_reduce_index<2 * RW, 32>(lane)] = acc[0];
+      __syncwarp();
+      if (lane < RW) {
+        const int i = r0 + lane;
+        const float Ak = fmaf(gam, sAk[i], sRow[lane]);
+        const float Aq = fmaf(gam, sAq[i], sRow[RW + lane]);
+        const float d_t = beta_t * (lds_elem(st + lay.vt, i, idt) - alpha_t * Ak);
+        if (!flush) {
+          orow[i] = fmaf(alpha_t, Aq, d_t * kq);
+          store1(a.ring_v, (unit * L + p) * DV + row_off + i, rdt, d_t);
+        } else {
+          sDt[i] = d_t;
+        }
+      }
+      __syncwarp();
     }
     if (!flush) {
       if (half == 0) {
@@ -370,10 +416,10 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
           lds_cols<8>(skt, cc * 8, idt, f);
           store8(a.ring_k, (unit * L + p) * DK + cc * 8, rdt, f);
         }
-        if (ctid == 0) a.ring_a[unit * L + p] = g_t;
+        if (ctid == NC - 1) a.ring_a[unit * L + p] = g_t;
       }
     } else {
-      consumer_sync<NC>();  // d_t of every row ready
+      gsync();  // d_t of every row ready
       TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK) + (size_t)row_off * DK;
       const float scale0 = alpha_t * gam;
       float f[VPT][E];
@@ -383,6 +429,7 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
 #pragma unroll
         for (int e = 0; e < E; ++e) f[r][e] *= scale0;
       }
+#pragma unroll 4
       for (int j = 0; j < p; ++j) {
         float kk[E];
         lds_cols<E>(sk, j * DK + cv * E, rdt, kk);
@@ -409,7 +456,7 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
       }
       group_reduce<VPT, G>(po, lane);
       if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = po[0];
-      consumer_sync<NC>();
+      gsync();
       for (int i = ctid; i < RB; i += NC) orow[i] = sC[i];
     }
     mbar_arrive(&rec_empty[s]);
@@ -417,10 +464,10 @@ __global__ void __launch_bounds__(NCW * 32 + 32) gdn_replay_kernel(const KArgs a
   if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
 }
 
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT>
-static cudaError_t launch_gdn(const KArgs &a, cudaStream_t s) {
-  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT>;
-  constexpr int threads = NCW * 32 + 32;
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP, int LMAX>
+static cudaError_t launch_gdn_l(const KArgs &a, cudaStream_t s) {
+  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, LMAX>;
+  constexpr int threads = NGRP * NCW * 32 + 32;
   const size_t ckb = (size_t)(DV / NSPLIT) * DK * sizeof(TC);
   const size_t rb = gdn_rec(DV / NSPLIT, DK, (int)sizeof(RT), (int)sizeof(IT), a.L).bytes;
   RingPlan plan;
@@ -429,6 +476,13 @@ static cudaError_t launch_gdn(const KArgs &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   kern<<<plan.grid, threads, plan.smem, s>>>(a, plan.nsr, plan.nsc);
   return cudaGetLastError();
+}
+
+// the common short windows get a kernel unrolled for L <= 16
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP = 1>
+static cudaError_t launch_gdn(const KArgs &a, cudaStream_t s) {
+  return a.L <= 16 ? launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, 16>(a, s)
+                   : launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, RS_MAX_L>(a, s);
 }
 
 template <typename TC, typename RT, typename IT>

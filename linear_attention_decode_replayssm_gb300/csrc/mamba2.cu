@@ -33,6 +33,7 @@
 // No tensor cores: the step is a bandwidth-bound GEMV (about 0.6 FLOP/byte).
 #include "common.cuh"
 #include "launch.h"
+#include "replayssm.h"
 
 namespace rs {
 
@@ -64,7 +65,9 @@ __host__ __device__ inline M2Rec m2_rec(int DV, int DK, int rec_es, int L) {
 __host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(8 * (2 * nsr + nsc) + 16); }
 
 
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP>
+// LMAX bounds the buffer length at compile time (L <= LMAX): loops over a
+// window's records unroll to a fixed count with predicated bodies.
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, int LMAX>
 __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr int E = V::E;
@@ -177,13 +180,25 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
               static_cast<const unsigned char *>(a.v) + ((size_t)b * a.sv + (size_t)h * DV) * RES;
           const unsigned char *qin =
               static_cast<const unsigned char *>(a.q) + ((size_t)b * a.sq + (size_t)h * DK) * RES;
-          for (int cc = lane; cc < (p + 1) * KC; cc += 32)
-            cp_async16(st + lay.k + cc * 16, (cc < p * KC ? rk + cc * 16 : kin + (cc - p * KC) * 16));
-          for (int cc = lane; cc < (p + 1) * VC; cc += 32)
-            cp_async16(st + lay.v + cc * 16, (cc < p * VC ? rv + cc * 16 : vin + (cc - p * VC) * 16));
+#pragma unroll
+          for (int i = 0; i < (LMAX * KC + 31) / 32; ++i) {
+            const int cc = lane + 32 * i;
+            if (cc < (p + 1) * KC)
+              cp_async16(st + lay.k + cc * 16, (cc < p * KC ? rk + cc * 16 : kin + (cc - p * KC) * 16));
+          }
+#pragma unroll
+          for (int i = 0; i < (LMAX * VC + 31) / 32; ++i) {
+            const int cc = lane + 32 * i;
+            if (cc < (p + 1) * VC)
+              cp_async16(st + lay.v + cc * 16, (cc < p * VC ? rv + cc * 16 : vin + (cc - p * VC) * 16));
+          }
           for (int cc = lane; cc < KC; cc += 32) cp_async16(st + lay.q + cc * 16, qin + cc * 16);
           float *sa = reinterpret_cast<float *>(st + lay.a);
-          for (int jj = lane; jj < p; jj += 32) cp_async4(sa + jj, a.ring_a + unit * L + jj);
+#pragma unroll
+          for (int i = 0; i < (LMAX + 31) / 32; ++i) {
+            const int jj = lane + 32 * i;
+            if (jj < p) cp_async4(sa + jj, a.ring_a + unit * L + jj);
+          }
           if (lane == 31) cp_async4(sa + p, a.alpha + (size_t)b * a.H + h);
         } else if (lane == 0) {
           meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
@@ -284,7 +299,10 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
             qq[i][0] = qq[i][1] = qq[i][2] = qq[i][3] = 0.f;
           }
         }
-        for (int ch = lw; ch * 4 <= p; ch += NCW) {
+#pragma unroll
+        for (int ci = 0; ci < (LMAX / 4 + NCW - 1) / NCW; ++ci) {
+          const int ch = lw + ci * NCW;
+          if (ch * 4 > p) break;
           float part4[4];
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
@@ -335,12 +353,16 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int j = og; j <= p; j += OG) {
-          const float cj = sW[j] * sS[j];
-          float vv[8];
-          lds_cols<8>(sv, j * DV + rg * 8, RDT, vv);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] = fmaf(cj, vv[e], acc[e]);
+        for (int i = 0; i < (LMAX + OG - 1) / OG; ++i) {
+          const int j = og + i * OG;
+          if (j <= p) {
+            const float cj = sW[j] * sS[j];
+            float vv[8];
+            lds_cols<8>(sv, j * DV + rg * 8, RDT, vv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(cj, vv[e], acc[e]);
+          }
         }
 #pragma unroll
         for (int off = RG; off < 32; off <<= 1) {
@@ -377,6 +399,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
 #pragma unroll
         for (int e = 0; e < E; ++e) f[r][e] *= gam;
       }
+#pragma unroll 4
       for (int j = 0; j <= p; ++j) {
         float kk[E];
         lds_cols<E>(sk, j * DK + cv * E, RDT, kk);
@@ -406,9 +429,9 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
 }
 
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP>
-static cudaError_t launch_mamba2(const KArgs &a, cudaStream_t s) {
-  auto kern = mamba2_replay_kernel<DV, DK, TC, RT, NCW, NGRP>;
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, int LMAX>
+static cudaError_t launch_mamba2_l(const KArgs &a, cudaStream_t s) {
+  auto kern = mamba2_replay_kernel<DV, DK, TC, RT, NCW, NGRP, LMAX>;
   constexpr int threads = NGRP * NCW * 32 + 32;
   const size_t ckb = (size_t)DV * DK * sizeof(TC);
   const size_t rb = m2_rec(DV, DK, (int)sizeof(RT), a.L).bytes;
@@ -417,6 +440,13 @@ static cudaError_t launch_mamba2(const KArgs &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   kern<<<plan.grid, threads, plan.smem, s>>>(a, plan.nsr, plan.nsc);
   return cudaGetLastError();
+}
+
+// the common short windows get a kernel unrolled for L <= 16
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP>
+static cudaError_t launch_mamba2(const KArgs &a, cudaStream_t s) {
+  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, RT, NCW, NGRP, 16>(a, s)
+                   : launch_mamba2_l<DV, DK, TC, RT, NCW, NGRP, RS_MAX_L>(a, s);
 }
 
 template <typename RT>
