@@ -21,7 +21,8 @@ Sources, cited below by short name:
             Faster Hybrid Model Decoding".
 
 Modules
-  plan        per-row write cursor and flush flag            (closed form)
+  plan        per-row write cursor and flush flag, plain and align
+              (prefix-caching) mode                          (closed form)
   recurrence  conventional Mamba-2 and delta-rule steps, the window unroll and
               the output-only window formula                 (definitions)
   replay      the method's ckpt + ring bookkeeping, with the storage roundings
@@ -34,7 +35,7 @@ is recorded in its docstring: all are pinned by ``tests/test_oracle_*.py``
 against closed forms, invariants, brute force or numbers printed on the pages.
 """
 
-from .plan import plan_step, simulate_cursors
+from .plan import plan_step, simulate_cursors, plan_align, simulate_align
 from .recurrence import (
     mamba2_step,
     gdn_step,
@@ -49,6 +50,7 @@ from .replay import (
     ReplayState,
     exact_step,
     replay_step,
+    materialize,
 )
 from .storage import round_to, STORAGE_DTYPES
 from . import traffic
@@ -56,6 +58,8 @@ from . import traffic
 __all__ = [
     "plan_step",
     "simulate_cursors",
+    "plan_align",
+    "simulate_align",
     "mamba2_step",
     "gdn_step",
     "gdn_corrected_value",
@@ -67,6 +71,7 @@ __all__ = [
     "ReplayState",
     "exact_step",
     "replay_step",
+    "materialize",
     "round_to",
     "STORAGE_DTYPES",
     "traffic",

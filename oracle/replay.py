@@ -174,3 +174,32 @@ def replay_step(st, slot_idx, write_pos, is_flush, v, k, q, alpha, beta=None):
             st.ring_k[s, :, p] = round_to(k[b], st.ring_dtype)
             st.ring_a[s, :, p] = round_to(alpha[b], st.a_dtype)
     return o
+
+
+def materialize(rs, slot_idx, held, dst_dtype="f64"):
+    """Exact state of each row from its checkpoint and held records, without
+    touching either: what a prefix cache stores for a block boundary that did
+    not fall on a flush ([Ghana] §What actually shipped: a cached prefix needs
+    the exact state at a block boundary, and FlashInfer added a separate
+    materialisation kernel for it).
+
+    slot_idx [B] source slot (negative: row skipped, result left zero);
+    held [B] records the slot's ring holds (the cursor its next step would
+    get).  The state is the window unroll ([Ghana] §The identity; delta rule:
+    the (d, k, g) unroll) rounded once to ``dst_dtype``.
+    Returns S [B, H, d_v, d_k] float64.
+
+    Parity: pinned through ``unroll`` / ``gdn_unroll`` (identity tests) and by
+    ``tests/test_oracle_pins.py`` against the state ``exact_step`` reaches.
+    """
+    B = len(slot_idx)
+    _, H, d_v, d_k = rs.ckpt.shape
+    out = np.zeros((B, H, d_v, d_k))
+    rebuild = unroll if rs.variant == "mamba2" else gdn_unroll
+    for b in range(B):
+        s, p = int(slot_idx[b]), int(held[b])
+        if s < 0:
+            continue
+        out[b] = round_to(rebuild(rs.ckpt[s], rs.ring_a[s, :, :p], rs.ring_v[s, :, :p], rs.ring_k[s, :, :p]),
+                          dst_dtype)
+    return out

@@ -131,3 +131,37 @@ def test_flush_that_skips_current_token_is_caught(monkeypatch, variant):
 
     monkeypatch.setattr(oracle, "replay_step", bad)
     assert _fails(pins.test_replay_equals_exact_float64, variant, False)
+
+
+def test_align_anchor_at_block_start_only_is_caught(monkeypatch):
+    """Forgetting the decode-start anchor (cursor counted from the block start
+    even when decoding began inside the block) must fail a pin."""
+    def bad(position, start, L, block):
+        position = np.asarray(position, dtype=np.int64)
+        if block == 0:
+            return oracle.plan.plan_step(position - np.asarray(start), L)
+        wp = np.mod(position - (position // block) * block, L).astype(np.int32)
+        return wp, ((wp == L - 1) | (np.mod(position + 1, block) == 0)).astype(np.uint8)
+
+    monkeypatch.setattr(oracle, "plan_align", bad)
+    assert _fails(pins.test_plan_align_matches_ring_simulation, 4, 40, 5)
+    assert _fails(pins.test_plan_align_small_case_by_hand)
+
+
+def test_align_without_forced_flush_is_caught(monkeypatch):
+    def bad(position, start, L, block):
+        return oracle.plan.plan_step(np.asarray(position, dtype=np.int64) - np.asarray(start), L)
+
+    monkeypatch.setattr(oracle, "plan_align", bad)
+    assert _fails(pins.test_plan_align_matches_ring_simulation, 16, 40, 0)
+    assert _fails(pins.test_align_mode_checkpoint_is_exact_at_block_ends, "mamba2")
+
+
+def test_materialize_dropping_last_record_is_caught(monkeypatch):
+    good = oracle.replay.materialize
+
+    def bad(rs, slot_idx, held, dst_dtype="f64"):
+        return good(rs, slot_idx, np.maximum(np.asarray(held) - 1, 0), dst_dtype)
+
+    monkeypatch.setattr(oracle, "materialize", bad)
+    assert _fails(pins.test_align_mode_checkpoint_is_exact_at_block_ends, "gdn")

@@ -50,6 +50,47 @@ def test_plan_forced_flush_and_errors():
     assert fl.sum() == 100
 
 
+@pytest.mark.parametrize("L", [2, 4, 16])
+@pytest.mark.parametrize("block", [0, 1, 3, 6, 16, 40, 64])
+@pytest.mark.parametrize("start", [0, 5, 39, 41, 130])
+def test_plan_align_matches_ring_simulation(L, block, start):
+    n = 4 * max(L, block) + 7
+    wp_sim, fl_sim = oracle.simulate_align(start, n, L, block)
+    pos = start + np.arange(n)
+    wp, fl = oracle.plan_align(pos, np.full(n, start), L, block)
+    assert wp.dtype == np.int32 and fl.dtype == np.uint8
+    np.testing.assert_array_equal(wp, wp_sim)
+    np.testing.assert_array_equal(fl, fl_sim)
+    if block:
+        # every block-completing token flushes, and the next token starts an empty ring
+        done = (pos + 1) % block == 0
+        assert np.all(fl[done] == 1)
+        assert np.all(wp[1:][done[:-1]] == 0)
+
+
+def test_plan_align_small_case_by_hand():
+    # L = 4, blocks of 6 tokens, decoding from position 0: the second window
+    # of each block is cut short by the forced flush on the block's last token
+    wp, fl = oracle.plan_align(np.arange(12), np.zeros(12), 4, 6)
+    np.testing.assert_array_equal(wp, [0, 1, 2, 3, 0, 1, 0, 1, 2, 3, 0, 1])
+    np.testing.assert_array_equal(fl, [0, 0, 0, 1, 0, 1, 0, 0, 0, 1, 0, 1])
+    # decode starting inside a block (position 9 of blocks of 8): anchored at 9
+    wp, fl = oracle.plan_align(9 + np.arange(9), np.full(9, 9), 4, 8)
+    np.testing.assert_array_equal(wp, [0, 1, 2, 3, 0, 1, 2, 0, 1])
+    np.testing.assert_array_equal(fl, [0, 0, 0, 1, 0, 0, 1, 0, 0])
+
+
+def test_plan_align_reduces_to_plain_plan():
+    pos = np.arange(0, 500)
+    # align off: the plain plan of the decoded-token count
+    np.testing.assert_array_equal(oracle.plan_align(pos + 7, np.full(500, 7), 16, 0),
+                                  oracle.plan_step(pos, 16))
+    # blocks a multiple of L, decode from a block start: forced flushes coincide
+    np.testing.assert_array_equal(oracle.plan_align(pos, np.zeros(500), 16, 64), oracle.plan_step(pos, 16))
+    with pytest.raises(ValueError):
+        oracle.plan_align([3], [4], 16, 8)
+
+
 # --------------------------------------------------------------------------
 # storage roundings
 # --------------------------------------------------------------------------
@@ -419,3 +460,44 @@ def test_traffic_state_term_limit():
             total += M_S + (i - 1) * r          # read the state and the records before it
             total += M_S if i == L else r        # flush writes the state, others append
         assert total == traffic.replay_window_bytes(L, M_S, r)
+
+
+@pytest.mark.parametrize("variant", ["mamba2", "gdn"])
+def test_align_mode_checkpoint_is_exact_at_block_ends(variant):
+    """Align mode: the forced flush leaves the exact state in the checkpoint at
+    every block boundary, and materialising checkpoint + held records gives
+    the exact state after every step."""
+    r = _rng(7)
+    B, H, dv, dk, L, block, steps = 4, 2, 8, 16, 4, 6, 40
+    slots = np.array([2, 0, 3, 1], dtype=np.int32)
+    start = np.array([0, 3, 5, 11])
+    ckpt = r.standard_normal((4, H, dv, dk)) * 0.2
+    nan = lambda *sh: np.full(sh, np.nan)
+    rs = oracle.ReplayState(variant, ckpt, nan(4, H, L, dv), nan(4, H, L, dk), nan(4, H, L), "f64", "f64", "f64")
+    ex = oracle.ExactState(variant, ckpt.copy())
+    boundary_checks = 0
+    for t in range(steps):
+        pos = start + t
+        wp, fl = oracle.plan_align(pos, start, L, block)
+        v = r.standard_normal((B, H, dv))
+        k = r.standard_normal((B, H, dk))
+        q = r.standard_normal((B, H, dk))
+        if variant == "mamba2":
+            a, beta = r.uniform(0.5, 1.0, (B, H)), None
+        else:
+            k = _unit(k)
+            a, beta = np.log(r.uniform(0.5, 1.0, (B, H))), r.uniform(0, 1, (B, H))
+        oracle.replay_step(rs, slots, wp, fl, v, k, q, a, beta)
+        oracle.exact_step(ex, slots, v, k, q, a, beta)
+        held = np.where(fl != 0, 0, wp + 1)
+        S = oracle.materialize(rs, slots, held)
+        assert rel_err(S, ex.S[slots], nd=2) < 1e-11
+        done = (pos + 1) % block == 0
+        if done.any():
+            boundary_checks += int(done.sum())
+            assert rel_err(rs.ckpt[slots[done]], ex.S[slots[done]], nd=2) < 1e-11
+    assert boundary_checks >= 4 * (steps // block) - 4
+    # held = 0 returns the checkpoint itself; a padded row stays zero
+    S = oracle.materialize(rs, np.array([1, -1]), np.array([0, 2]))
+    np.testing.assert_array_equal(S[0], rs.ckpt[1])
+    assert np.all(S[1] == 0)
