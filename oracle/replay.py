@@ -27,6 +27,13 @@ indexed by the block table; null-padded slots are allowed, §Tests):
                  a state; [PR48792] review comment on S_{t-1} q_t and
                  S_{t-1} k_t).
 
+Two-precision checkpoint ([Ghana] §The precision argument, derived): a
+Mamba-2 ``ReplayState`` may carry a low-precision read copy ``ckpt_lp``.
+Non-flush steps start from the read copy; a flush starts from the recurrence
+copy ``ckpt`` and casts its unrounded result into both copies.  (Gated
+DeltaNet is left out: there the pages' flush recomputes the corrected values
+from raw cached v, a ring this layout does not keep.)
+
 Readings taken where the pages leave a step open:
   * The current token is record h = p + 1 of its window, where p = write_pos
     is the number of records already in the ring.  A flush folds those p
@@ -105,16 +112,31 @@ class ReplayState:
     ckpt_dtype: str = "f64"
     ring_dtype: str = "f64"
     a_dtype: str = "f32"
+    # two-precision checkpoint (Mamba-2): a low-precision read copy
+    ckpt_lp: np.ndarray = None
+    lp_dtype: str = None
 
     @property
     def L(self):
         return self.ring_a.shape[2]
+
+    def with_read_copy(self, lp_dtype):
+        """Add the low-precision read copy of the two-precision checkpoint
+        ([Ghana] §The precision argument, derived): the copy is cast from the
+        same values as the recurrence copy (here: the starting checkpoint)."""
+        if self.variant != "mamba2":
+            raise NotImplementedError("two-precision checkpoint: Mamba-2 only")
+        self.lp_dtype = lp_dtype
+        self.ckpt_lp = round_to(self.ckpt, lp_dtype)
+        return self
 
     def reset_slot(self, s, ckpt0):
         """A new request takes slot s: fresh checkpoint, ring left as it was
         ([PR48792] §CUDA graphs and continuous batching: the cursor is derived
         from decode_step mod L, so recycled blocks need no zero-init)."""
         self.ckpt[s] = np.asarray(ckpt0, dtype=np.float64)
+        if self.ckpt_lp is not None:
+            self.ckpt_lp[s] = round_to(ckpt0, self.lp_dtype)
 
 
 def _f64(x):
@@ -160,7 +182,10 @@ def replay_step(st, slot_idx, write_pos, is_flush, v, k, q, alpha, beta=None):
             raise ValueError(f"row {b}: write_pos {p} outside [0, {st.L})")
         recs = (st.ring_a[s, :, :p], st.ring_v[s, :, :p], st.ring_k[s, :, :p])
         if st.variant == "mamba2":
-            S_prev = unroll(st.ckpt[s], *recs)
+            # two-precision checkpoint: a non-flush step only reads, so it
+            # starts from the read copy; a flush starts from the recurrence copy
+            base = st.ckpt[s] if (st.ckpt_lp is None or is_flush[b]) else st.ckpt_lp[s]
+            S_prev = unroll(base, *recs)
             S_t, o[b] = mamba2_step(S_prev, alpha[b], v[b], k[b], q[b])
             new_v = v[b]
         else:
@@ -169,6 +194,8 @@ def replay_step(st, slot_idx, write_pos, is_flush, v, k, q, alpha, beta=None):
             S_t, o[b] = gdn_step(S_prev, alpha[b], beta[b], v[b], k[b], q[b])
         if is_flush[b]:
             st.ckpt[s] = round_to(S_t, st.ckpt_dtype)
+            if st.ckpt_lp is not None:  # both copies cast from the same unrounded matrix
+                st.ckpt_lp[s] = round_to(S_t, st.lp_dtype)
         else:
             st.ring_v[s, :, p] = round_to(new_v, st.ring_dtype)
             st.ring_k[s, :, p] = round_to(k[b], st.ring_dtype)

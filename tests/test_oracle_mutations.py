@@ -165,3 +165,46 @@ def test_materialize_dropping_last_record_is_caught(monkeypatch):
 
     monkeypatch.setattr(oracle, "materialize", bad)
     assert _fails(pins.test_align_mode_checkpoint_is_exact_at_block_ends, "gdn")
+
+
+def test_two_precision_flush_from_read_copy_is_caught(monkeypatch):
+    """A flush that starts from the low-precision read copy (so its rounding
+    enters the recurrence) must fail a pin."""
+    good = oracle.replay.replay_step
+
+    def bad(st, slot_idx, write_pos, is_flush, *args):
+        if st.ckpt_lp is not None:
+            hp = st.ckpt.copy()
+            st.ckpt[...] = st.ckpt_lp
+            o = good(st, slot_idx, write_pos, is_flush, *args)
+            keep = np.asarray(is_flush) == 0
+            for b, s in enumerate(slot_idx):
+                if keep[b]:
+                    st.ckpt[s] = hp[s]
+            return o
+        return good(st, slot_idx, write_pos, is_flush, *args)
+
+    monkeypatch.setattr(oracle, "replay_step", bad)
+    assert _fails(pins.test_two_precision_read_error_is_one_rounding, "f16")
+
+
+def test_two_precision_reading_the_recurrence_copy_is_caught(monkeypatch):
+    """Non-flush steps that read the recurrence copy instead of the read copy
+    (so no read error at all) must fail a pin."""
+    good = oracle.replay.replay_step
+
+    def bad(st, slot_idx, write_pos, is_flush, *args):
+        lp = st.ckpt_lp
+        st.ckpt_lp = None
+        try:
+            o = good(st, slot_idx, write_pos, is_flush, *args)
+        finally:
+            st.ckpt_lp = lp
+        if lp is not None:
+            for b, s in enumerate(slot_idx):
+                if is_flush[b]:
+                    lp[s] = oracle.round_to(st.ckpt[s], st.lp_dtype)
+        return o
+
+    monkeypatch.setattr(oracle, "replay_step", bad)
+    assert _fails(pins.test_two_precision_read_error_is_one_rounding, "bf16")

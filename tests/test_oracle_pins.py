@@ -501,3 +501,76 @@ def test_align_mode_checkpoint_is_exact_at_block_ends(variant):
     S = oracle.materialize(rs, np.array([1, -1]), np.array([0, 2]))
     np.testing.assert_array_equal(S[0], rs.ckpt[1])
     assert np.all(S[1] == 0)
+
+
+# --------------------------------------------------------------------------
+# two-precision checkpoint (Mamba-2): read copy for non-flush steps
+# --------------------------------------------------------------------------
+def _two_precision_run(lp_dtype, steps, alpha_lo, alpha_hi, L=4, H=2, dv=8, dk=16, seed=11, single=None):
+    """One row, recurrence copy in float64 and a read copy in ``lp_dtype``
+    (or, with ``single``, one checkpoint rounded to ``single`` at every flush).
+    Returns per-step outputs of the method and of the exact recurrence, the
+    flags, and the predicted read error of the pages' derivation."""
+    r = _rng(seed)
+    ckpt = r.standard_normal((1, H, dv, dk)) * 0.3
+    nan = lambda *sh: np.full(sh, np.nan)
+    rs = oracle.ReplayState("mamba2", ckpt.copy(), nan(1, H, L, dv), nan(1, H, L, dk), nan(1, H, L),
+                            ckpt_dtype=single or "f64", a_dtype="f64")
+    if single is None:
+        rs.with_read_copy(lp_dtype)
+    ex = oracle.ExactState("mamba2", ckpt.copy())
+    S_m = ckpt[0].copy()           # exact state at the last flush
+    gam = np.ones(H)               # decay since then
+    outs, exact, flags, predicted = [], [], [], []
+    for t in range(steps):
+        wp, fl = oracle.plan_step([t], L)
+        v = r.standard_normal((1, H, dv)) * 0.3
+        k = r.standard_normal((1, H, dk)) * 0.3
+        q = r.standard_normal((1, H, dk)) * 0.3
+        a = r.uniform(alpha_lo, alpha_hi, (1, H))
+        o_r = oracle.replay_step(rs, [0], wp, fl, v, k, q, a)
+        o_e = oracle.exact_step(ex, [0], v, k, q, a)
+        gam = gam * a[0]
+        if single is None:
+            eps = oracle.round_to(S_m, lp_dtype) - S_m
+            predicted.append(gam[:, None] * np.einsum("hij,hj->hi", eps, q[0]))
+        if fl[0]:
+            S_m = ex.S[0].copy()
+            gam = np.ones(H)
+        outs.append(o_r[0])
+        exact.append(o_e[0])
+        flags.append(int(fl[0]))
+    return np.array(outs), np.array(exact), np.array(flags), np.array(predicted) if predicted else None
+
+
+def test_two_precision_with_exact_read_copy_is_exact():
+    outs, exact, _, _ = _two_precision_run("f64", 40, 0.5, 1.0)
+    assert rel_err(outs, exact) < 1e-12
+
+
+@pytest.mark.parametrize("lp", ["f16", "bf16"])
+def test_two_precision_read_error_is_one_rounding(lp):
+    """The pages' derivation: a non-flush step h records after the last flush
+    errs by exactly gamma_h * eps_m * q, eps_m the read copy's rounding of the
+    flushed state; a flush step is exact (it starts from the recurrence copy)."""
+    outs, exact, flags, pred = _two_precision_run(lp, 48, 0.8, 1.0)
+    err = outs - exact
+    nf = flags == 0
+    assert np.abs(err[nf]).max() > 0                      # the read copy does err
+    np.testing.assert_allclose(err[nf], pred[nf], rtol=0, atol=1e-12 * np.abs(exact).max())
+    assert np.abs(err[~nf]).max() < 1e-12 * np.abs(exact).max()
+
+
+def test_two_precision_error_does_not_accumulate():
+    """Long-memory head: with separate copies the error stays at one rounding
+    of the latest checkpoint; one fp16 checkpoint rounded at every flush keeps
+    accumulating ([Ghana] §The precision argument, derived)."""
+    n, lo, hi = 2000, 0.9995, 0.99999
+    o2, e2, _, _ = _two_precision_run("f16", n, lo, hi, seed=5)
+    o1, e1, _, _ = _two_precision_run(None, n, lo, hi, seed=5, single="f16")
+    early, late = slice(8, 40), slice(n - 32, n)
+    two_early, two_late = rel_err(o2[early], e2[early]), rel_err(o2[late], e2[late])
+    one_early, one_late = rel_err(o1[early], e1[early]), rel_err(o1[late], e1[late])
+    assert two_late < 2.0 * two_early
+    assert one_late > 2.5 * one_early
+    assert two_late < one_late / 3.0
