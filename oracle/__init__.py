@@ -27,6 +27,8 @@ Modules
               the output-only window formula                 (definitions)
   replay      the method's ckpt + ring bookkeeping, with the storage roundings
               it performs, in float64 arithmetic             (algorithm steps)
+  spec        speculative verification with pointer commit (Mamba-2)
+                                                             (algorithm steps)
   storage     round-to-nearest-even casts to fp32 / fp16 / bf16
   traffic     the byte and FLOP model the pages price the method with
 
@@ -53,7 +55,7 @@ from .replay import (
     materialize,
 )
 from .storage import round_to, STORAGE_DTYPES
-from . import traffic
+from . import spec, traffic
 
 __all__ = [
     "plan_step",
@@ -74,5 +76,6 @@ __all__ = [
     "materialize",
     "round_to",
     "STORAGE_DTYPES",
+    "spec",
     "traffic",
 ]
