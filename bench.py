@@ -44,6 +44,10 @@ WORKLOADS = {
                          ring="bf16",
                          desc="Mamba-2 layer, Nemotron-3-Super shapes: batch 256, 128 heads, d_v 64, d_k 128, "
                               "fp32 checkpoint, bf16 v/k/q, fp32 alpha=sigmoid(N(3,1)), L 16, staggered cursors"),
+    "mamba2_bs256_lp16": dict(variant="mamba2", B=256, H=128, d_v=64, d_k=128, L=16, ckpt="f32", inp="bf16",
+                              ring="bf16", lp="f16",
+                              desc="Mamba-2 layer as mamba2_bs256 with a two-precision checkpoint: fp32 "
+                                   "recurrence copy, fp16 read copy for non-flush rows"),
     "gdn_bs256": dict(variant="gdn", B=256, H=32, d_v=128, d_k=128, L=16, ckpt="f32", inp="bf16", ring="f16",
                       desc="Gated DeltaNet layer: batch 256, 32 value heads of 128 x 128, fp32 checkpoint, "
                            "fp16 d/k rings, fp32 g ring, L 16, staggered cursors"),
@@ -247,6 +251,7 @@ class Layer:
         sk = math.sqrt(dk)
         self.ckpt = (randn(B, H, dv, dk) / sk).to(td[spec["ckpt"]])
         self.state = self.ckpt.clone() if with_state else None  # for the conventional kernel
+        self.ckpt_lp = self.ckpt.to(td[spec["lp"]]) if spec.get("lp") else None  # two-precision read copy
         self.ring_v = (randn(B, H, L, dv) / sk).to(td[spec["ring"]])
         self.ring_k = (unit(randn(B, H, L, dk)) if gdn else randn(B, H, L, dk) / sk).to(td[spec["ring"]])
         self.ring_a = decay(B, H, L)
@@ -285,7 +290,7 @@ class Layer:
         if self.spec["variant"] == "gdn":
             self.lib.replayssm_decode_gdn(beta=x["beta"], **kw)
         else:
-            self.lib.replayssm_decode_mamba2(**kw)
+            self.lib.replayssm_decode_mamba2(ckpt_lp=self.ckpt_lp, **kw)
 
     def conventional_step(self, t, stream=None):
         x = self.inputs[t % N_INPUT_SETS]
@@ -303,7 +308,7 @@ class Layer:
             tot += traffic.step_bytes(variant=s["variant"], H=s["H"], d_v=s["d_v"], d_k=s["d_k"],
                                       ckpt_dtype=s["ckpt"], in_dtype=s["inp"], ring_dtype=s["ring"],
                                       slot_idx=slot, write_pos=self.wp_host[t], is_flush=self.fl_host[t],
-                                      replay=replay)
+                                      replay=replay, lp_dtype=s.get("lp") if replay else None)
         return tot / (t1 - t0)
 
 
@@ -417,6 +422,93 @@ def measure_e2e(lib, torch, layer, steps, dist):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         el = float(tt.item())
     return el, h2d, d2h
+
+
+def measure_materialize(lib, torch, layer, args, sampler, launches=32):
+    """Prefix-cache materialisation of every row of the layer (checkpoint
+    unrolled with the records its ring holds, written to a separate pool),
+    device-timed over a CUDA graph of ``launches`` calls."""
+    import numpy as np
+
+    from linear_attention_decode_replayssm_gb300 import traffic
+
+    s = layer.spec
+    held_np = layer.wp_host[0].astype(np.int32)
+    held = torch.from_numpy(held_np).to(layer.device)
+    dst = torch.empty_like(layer.ckpt)
+    dst_idx = layer.slot_idx.flip(0).contiguous()
+    stream = torch.cuda.Stream(device=layer.device)
+    stream.wait_stream(torch.cuda.current_stream())
+
+    def one(t, st):
+        lib.replayssm_materialize(variant=layer.variant_code, ckpt=layer.ckpt, ring_v=layer.ring_v,
+                                  ring_k=layer.ring_k, ring_a=layer.ring_a, slot_idx=layer.slot_idx, held=held,
+                                  dst=dst, dst_idx=dst_idx, stream=st)
+
+    with torch.cuda.stream(stream):
+        for t in range(3):
+            one(t, stream)
+    ms = _timed_graph(torch, one, 0, launches, stream, args.eager, None, sampler)
+    nbytes = traffic.materialize_bytes(H=s["H"], d_v=s["d_v"], d_k=s["d_k"], ckpt_dtype=s["ckpt"],
+                                       ring_dtype=s["ring"], slot_idx=layer.slot_idx.cpu().numpy(), held=held_np)
+    del dst
+    return dict(ms_per_launch=ms / launches, bytes_per_launch=nbytes, launches=launches)
+
+
+def measure_spec(lib, torch, layer, args, sampler, T, steps=256, n_sets=4):
+    """Speculative verification of T drafts per row on the layer, with the
+    device-side commit of a seeded random number of accepted drafts (1..T),
+    both inside one CUDA graph of ``steps`` steps."""
+    import numpy as np
+
+    from linear_attention_decode_replayssm_gb300 import traffic
+
+    s, dev = layer.spec, layer.device
+    B, H, dv, dk, L = (s[k] for k in ("B", "H", "d_v", "d_k", "L"))
+    td = {"f32": torch.float32, "bf16": torch.bfloat16}[s["inp"]]
+    g = torch.Generator(device=dev)
+    g.manual_seed(31 + T)
+    sk = math.sqrt(dk)
+    sets = []
+    for _ in range(n_sets):
+        rn = lambda *sh: torch.randn(*sh, generator=g, device=dev)
+        sets.append(dict(v=(rn(B, T, H, dv) / sk).to(td), k=(rn(B, T, H, dk) / sk).to(td),
+                         q=(rn(B, T, H, dk) / sk).to(td), alpha=torch.sigmoid(3.0 + rn(B, T, H))))
+    rng = np.random.default_rng(T)
+    acc = rng.integers(1, T + 1, (steps + 3, B)).astype(np.int32)
+    h0 = (layer.decode_step0 % L).astype(np.int32)
+    # host walk of the commit rule, for the byte count of each step
+    hs, fls, h = [], [], h0.copy()
+    fl = lib.replayssm_plan_spec(h, L, T)
+    for t in range(steps + 3):
+        hs.append(h.copy())
+        fls.append(fl.copy())
+        h = (np.where(fl != 0, 0, h) + acc[t]).astype(np.int32)
+        fl = lib.replayssm_plan_spec(h, L, T)
+    acc_d = torch.from_numpy(acc).to(dev)
+    h_d = torch.from_numpy(h0).to(dev)
+    fl_d = torch.from_numpy(fls[0]).to(dev)
+    out = torch.empty(B, T, H, dv, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+
+    def one(t, st):
+        x = sets[t % n_sets]
+        lib.replayssm_spec_verify_mamba2(ckpt=layer.ckpt, ring_v=layer.ring_v, ring_k=layer.ring_k,
+                                         ring_a=layer.ring_a, slot_idx=layer.slot_idx, committed=h_d, is_flush=fl_d,
+                                         v=x["v"], k=x["k"], q=x["q"], alpha=x["alpha"], out=out, stream=st)
+        lib.replayssm_spec_commit(committed=h_d, is_flush=fl_d, accepted=acc_d[t], L=L, T=T, stream=st)
+
+    with torch.cuda.stream(stream):
+        for t in range(3):
+            one(t, stream)
+    ms = _timed_graph(torch, one, 3, steps + 3, stream, args.eager, None, sampler)
+    slot = layer.slot_idx.cpu().numpy()
+    nbytes = sum(traffic.spec_bytes(H=H, d_v=dv, d_k=dk, T=T, ckpt_dtype=s["ckpt"], in_dtype=s["inp"],
+                                    slot_idx=slot, committed=hs[t], is_flush=fls[t]) for t in range(3, steps + 3))
+    del sets
+    return dict(ms_per_step=ms / steps, bytes_per_step=nbytes / steps, T=T, steps=steps,
+                mean_accepted=float(acc[3:].mean()), flush_frac=float(np.mean([f.mean() for f in fls[3:]])))
 
 
 def measure_layers40(lib, torch, args, device, sampler):
@@ -543,13 +635,23 @@ def run_native(args):
     layer, main = measure_layer(_lib, torch, spec, device, args, dist, sampler, seed=rank)
     extra = {}
     if not args.no_extras:
-        other = "gdn_bs256" if args.workload == "mamba2_bs256" else "mamba2_bs256"
+        others = [n for n in WORKLOADS if n != args.workload]
         del layer
         torch.cuda.empty_cache()
-        _, o = measure_layer(_lib, torch, WORKLOADS[other], device, args, dist, sampler, seed=100 + rank)
-        extra[other] = o
-        torch.cuda.empty_cache()
+        for i, other in enumerate(others):
+            _, o = measure_layer(_lib, torch, WORKLOADS[other], device, args, dist, sampler, seed=100 + i + rank)
+            extra[other] = o
+            torch.cuda.empty_cache()
         layer = Layer(_lib, spec, device, rank, args.warmup + args.e2e_steps + 4)
+    mat, specs = None, []
+    if not args.no_extras:
+        mat = measure_materialize(_lib, torch, layer, args, sampler)
+        torch.cuda.empty_cache()
+        if spec["variant"] == "mamba2" and not spec.get("lp"):
+            for T in (4, 8):
+                specs.append(measure_spec(_lib, torch, layer, args, sampler, T))
+                torch.cuda.empty_cache()
+            layer = Layer(_lib, spec, device, rank, args.warmup + args.e2e_steps + 4)
     layers40 = None
     if not args.no_extras and args.layers40_steps > 0:
         del layer
@@ -641,6 +743,33 @@ def run_native(args):
             "conventional_hbm_gbs": o["conv_bytes_per_step"] / (o["conv_ms_per_step"] / 1e3) / 1e9,
             "speedup_vs_conventional": o["conv_ms_per_step"] / o["ms_per_step"],
             "modelled_traffic_ratio": o["bytes_per_step"] / o["conv_bytes_per_step"],
+        }
+    if mat is not None:
+        gbs = mat["bytes_per_launch"] / (mat["ms_per_launch"] / 1e3) / 1e9
+        line["materialize"] = {
+            "workload": "prefix-cache state materialisation of every row of the main workload's layer "
+                        "(checkpoint + held records read, state written to a separate pool)",
+            "ms_per_launch": mat["ms_per_launch"],
+            "rows_per_s": world * B / (mat["ms_per_launch"] / 1e3),
+            "hbm_gbs": gbs,
+            "frac": gbs / peak,
+            "algorithmic_bytes_per_launch": mat["bytes_per_launch"],
+            "launches": mat["launches"],
+        }
+    for sp in specs:
+        gbs = sp["bytes_per_step"] / (sp["ms_per_step"] / 1e3) / 1e9
+        line[f"spec_verify_T{sp['T']}"] = {
+            "workload": f"speculative verification of {sp['T']} drafts per row on the main workload's layer, "
+                        f"device-side commit of a random 1..{sp['T']} accepted drafts, one graph of "
+                        f"{sp['steps']} steps",
+            "ms_per_step": sp["ms_per_step"],
+            "vs_standard_step": sp["ms_per_step"] / ms,
+            "committed_tokens_per_s": world * B * sp["mean_accepted"] / (sp["ms_per_step"] / 1e3),
+            "mean_accepted": sp["mean_accepted"],
+            "flush_frac": sp["flush_frac"],
+            "hbm_gbs": gbs,
+            "frac": gbs / peak,
+            "algorithmic_bytes_per_step": sp["bytes_per_step"],
         }
     if layers40 is not None:
         ms40 = layers40["ms_per_step"]

@@ -16,6 +16,9 @@
  *   Mamba-2 non-flush ([Ghana] §Output without a state):
  *     o = gamma_{p+1} S_ckpt q + sum_{j=1..p+1} gamma_{j+1:p+1} v_j (k_j . q),
  *     then the record (alpha, v, k) is appended at ring slot p.
+ *   Two-precision checkpoint ([Ghana] §The precision argument, derived):
+ *     non-flush rows read a low-precision copy of the checkpoint, flushes
+ *     read the full-precision one and refresh both (rs_step_args.ckpt_lp).
  *   Mamba-2 flush ([Ghana] §The identity):
  *     S_new = gamma_{p+1} S_ckpt + sum_j gamma_{j+1:p+1} v_j k_j^T,
  *     o = S_new q (unrounded), S_ckpt <- S_new cast to the checkpoint type;
@@ -63,7 +66,7 @@ extern "C" {
 /* Same type as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st *rs_stream_t;
 
-#define RS_ABI_VERSION 1
+#define RS_ABI_VERSION 2
 #define RS_MAX_L 64 /* largest supported buffer length */
 
 typedef enum {
@@ -82,9 +85,11 @@ typedef enum { RS_MAMBA2 = 0, RS_GDN = 1 } rs_variant;
 typedef enum {
   RS_DERR_SLOT = 1,      /* slot_idx[b] >= num_slots */
   RS_DERR_WRITE_POS = 2, /* write_pos[b] outside [0, L) */
-  RS_DERR_TIMEOUT = 4    /* a pipeline wait gave up after 2 s: outputs of the
+  RS_DERR_TIMEOUT = 4,   /* a pipeline wait gave up after 2 s: outputs of the
                             call are incomplete (never expected; reported
                             instead of hanging the GPU) */
+  RS_DERR_DST = 8,       /* dst_idx[b] >= num_dst (replayssm_materialize) */
+  RS_DERR_ACCEPTED = 16  /* accepted[b] outside [1, T] (replayssm_spec_commit) */
 } rs_dev_error;
 
 /*
@@ -138,6 +143,15 @@ typedef struct rs_step_args {
   float *out;
   int64_t stride_v_row, stride_k_row, stride_q_row, stride_out_row; /* elements */
   int32_t *dev_err; /* optional device int32, see rs_dev_error */
+  /* Two-precision checkpoint (Mamba-2 only; NULL = one checkpoint copy):
+   * ckpt_lp [num_slots, H, d_v, d_k] of lp_dtype (RS_F16 or RS_BF16) is the
+   * read copy, ckpt (RS_F32) the recurrence copy.  A non-flush row reads
+   * only ckpt_lp; a flush row reads ckpt, and casts S_new into both copies,
+   * each rounded once (RN-even) from the same fp32 matrix.  The caller seeds
+   * ckpt_lp from the same state as ckpt when a request starts. */
+  void *ckpt_lp;
+  int32_t lp_dtype;
+  int32_t reserved2; /* must be 0 */
 } rs_step_args;
 
 /* RS_ABI_VERSION of the loaded library. */
@@ -158,6 +172,143 @@ int replayssm_supported(int variant, int d_v, int d_k, int ckpt_dtype);
  */
 int replayssm_plan_step(const int64_t *decode_step, const uint8_t *force_flush,
                         int32_t B, int32_t L, int32_t *write_pos, uint8_t *is_flush);
+
+/*
+ * Align (prefix-caching) mode step plan ([PR48792] §What this PR adds, the
+ * prefix-caching bullet, and §Tests; [Ghana] §What actually shipped).  A
+ * cached prefix needs the exact state at every cache-block boundary, and the
+ * checkpoint is exact only right after a flush, so the step that completes a
+ * block of `block` tokens is forced to flush and the ring is re-anchored at
+ * each block start:
+ *   anchor[b]    = max(start[b], floor(position[b] / block) * block),
+ *   write_pos[b] = (position[b] - anchor[b]) mod L,
+ *   is_flush[b]  = (write_pos[b] == L - 1) or ((position[b] + 1) mod block == 0).
+ * position [B]: absolute position of the token decoded this step (tokens
+ * before it); start [B]: position of the row's first decoded token (the
+ * prefill left an exact checkpoint covering the tokens before it).  block = 0
+ * turns align mode off: the plain plan of decode_step = position - start.
+ * Any L works with any block (L need not divide the block).  All HOST memory.
+ * Returns RS_OK, or RS_EINVAL (null pointer, B < 0, L outside [1, RS_MAX_L],
+ * block < 0, start < 0 or position < start: outputs untouched).
+ */
+int replayssm_plan_align(const int64_t *position, const int64_t *start, int32_t block, int32_t B,
+                         int32_t L, int32_t *write_pos, uint8_t *is_flush);
+
+/*
+ * State materialisation for prefix caching ([Ghana] §What actually shipped:
+ * between flushes only the checkpoint and the ring exist, so a separate
+ * kernel builds the exact state; §The identity for the unroll).  For each row
+ * b with p = held[b] records in its ring, writes
+ *   Mamba-2: S = gamma S_ckpt + sum_{j<p} w_j v_j k_j^T,
+ *            w_j = product of the decays of records j+1..p-1, gamma = all p;
+ *   GDN:     the same with d_j for v_j, w_j = exp(sum of g after j),
+ *            gamma = exp(sum of all p log-gates),
+ * rounded once (RN-even) to ckpt_dtype, into dst[dst_idx[b]].  The
+ * checkpoint and the ring are only read.  held[b] is the cursor the row's
+ * next decode step would get (write_pos + 1 after a non-flush step, 0 after
+ * a flush).
+ *
+ * Layouts: ckpt [num_slots, H, d_v, d_k] and dst [num_dst, H, d_v, d_k], both
+ * ckpt_dtype (RS_F32 or RS_F16); ring_v [num_slots, H, L, d_v], ring_k
+ * [num_slots, H, L, d_k] ring_dtype (RS_F32, RS_F16 or RS_BF16); ring_a
+ * [num_slots, H, L] fp32; slot_idx, held, dst_idx [B] int32.  All DEVICE
+ * pointers owned by the caller; ckpt, dst, ring_v, ring_k 16-byte aligned.
+ * A row with slot_idx or dst_idx negative is skipped.  dst may be ckpt itself
+ * when every row's dst_idx equals its slot_idx (an in-place fold: the caller
+ * then restarts the row's cursor at 0); otherwise dst must not overlap the
+ * checkpoints or rings the call reads, and two rows must not name the same
+ * dst slot.  Out-of-range slot_idx, dst_idx or held skip the row and set
+ * RS_DERR_SLOT, RS_DERR_DST or RS_DERR_WRITE_POS in *dev_err (when not NULL).
+ * variant is RS_MAMBA2 or RS_GDN.  Asynchronous on stream; graph-capturable.
+ */
+typedef struct rs_materialize_args {
+  int32_t B, H, d_v, d_k, L;
+  int32_t num_slots;  /* slots in the checkpoint and ring pools */
+  int32_t num_dst;    /* slots in the destination pool */
+  int32_t ckpt_dtype; /* rs_dtype of ckpt and dst */
+  int32_t ring_dtype; /* rs_dtype of ring_v and ring_k */
+  int32_t reserved;   /* must be 0 */
+  const int32_t *slot_idx;
+  const int32_t *held;
+  const int32_t *dst_idx;
+  const void *ckpt;
+  const void *ring_v;
+  const void *ring_k;
+  const float *ring_a;
+  void *dst;
+  int32_t *dev_err; /* optional device int32, see rs_dev_error */
+} rs_materialize_args;
+
+int replayssm_materialize(const rs_materialize_args *args, int variant, rs_stream_t stream);
+
+/*
+ * Speculative verification, Mamba-2 ([Ghana] §Speculative decoding: rollback
+ * becomes a pointer; [NV] §Benefit 2, output-only evaluation).  Each row
+ * holds h = committed[b] records in its ring (0 <= h <= L) and verifies T
+ * draft tokens (1 <= T <= 16, T <= L):
+ *   non-flush (h + T <= L): the drafts' records go to ring slots h..h+T-1
+ *     and draft i's output is the state after the h committed records and
+ *     drafts 0..i, applied to q_i, evaluated without forming that state;
+ *   flush (is_flush[b], set when h + T > L): the h committed records are
+ *     folded into the checkpoint first (stored, cast to ckpt_dtype), then the
+ *     drafts go to ring slots 0..T-1 and their outputs run from the unrounded
+ *     folded state.
+ * Nothing is committed here: after sampling, replayssm_spec_commit advances
+ * the committed count by the accepted drafts; rejected records are simply
+ * overwritten later (rollback is a pointer move).
+ *
+ * Layouts: ckpt [num_slots, H, d_v, d_k] ckpt_dtype (RS_F32 | RS_F16);
+ * ring_v [num_slots, H, L, d_v], ring_k [num_slots, H, L, d_k] in in_dtype
+ * (records are the inputs verbatim), ring_a [num_slots, H, L] fp32;
+ * v [B, T, H, d_v], k, q [B, T, H, d_k] in_dtype (RS_BF16 | RS_F32), packed;
+ * alpha [B, T, H] fp32; out [B, T, H, d_v] fp32; slot_idx, committed [B]
+ * int32; is_flush [B] uint8.  DEVICE pointers owned by the caller; ckpt,
+ * rings, v, k, q 16-byte aligned.  A padded row (slot_idx < 0) gets zero
+ * outputs.  An out-of-range slot or committed count (h > L, or h + T > L
+ * without is_flush) skips the row (zero outputs) and sets RS_DERR_SLOT /
+ * RS_DERR_WRITE_POS in *dev_err.  Asynchronous on stream; graph-capturable.
+ */
+typedef struct rs_spec_args {
+  int32_t B, H, d_v, d_k, L, T;
+  int32_t num_slots;
+  int32_t ckpt_dtype, in_dtype;
+  int32_t reserved; /* must be 0 */
+  const int32_t *slot_idx;
+  const int32_t *committed;
+  const uint8_t *is_flush;
+  const void *v;
+  const void *k;
+  const void *q;
+  const float *alpha;
+  void *ckpt;
+  void *ring_v;
+  void *ring_k;
+  float *ring_a;
+  float *out;
+  int32_t *dev_err;
+} rs_spec_args;
+
+int replayssm_spec_verify_mamba2(const rs_spec_args *args, rs_stream_t stream);
+
+/*
+ * Host plan of a verification step ([Ghana] §Speculative decoding: the flush
+ * rule depends only on h and T): is_flush[b] = committed[b] + T > L.  HOST
+ * memory.  RS_EINVAL for a null pointer, B < 0, L outside [1, RS_MAX_L], T
+ * outside [1, min(L, 16)] or committed[b] outside [0, L] (outputs untouched).
+ */
+int replayssm_plan_spec(const int32_t *committed, int32_t B, int32_t L, int32_t T, uint8_t *is_flush);
+
+/*
+ * Pointer commit after sampling, on the device so it can sit in the same
+ * CUDA graph as the verification: with a = accepted[b] in [1, T],
+ *   committed_out[b] = (is_flush[b] ? 0 : committed[b]) + a,
+ *   is_flush_out[b]  = committed_out[b] + T > L   (the next step's flag).
+ * DEVICE pointers; the outputs may alias the inputs.  An accepted count
+ * outside [1, T] commits nothing for that row and sets RS_DERR_ACCEPTED.
+ */
+int replayssm_spec_commit(const int32_t *committed, const uint8_t *is_flush, const int32_t *accepted,
+                          int32_t B, int32_t L, int32_t T, int32_t *committed_out, uint8_t *is_flush_out,
+                          int32_t *dev_err, rs_stream_t stream);
 
 /* ReplaySSM Mamba-2 cached decode step, non-flush and flush rows in one
  * launch (beta unused). */

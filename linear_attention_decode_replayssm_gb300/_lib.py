@@ -19,8 +19,8 @@ from . import build as _build
 RS_OK, RS_EINVAL, RS_EUNSUPPORTED, RS_EALIGN, RS_ECUDA = 0, -1, -2, -3, -4
 RS_F32, RS_F16, RS_BF16 = 0, 1, 2
 RS_MAMBA2, RS_GDN = 0, 1
-RS_DERR_SLOT, RS_DERR_WRITE_POS, RS_DERR_TIMEOUT = 1, 2, 4
-RS_ABI_VERSION = 1
+RS_DERR_SLOT, RS_DERR_WRITE_POS, RS_DERR_TIMEOUT, RS_DERR_DST, RS_DERR_ACCEPTED = 1, 2, 4, 8, 16
+RS_ABI_VERSION = 2
 RS_MAX_L = 64
 
 # every symbol include/replayssm.h declares
@@ -28,6 +28,11 @@ EXPORTS = (
     "replayssm_abi_version",
     "replayssm_supported",
     "replayssm_plan_step",
+    "replayssm_plan_align",
+    "replayssm_materialize",
+    "replayssm_spec_verify_mamba2",
+    "replayssm_plan_spec",
+    "replayssm_spec_commit",
     "replayssm_decode_mamba2",
     "replayssm_decode_gdn",
     "conventional_decode",
@@ -50,6 +55,34 @@ class StepArgs(ctypes.Structure):
         ("stride_v_row", ctypes.c_int64), ("stride_k_row", ctypes.c_int64),
         ("stride_q_row", ctypes.c_int64), ("stride_out_row", ctypes.c_int64),
         ("dev_err", ctypes.c_void_p),
+        ("ckpt_lp", ctypes.c_void_p), ("lp_dtype", ctypes.c_int32), ("reserved2", ctypes.c_int32),
+    ]
+
+
+class MaterializeArgs(ctypes.Structure):
+    """Mirror of ``rs_materialize_args``."""
+
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("d_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
+        ("L", ctypes.c_int32), ("num_slots", ctypes.c_int32), ("num_dst", ctypes.c_int32),
+        ("ckpt_dtype", ctypes.c_int32), ("ring_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("slot_idx", ctypes.c_void_p), ("held", ctypes.c_void_p), ("dst_idx", ctypes.c_void_p),
+        ("ckpt", ctypes.c_void_p), ("ring_v", ctypes.c_void_p), ("ring_k", ctypes.c_void_p),
+        ("ring_a", ctypes.c_void_p), ("dst", ctypes.c_void_p), ("dev_err", ctypes.c_void_p),
+    ]
+
+
+class SpecArgs(ctypes.Structure):
+    """Mirror of ``rs_spec_args``."""
+
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("d_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
+        ("L", ctypes.c_int32), ("T", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+        ("ckpt_dtype", ctypes.c_int32), ("in_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("slot_idx", ctypes.c_void_p), ("committed", ctypes.c_void_p), ("is_flush", ctypes.c_void_p),
+        ("v", ctypes.c_void_p), ("k", ctypes.c_void_p), ("q", ctypes.c_void_p), ("alpha", ctypes.c_void_p),
+        ("ckpt", ctypes.c_void_p), ("ring_v", ctypes.c_void_p), ("ring_k", ctypes.c_void_p),
+        ("ring_a", ctypes.c_void_p), ("out", ctypes.c_void_p), ("dev_err", ctypes.c_void_p),
     ]
 
 
@@ -73,6 +106,18 @@ def load():
     lib.replayssm_plan_step.restype = ctypes.c_int
     lib.replayssm_plan_step.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_void_p, ctypes.c_void_p]
+    lib.replayssm_plan_align.restype = ctypes.c_int
+    lib.replayssm_plan_align.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    lib.replayssm_materialize.restype = ctypes.c_int
+    lib.replayssm_materialize.argtypes = [P(MaterializeArgs), ctypes.c_int, ctypes.c_void_p]
+    lib.replayssm_spec_verify_mamba2.restype = ctypes.c_int
+    lib.replayssm_spec_verify_mamba2.argtypes = [P(SpecArgs), ctypes.c_void_p]
+    lib.replayssm_plan_spec.restype = ctypes.c_int
+    lib.replayssm_plan_spec.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_void_p]
+    lib.replayssm_spec_commit.restype = ctypes.c_int
+    lib.replayssm_spec_commit.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int32] * 3 + [ctypes.c_void_p] * 4
     for name in ("replayssm_decode_mamba2", "replayssm_decode_gdn"):
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
@@ -131,6 +176,27 @@ def replayssm_plan_step(decode_step, L, force_flush=None, write_pos=None, is_flu
     return write_pos, is_flush
 
 
+def replayssm_plan_align(position, start, L, block, write_pos=None, is_flush=None):
+    """Align (prefix-caching) mode cursor and flag on the host: forced flush
+    on the token that completes a cache block of ``block`` tokens, ring
+    re-anchored at each block start (block 0 = off)."""
+    pos = np.ascontiguousarray(position, dtype=np.int64)
+    st = np.ascontiguousarray(start, dtype=np.int64)
+    B = pos.shape[0]
+    if st.shape != (B,):
+        raise ValueError("start must have shape [B]")
+    if write_pos is None:
+        write_pos = np.empty(B, dtype=np.int32)
+    if is_flush is None:
+        is_flush = np.empty(B, dtype=np.uint8)
+    if write_pos.dtype != np.int32 or is_flush.dtype != np.uint8 or not (
+            write_pos.flags.c_contiguous and is_flush.flags.c_contiguous):
+        raise ValueError("write_pos must be contiguous int32 and is_flush contiguous uint8")
+    _check(load().replayssm_plan_align(pos.ctypes.data, st.ctypes.data, int(block), B, int(L),
+                                       write_pos.ctypes.data, is_flush.ctypes.data), "replayssm_plan_align")
+    return write_pos, is_flush
+
+
 # --------------------------------------------------------------------------
 # decode steps
 # --------------------------------------------------------------------------
@@ -169,7 +235,7 @@ def _rows(t, name, H, d):
 
 
 def _fill(args, *, variant, ckpt, slot_idx, v, k, q, alpha, out, beta=None, ring_v=None, ring_k=None,
-          ring_a=None, write_pos=None, is_flush=None, dev_err=None):
+          ring_a=None, write_pos=None, is_flush=None, dev_err=None, ckpt_lp=None):
     torch = _torch()
     _need(ckpt, "ckpt", ndim=4)
     if not ckpt.is_contiguous():
@@ -234,6 +300,14 @@ def _fill(args, *, variant, ckpt, slot_idx, v, k, q, alpha, out, beta=None, ring
         args.dev_err = dev_err.data_ptr()
     else:
         args.dev_err = None
+    args.reserved2 = 0
+    if ckpt_lp is not None:
+        _need(ckpt_lp, "ckpt_lp", ndim=4)
+        if not ckpt_lp.is_contiguous() or ckpt_lp.shape != ckpt.shape:
+            raise ValueError("ckpt_lp must be contiguous with the shape of ckpt")
+        args.ckpt_lp, args.lp_dtype = ckpt_lp.data_ptr(), _dtype_code(ckpt_lp)
+    else:
+        args.ckpt_lp, args.lp_dtype = None, 0
     return args
 
 
@@ -244,11 +318,13 @@ def _stream(stream):
 
 
 def replayssm_decode_mamba2(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos, is_flush, v, k, q, alpha,
-                            out, dev_err=None, stream=None):
-    """One ReplaySSM Mamba-2 decode step in place on ckpt and the rings; o in ``out``."""
+                            out, dev_err=None, stream=None, ckpt_lp=None):
+    """One ReplaySSM Mamba-2 decode step in place on ckpt and the rings; o in
+    ``out``.  ``ckpt_lp`` (fp16 or bf16, shape of ckpt) makes ckpt the
+    recurrence copy of a two-precision checkpoint and ckpt_lp its read copy."""
     args = _fill(StepArgs(), variant=RS_MAMBA2, ckpt=ckpt, slot_idx=slot_idx, v=v, k=k, q=q, alpha=alpha,
                  out=out, ring_v=ring_v, ring_k=ring_k, ring_a=ring_a, write_pos=write_pos,
-                 is_flush=is_flush, dev_err=dev_err)
+                 is_flush=is_flush, dev_err=dev_err, ckpt_lp=ckpt_lp)
     return _check(load().replayssm_decode_mamba2(ctypes.byref(args), _stream(stream)), "replayssm_decode_mamba2")
 
 
@@ -267,6 +343,120 @@ def conventional_decode(*, variant, state, slot_idx, v, k, q, alpha, out, beta=N
                  beta=beta, out=out, dev_err=dev_err)
     return _check(load().conventional_decode(ctypes.byref(args), int(variant), _stream(stream)),
                   "conventional_decode")
+
+
+def replayssm_materialize(*, variant, ckpt, ring_v, ring_k, ring_a, slot_idx, held, dst, dst_idx, dev_err=None,
+                          stream=None):
+    """Exact state of each row (checkpoint unrolled with its ``held`` ring
+    records) written to ``dst[dst_idx[b]]``; checkpoint and ring only read."""
+    torch = _torch()
+    _need(ckpt, "ckpt", ndim=4)
+    _need(dst, "dst", ckpt.dtype, 4)
+    if not ckpt.is_contiguous() or not dst.is_contiguous() or dst.shape[1:] != ckpt.shape[1:]:
+        raise ValueError("ckpt and dst must be contiguous [slots, H, d_v, d_k] of one shape and dtype")
+    S, H, d_v, d_k = ckpt.shape
+    for name, t, shp in (("ring_v", ring_v, (S, H, None, d_v)), ("ring_k", ring_k, (S, H, None, d_k)),
+                         ("ring_a", ring_a, (S, H, None))):
+        _need(t, name)
+        if not t.is_contiguous() or t.dim() != len(shp) or any(
+                want is not None and got != want for got, want in zip(t.shape, shp)):
+            raise ValueError(f"{name} must be contiguous with shape {shp} (None = L)")
+    L = ring_a.shape[2]
+    if ring_v.shape[2] != L or ring_k.shape[2] != L or ring_v.dtype != ring_k.dtype:
+        raise ValueError("ring_v, ring_k and ring_a disagree on L or dtype")
+    _need(ring_a, "ring_a", torch.float32)
+    for name, t in (("slot_idx", slot_idx), ("held", held), ("dst_idx", dst_idx)):
+        _need(t, name, torch.int32, 1)
+    B = slot_idx.shape[0]
+    if held.shape[0] != B or dst_idx.shape[0] != B:
+        raise ValueError("slot_idx, held and dst_idx must have B entries")
+    a = MaterializeArgs()
+    a.B, a.H, a.d_v, a.d_k, a.L, a.num_slots, a.num_dst = B, H, d_v, d_k, L, S, dst.shape[0]
+    a.ckpt_dtype, a.ring_dtype, a.reserved = _dtype_code(ckpt), _dtype_code(ring_v), 0
+    a.slot_idx, a.held, a.dst_idx = slot_idx.data_ptr(), held.data_ptr(), dst_idx.data_ptr()
+    a.ckpt, a.ring_v, a.ring_k, a.ring_a = ckpt.data_ptr(), ring_v.data_ptr(), ring_k.data_ptr(), ring_a.data_ptr()
+    a.dst = dst.data_ptr()
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+        a.dev_err = dev_err.data_ptr()
+    else:
+        a.dev_err = None
+    return _check(load().replayssm_materialize(ctypes.byref(a), int(variant), _stream(stream)),
+                  "replayssm_materialize")
+
+
+def replayssm_plan_spec(committed, L, T, is_flush=None):
+    """Host flag of a verification step: committed + T > L (NumPy arrays)."""
+    h = np.ascontiguousarray(committed, dtype=np.int32)
+    B = h.shape[0]
+    if is_flush is None:
+        is_flush = np.empty(B, dtype=np.uint8)
+    if is_flush.dtype != np.uint8 or not is_flush.flags.c_contiguous:
+        raise ValueError("is_flush must be contiguous uint8")
+    _check(load().replayssm_plan_spec(h.ctypes.data, B, int(L), int(T), is_flush.ctypes.data), "replayssm_plan_spec")
+    return is_flush
+
+
+def replayssm_spec_verify_mamba2(*, ckpt, ring_v, ring_k, ring_a, slot_idx, committed, is_flush, v, k, q, alpha,
+                                 out, dev_err=None, stream=None):
+    """Verify T draft tokens per row (v [B, T, H, d_v], k, q [B, T, H, d_k],
+    alpha [B, T, H]); outputs in ``out`` [B, T, H, d_v].  Commits nothing."""
+    torch = _torch()
+    _need(ckpt, "ckpt", ndim=4)
+    if not ckpt.is_contiguous():
+        raise ValueError("ckpt must be contiguous [num_slots, H, d_v, d_k]")
+    S, H, d_v, d_k = ckpt.shape
+    _need(slot_idx, "slot_idx", torch.int32, 1)
+    B = slot_idx.shape[0]
+    _need(alpha, "alpha", torch.float32, 3)
+    T = alpha.shape[1]
+    for name, t, d in (("v", v, d_v), ("k", k, d_k), ("q", q, d_k)):
+        _need(t, name, ndim=4)
+        if t.shape != (B, T, H, d) or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, T, H, {d}]")
+    if not (v.dtype == k.dtype == q.dtype):
+        raise TypeError("v, k, q must share one dtype")
+    if alpha.shape != (B, T, H) or not alpha.is_contiguous():
+        raise ValueError("alpha must be contiguous [B, T, H]")
+    _need(out, "out", torch.float32, 4)
+    if out.shape != (B, T, H, d_v) or not out.is_contiguous():
+        raise ValueError("out must be contiguous [B, T, H, d_v]")
+    for name, t, shp in (("ring_v", ring_v, (S, H, None, d_v)), ("ring_k", ring_k, (S, H, None, d_k)),
+                         ("ring_a", ring_a, (S, H, None))):
+        _need(t, name)
+        if not t.is_contiguous() or t.dim() != len(shp) or any(
+                want is not None and got != want for got, want in zip(t.shape, shp)):
+            raise ValueError(f"{name} must be contiguous with shape {shp} (None = L)")
+    if ring_v.dtype != v.dtype or ring_k.dtype != v.dtype:
+        raise TypeError("Mamba-2 rings hold the inputs verbatim: ring dtype must equal the input dtype")
+    _need(committed, "committed", torch.int32, 1)
+    _need(is_flush, "is_flush", torch.uint8, 1)
+    a = SpecArgs()
+    a.B, a.H, a.d_v, a.d_k, a.L, a.T, a.num_slots = B, H, d_v, d_k, ring_a.shape[2], T, S
+    a.ckpt_dtype, a.in_dtype, a.reserved = _dtype_code(ckpt), _dtype_code(v), 0
+    a.slot_idx, a.committed, a.is_flush = slot_idx.data_ptr(), committed.data_ptr(), is_flush.data_ptr()
+    a.v, a.k, a.q, a.alpha = v.data_ptr(), k.data_ptr(), q.data_ptr(), alpha.data_ptr()
+    a.ckpt, a.ring_v, a.ring_k, a.ring_a = ckpt.data_ptr(), ring_v.data_ptr(), ring_k.data_ptr(), ring_a.data_ptr()
+    a.out = out.data_ptr()
+    a.dev_err = dev_err.data_ptr() if dev_err is not None else None
+    return _check(load().replayssm_spec_verify_mamba2(ctypes.byref(a), _stream(stream)),
+                  "replayssm_spec_verify_mamba2")
+
+
+def replayssm_spec_commit(*, committed, is_flush, accepted, L, T, committed_out=None, is_flush_out=None,
+                          dev_err=None, stream=None):
+    """Device-side pointer commit; in place unless outputs are given."""
+    torch = _torch()
+    _need(committed, "committed", torch.int32, 1)
+    _need(is_flush, "is_flush", torch.uint8, 1)
+    _need(accepted, "accepted", torch.int32, 1)
+    committed_out = committed if committed_out is None else committed_out
+    is_flush_out = is_flush if is_flush_out is None else is_flush_out
+    B = committed.shape[0]
+    return _check(load().replayssm_spec_commit(committed.data_ptr(), is_flush.data_ptr(), accepted.data_ptr(), B,
+                                               int(L), int(T), committed_out.data_ptr(), is_flush_out.data_ptr(),
+                                               None if dev_err is None else dev_err.data_ptr(), _stream(stream)),
+                  "replayssm_spec_commit")
 
 
 def raw_call(name, args, *extra):

@@ -60,53 +60,6 @@ cudaError_t dev_info(int dev, DevInfo *out) {
 
 }  // namespace
 
-cudaError_t plan_pipe(const void *kernel, int threads, size_t stage_bytes, HeadFn head, int max_stages,
-                      int ctas_per_sm, int units, PipePlan *out) {
-  static std::mutex mu;
-  static std::map<std::tuple<int, const void *, size_t>, PipePlan> cache;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const auto key = std::make_tuple(dev, kernel, stage_bytes);
-  PipePlan plan{};
-  bool hit = false;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) {
-      plan = it->second;
-      hit = true;
-    }
-  }
-  if (!hit) {
-    DevInfo d;
-    e = dev_info(dev, &d);
-    if (e != cudaSuccess) return e;
-    int ctas = 0, ns = 0;
-    for (int c = ctas_per_sm; c >= 1 && ns < 2; --c) {
-      const long budget = std::min<long>(d.smem_sm / c - 1024, d.smem_block);
-      const long n = (budget - (long)head(max_stages)) / (long)stage_bytes;
-      ns = (int)std::min<long>(n, max_stages);
-      ctas = c;
-    }
-    if (ns < 2) return cudaErrorInvalidValue;  // one stage would not overlap copies with compute
-    plan.nstage = ns;
-    plan.smem = head(ns) + (size_t)ns * stage_bytes;
-    e = ensure_smem(kernel, plan.smem);
-    if (e != cudaSuccess) return e;
-    int fit = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kernel, threads, plan.smem);
-    if (e != cudaSuccess) return e;
-    if (fit < 1) return cudaErrorInvalidConfiguration;
-    plan.grid = (unsigned)(d.sms * std::min(ctas, fit));
-    std::lock_guard<std::mutex> lock(mu);
-    cache[key] = plan;
-  }
-  plan.grid = std::min<unsigned>(plan.grid, (unsigned)units);
-  *out = plan;
-  return cudaSuccess;
-}
-
 cudaError_t plan_rings(const void *kernel, int threads, size_t ck_bytes, size_t rec_bytes, RingHeadFn head,
                        int units, RingPlan *out) {
   static std::mutex mu;
@@ -209,6 +162,13 @@ int validate(const rs_step_args *a, bool replay, bool gdn) {
       return RS_EALIGN;
   }
   if ((int64_t)a->B * a->H > 0x7fffffffLL) return RS_EINVAL;
+  if (a->reserved2 != 0) return RS_EINVAL;
+  if (a->ckpt_lp) {
+    // two-precision checkpoint: Mamba-2 replay, fp32 recurrence copy, 16-bit read copy
+    if (!replay || gdn) return RS_EUNSUPPORTED;
+    if (a->ckpt_dtype != RS_F32 || (a->lp_dtype != RS_F16 && a->lp_dtype != RS_BF16)) return RS_EUNSUPPORTED;
+    if (!aligned16(a->ckpt_lp)) return RS_EALIGN;
+  }
   return RS_OK;
 }
 
@@ -232,6 +192,7 @@ rs::KArgs to_kargs(const rs_step_args *a) {
   k.ring_v = a->ring_v;
   k.ring_k = a->ring_k;
   k.ring_a = a->ring_a;
+  k.ckpt_lp = a->ckpt_lp;
   k.out = a->out;
   k.sv = a->stride_v_row;
   k.sk = a->stride_k_row;
@@ -255,7 +216,7 @@ int replayssm_abi_version(void) { return RS_ABI_VERSION; }
 
 int replayssm_supported(int variant, int d_v, int d_k, int ckpt_dtype) {
   if (variant != RS_MAMBA2 && variant != RS_GDN) return 0;
-  if (variant == RS_MAMBA2) return rs::find_mamba2(d_v, d_k, ckpt_dtype, RS_BF16) != nullptr;
+  if (variant == RS_MAMBA2) return rs::find_mamba2(d_v, d_k, ckpt_dtype, RS_BF16, -1) != nullptr;
   return rs::find_gdn(d_v, d_k, ckpt_dtype, RS_F16, RS_BF16) != nullptr;
 }
 
@@ -274,10 +235,97 @@ int replayssm_plan_step(const int64_t *decode_step, const uint8_t *force_flush, 
   return RS_OK;
 }
 
+int replayssm_plan_align(const int64_t *position, const int64_t *start, int32_t block, int32_t B, int32_t L,
+                         int32_t *write_pos, uint8_t *is_flush) {
+  if (B < 0 || L < 1 || L > RS_MAX_L || block < 0) return RS_EINVAL;
+  if (B == 0) return RS_OK;
+  if (!position || !start || !write_pos || !is_flush) return RS_EINVAL;
+  for (int32_t b = 0; b < B; ++b)
+    if (start[b] < 0 || position[b] < start[b]) return RS_EINVAL;
+  for (int32_t b = 0; b < B; ++b) {
+    int64_t anchor = start[b];
+    bool completes = false;
+    if (block > 0) {
+      anchor = std::max<int64_t>(anchor, position[b] / block * block);
+      completes = (position[b] + 1) % block == 0;
+    }
+    const int32_t wp = (int32_t)((position[b] - anchor) % L);
+    write_pos[b] = wp;
+    is_flush[b] = (uint8_t)(wp == L - 1 || completes);
+  }
+  return RS_OK;
+}
+
+int replayssm_materialize(const rs_materialize_args *a, int variant, rs_stream_t stream) {
+  if (!a || (variant != RS_MAMBA2 && variant != RS_GDN)) return RS_EINVAL;
+  if (a->reserved != 0) return RS_EINVAL;
+  if (a->B < 0 || a->H < 1 || a->num_slots < 1 || a->num_dst < 1 || a->d_v < 1 || a->d_k < 1) return RS_EINVAL;
+  if (a->L < 2 || a->L > RS_MAX_L) return RS_EINVAL;
+  if (a->ckpt_dtype != RS_F32 && a->ckpt_dtype != RS_F16) return RS_EUNSUPPORTED;
+  if (a->ring_dtype != RS_F32 && a->ring_dtype != RS_F16 && a->ring_dtype != RS_BF16) return RS_EUNSUPPORTED;
+  const rs::MatLaunchFn fn = rs::find_materialize(a->d_v, a->d_k, a->ckpt_dtype);
+  if (!fn) return RS_EUNSUPPORTED;
+  if (a->B == 0) return RS_OK;
+  if (!a->slot_idx || !a->held || !a->dst_idx || !a->ckpt || !a->ring_v || !a->ring_k || !a->ring_a || !a->dst)
+    return RS_EINVAL;
+  if (!aligned16(a->ckpt) || !aligned16(a->dst) || !aligned16(a->ring_v) || !aligned16(a->ring_k)) return RS_EALIGN;
+  if (!aligned4(a->ring_a) || !aligned4(a->slot_idx) || !aligned4(a->held) || !aligned4(a->dst_idx))
+    return RS_EALIGN;
+  if ((int64_t)a->B * a->H * 2 > 0x7fffffffLL) return RS_EINVAL;
+  const cudaError_t e = fn(*a, variant == RS_GDN, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RS_OK : RS_ECUDA;
+}
+
+int replayssm_spec_verify_mamba2(const rs_spec_args *a, rs_stream_t stream) {
+  if (!a || a->reserved != 0) return RS_EINVAL;
+  if (a->B < 0 || a->H < 1 || a->num_slots < 1 || a->d_v < 1 || a->d_k < 1) return RS_EINVAL;
+  if (a->L < 1 || a->L > RS_MAX_L || a->T < 1 || a->T > 16 || a->T > a->L) return RS_EINVAL;
+  if (a->ckpt_dtype != RS_F32 && a->ckpt_dtype != RS_F16) return RS_EUNSUPPORTED;
+  if (a->in_dtype != RS_F32 && a->in_dtype != RS_BF16) return RS_EUNSUPPORTED;
+  const rs::SpecLaunchFn fn = rs::find_spec(a->d_v, a->d_k, a->ckpt_dtype, a->in_dtype);
+  if (!fn) return RS_EUNSUPPORTED;
+  if (a->B == 0) return RS_OK;
+  if (!a->slot_idx || !a->committed || !a->is_flush || !a->v || !a->k || !a->q || !a->alpha || !a->ckpt ||
+      !a->ring_v || !a->ring_k || !a->ring_a || !a->out)
+    return RS_EINVAL;
+  if (!aligned16(a->ckpt) || !aligned16(a->ring_v) || !aligned16(a->ring_k) || !aligned16(a->v) ||
+      !aligned16(a->k) || !aligned16(a->q))
+    return RS_EALIGN;
+  if (!aligned4(a->ring_a) || !aligned4(a->alpha) || !aligned4(a->out) || !aligned4(a->slot_idx) ||
+      !aligned4(a->committed))
+    return RS_EALIGN;
+  if ((int64_t)a->B * a->H > 0x7fffffffLL) return RS_EINVAL;
+  const cudaError_t e = fn(*a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RS_OK : RS_ECUDA;
+}
+
+int replayssm_plan_spec(const int32_t *committed, int32_t B, int32_t L, int32_t T, uint8_t *is_flush) {
+  if (B < 0 || L < 1 || L > RS_MAX_L || T < 1 || T > 16 || T > L) return RS_EINVAL;
+  if (B == 0) return RS_OK;
+  if (!committed || !is_flush) return RS_EINVAL;
+  for (int32_t b = 0; b < B; ++b)
+    if (committed[b] < 0 || committed[b] > L) return RS_EINVAL;
+  for (int32_t b = 0; b < B; ++b) is_flush[b] = (uint8_t)(committed[b] + T > L);
+  return RS_OK;
+}
+
+int replayssm_spec_commit(const int32_t *committed, const uint8_t *is_flush, const int32_t *accepted, int32_t B,
+                          int32_t L, int32_t T, int32_t *committed_out, uint8_t *is_flush_out, int32_t *dev_err,
+                          rs_stream_t stream) {
+  if (B < 0 || L < 1 || L > RS_MAX_L || T < 1 || T > 16 || T > L) return RS_EINVAL;
+  if (B == 0) return RS_OK;
+  if (!committed || !is_flush || !accepted || !committed_out || !is_flush_out) return RS_EINVAL;
+  if (!aligned4(committed) || !aligned4(accepted) || !aligned4(committed_out)) return RS_EALIGN;
+  const cudaError_t e = rs::launch_spec_commit(committed, is_flush, accepted, B, L, T, committed_out,
+                                               is_flush_out, dev_err, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RS_OK : RS_ECUDA;
+}
+
 int replayssm_decode_mamba2(const rs_step_args *args, rs_stream_t stream) {
   const int st = validate(args, /*replay=*/true, /*gdn=*/false);
   if (st != RS_OK || args->B == 0) return st;
-  return run(rs::find_mamba2(args->d_v, args->d_k, args->ckpt_dtype, args->in_dtype), args, stream);
+  const int lp = args->ckpt_lp ? args->lp_dtype : -1;
+  return run(rs::find_mamba2(args->d_v, args->d_k, args->ckpt_dtype, args->in_dtype, lp), args, stream);
 }
 
 int replayssm_decode_gdn(const rs_step_args *args, rs_stream_t stream) {

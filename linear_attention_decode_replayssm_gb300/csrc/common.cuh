@@ -31,6 +31,7 @@ struct KArgs {
   const void *v, *k, *q;
   const float *alpha, *beta;
   void *ckpt, *ring_v, *ring_k;
+  void *ckpt_lp;  // read copy of a two-precision checkpoint, or nullptr
   float *ring_a, *out;
   long long sv, sk, sq, so;  // row strides in elements
   int32_t *dev_err;
@@ -221,6 +222,42 @@ __device__ __forceinline__ void suffix_scan64(float &x0, float &x1, int lane, Op
 
 __device__ __forceinline__ void report(int32_t *dev_err, int bit) {
   if (dev_err) atomicOr(dev_err, bit);
+}
+
+// ---------------------------------------------------------------------------
+// 8-byte vectors of four 16-bit elements: the read copy of a two-precision
+// checkpoint, in the element positions of a 16-byte fp32 vector
+// ---------------------------------------------------------------------------
+template <typename TL>
+struct LpVec;
+
+template <>
+struct LpVec<__half> {
+  __device__ __forceinline__ static void unpack(const uint2 &r, float (&f)[4]) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&r.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&r.y));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
+  __device__ __forceinline__ static uint2 pack(const float (&f)[4]) {
+    const __half2 a = __floats2half2_rn(f[0], f[1]), b = __floats2half2_rn(f[2], f[3]);
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+  }
+};
+
+template <>
+struct LpVec<__nv_bfloat16> {
+  __device__ __forceinline__ static void unpack(const uint2 &r, float (&f)[4]) {
+    bf16x2_to_f(r.x, f[0], f[1]);
+    bf16x2_to_f(r.y, f[2], f[3]);
+  }
+  __device__ __forceinline__ static uint2 pack(const float (&f)[4]) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+  }
+};
+
+__device__ __forceinline__ void st_vec2(void *p, const uint2 &v) {
+  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
 }  // namespace rs

@@ -4,28 +4,29 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "replayssm.h"
 
 namespace rs {
 
 using LaunchFn = cudaError_t (*)(const KArgs &, cudaStream_t);
 
 // nullptr when the (d_v, d_k, checkpoint dtype) combination is not built in.
-LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype);
+// lp_dtype: read-copy type of a two-precision checkpoint, or -1 for none
+LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype, int lp_dtype);
 LaunchFn find_gdn(int d_v, int d_k, int ckpt_dtype, int ring_dtype, int in_dtype);
 LaunchFn find_conventional(int variant, int d_v, int d_k, int ckpt_dtype);
 
-// Launch shape of a persistent bulk-copy pipeline: CTAs, stages per CTA and
-// dynamic shared memory, chosen from the device's shared-memory limits
-// (`ctas_per_sm` CTAs per SM when two stages each still fit, else fewer) and
-// the kernel's occupancy.
-struct PipePlan {
-  unsigned grid;
-  int nstage;
-  size_t smem;
-};
-using HeadFn = uint32_t (*)(int nstage);
-cudaError_t plan_pipe(const void *kernel, int threads, size_t stage_bytes, HeadFn head, int max_stages,
-                      int ctas_per_sm, int units, PipePlan *out);
+// State materialisation; `gdn` selects log-gate weights (exp of suffix sums)
+// over decay products.
+using MatLaunchFn = cudaError_t (*)(const rs_materialize_args &, int gdn, cudaStream_t);
+MatLaunchFn find_materialize(int d_v, int d_k, int ckpt_dtype);
+
+// Speculative verification (Mamba-2) and the device-side commit.
+using SpecLaunchFn = cudaError_t (*)(const rs_spec_args &, cudaStream_t);
+SpecLaunchFn find_spec(int d_v, int d_k, int ckpt_dtype, int in_dtype);
+cudaError_t launch_spec_commit(const int32_t *committed, const uint8_t *is_flush, const int32_t *accepted, int B,
+                               int L, int T, int32_t *committed_out, uint8_t *is_flush_out, int32_t *dev_err,
+                               cudaStream_t s);
 
 // Launch shape of a kernel with a checkpoint-slot ring (nsc slots of
 // `ck_bytes`) and a record-slot ring (nsr slots of `rec_bytes`): two CTAs

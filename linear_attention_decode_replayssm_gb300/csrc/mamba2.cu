@@ -31,6 +31,8 @@
 // state) spread evenly over the CTAs.  Every wait is bounded: on a timeout
 // the kernel reports RS_DERR_TIMEOUT, drains its own copies and returns.
 // No tensor cores: the step is a bandwidth-bound GEMV (about 0.6 FLOP/byte).
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 #include "replayssm.h"
@@ -67,9 +69,11 @@ __host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(
 
 // LMAX bounds the buffer length at compile time (L <= LMAX): loops over a
 // window's records unroll to a fixed count with predicated bodies.
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, int LMAX>
+// TL is the read-copy type of a two-precision checkpoint (TL == TC: one copy).
+template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX>
 __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
+  constexpr bool TWO = !std::is_same<TC, TL>::value;
   constexpr int E = V::E;
   constexpr int G = DK / E;          // lanes per state row
   constexpr int NC = NCW * 32;       // consumer threads per group
@@ -79,6 +83,8 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   constexpr int RES = (int)sizeof(RT);
   constexpr int PROD = NGRP * NCW;   // warp index of the producer
   constexpr uint32_t CKB = DV * DK * (uint32_t)sizeof(TC);
+  constexpr uint32_t CKB_LP = DV * DK * (uint32_t)sizeof(TL);
+  static_assert(!TWO || (E == 4 && sizeof(TL) == 2), "read copy: 16-bit elements under an fp32 checkpoint");
   static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && DV % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
   static_assert(DK % 8 == 0 && DV % 8 == 0, "head dims must be multiples of 8");
@@ -166,9 +172,13 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
           const size_t unit = (size_t)slot * a.H + h;
           if (lane == 0) {
             meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
-            mbar_expect_tx(&full[s], CKB);
-            bulk_load(ck_slots + (size_t)c * CKB, static_cast<const TC *>(a.ckpt) + unit * (DV * DK), CKB,
-                      &full[s], pol_stream);
+            // a two-precision non-flush row reads only the read copy
+            const bool lp = TWO && !fl;
+            const uint32_t nb = lp ? CKB_LP : CKB;
+            const void *src = lp ? static_cast<const void *>(static_cast<const TL *>(a.ckpt_lp) + unit * (DV * DK))
+                                 : static_cast<const void *>(static_cast<const TC *>(a.ckpt) + unit * (DV * DK));
+            mbar_expect_tx(&full[s], nb);
+            bulk_load(ck_slots + (size_t)c * CKB, src, nb, &full[s], pol_stream);
           }
           constexpr uint32_t kb = DK * RES, vb = DV * RES;
           constexpr int KC = kb / 16, VC = vb / 16;  // 16-byte chunks per k / v record
@@ -253,38 +263,41 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       mbar_arrive(&rec_empty[s]);
       continue;
     }
-    // take this thread's share of the checkpoint into registers and hand the
-    // slot straight back to the producer
-    uint4 raw[VPT];
-    {
-      const uint4 *ck = reinterpret_cast<const uint4 *>(ck_slots + (size_t)c * CKB);
-#pragma unroll
-      for (int r = 0; r < VPT; ++r) raw[r] = ck[(row0 + r * RPP) * G + cv];
-    }
-    mbar_arrive(&ck_empty[c]);
     const size_t unit = (size_t)slot * a.H + h;
     const float *sa = reinterpret_cast<const float *>(st + lay.a);
     float *scr = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + lay.scr);
     float *sW = scr, *sS = scr + L, *sC = scr + 2 * L, *sGam = scr + 2 * L + DV;
     const unsigned char *sk = st + lay.k, *sv = st + lay.v;
+    const unsigned char *ck_slot = ck_slots + (size_t)c * CKB;
 
     // window weights w_j (suffix products of the decays) and gamma
-    if (lw == 0) {
-      float x0 = lane <= p ? sa[lane] : 1.f;
-      float x1 = lane + 32 <= p ? sa[lane + 32] : 1.f;
-      suffix_scan64(x0, x1, lane, [](float x, float y) { return x * y; });
-      const float n0 = __shfl_down_sync(0xffffffffu, x0, 1);
-      const float n1 = __shfl_down_sync(0xffffffffu, x1, 1);
-      const float hi0 = __shfl_sync(0xffffffffu, x1, 0);
-      if (lane <= p) sW[lane] = lane == 31 ? hi0 : n0;
-      if (lane + 32 <= p) sW[lane + 32] = lane == 31 ? 1.f : n1;
-      if (lane == 0) sGam[0] = x0;
-    }
-    float qv[E];
-    lds_cols<E>(st + lay.q, cv * E, RDT, qv);
+    auto weights = [&]() {
+      if (lw == 0) {
+        float x0 = lane <= p ? sa[lane] : 1.f;
+        float x1 = lane + 32 <= p ? sa[lane + 32] : 1.f;
+        suffix_scan64(x0, x1, lane, [](float x, float y) { return x * y; });
+        const float n0 = __shfl_down_sync(0xffffffffu, x0, 1);
+        const float n1 = __shfl_down_sync(0xffffffffu, x1, 1);
+        const float hi0 = __shfl_sync(0xffffffffu, x1, 0);
+        if (lane <= p) sW[lane] = lane == 31 ? hi0 : n0;
+        if (lane + 32 <= p) sW[lane + 32] = lane == 31 ? 1.f : n1;
+        if (lane == 0) sGam[0] = x0;
+      }
+    };
 
     float part[VPT];
     if (!flush) {
+      // take this thread's share of the checkpoint (the read copy of a
+      // two-precision checkpoint) into registers and hand the slot straight
+      // back to the producer
+      using Raw = typename std::conditional<TWO, uint2, uint4>::type;
+      Raw raw[VPT];
+#pragma unroll
+      for (int r = 0; r < VPT; ++r) raw[r] = reinterpret_cast<const Raw *>(ck_slot)[(row0 + r * RPP) * G + cv];
+      mbar_arrive(&ck_empty[c]);
+      weights();
+      float qv[E];
+      lds_cols<E>(st + lay.q, cv * E, RDT, qv);
       // s_j = k_j . q: a warp takes records four at a time; each lane holds
       // its 4-column chunk of q and accumulates four partial dots, and one
       // transposed reduction finishes the chunk
@@ -332,7 +345,11 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
 #pragma unroll
       for (int r = 0; r < VPT; ++r) {
         float f[E];
-        V::unpack(raw[r], f);
+        if constexpr (TWO) {
+          LpVec<TL>::unpack(raw[r], f);
+        } else {
+          V::unpack(raw[r], f);
+        }
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) acc = fmaf(f[e], qv[e], acc);
@@ -389,6 +406,13 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       }
       if (ctid == NC - 1) a.ring_a[unit * L + p] = sa[p];
     } else {
+      uint4 raw[VPT];
+#pragma unroll
+      for (int r = 0; r < VPT; ++r) raw[r] = reinterpret_cast<const uint4 *>(ck_slot)[(row0 + r * RPP) * G + cv];
+      mbar_arrive(&ck_empty[c]);
+      weights();
+      float qv[E];
+      lds_cols<E>(st + lay.q, cv * E, RDT, qv);
       gsync();  // weights ready
       const float gam = sGam[0];
       TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK);
@@ -418,6 +442,12 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
         for (int e = 0; e < E; ++e) acc = fmaf(f[r][e], qv[e], acc);
         part[r] = acc;
         st_vec(ckg + (size_t)(row0 + r * RPP) * DK + cv * E, V::pack(f[r]));
+        if constexpr (TWO) {
+          // the read copy: an independent rounding of the same fp32 matrix
+          TL *lpg = static_cast<TL *>(a.ckpt_lp) + unit * (DV * DK);
+          float g4[4] = {f[r][0], f[r][1], f[r][2], f[r][3]};
+          st_vec2(lpg + (size_t)(row0 + r * RPP) * DK + cv * E, LpVec<TL>::pack(g4));
+        }
       }
       group_reduce<VPT, G>(part, lane);
       if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
@@ -429,9 +459,9 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
 }
 
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, int LMAX>
+template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX>
 static cudaError_t launch_mamba2_l(const KArgs &a, cudaStream_t s) {
-  auto kern = mamba2_replay_kernel<DV, DK, TC, RT, NCW, NGRP, LMAX>;
+  auto kern = mamba2_replay_kernel<DV, DK, TC, TL, RT, NCW, NGRP, LMAX>;
   constexpr int threads = NGRP * NCW * 32 + 32;
   const size_t ckb = (size_t)DV * DK * sizeof(TC);
   const size_t rb = m2_rec(DV, DK, (int)sizeof(RT), a.L).bytes;
@@ -443,15 +473,25 @@ static cudaError_t launch_mamba2_l(const KArgs &a, cudaStream_t s) {
 }
 
 // the common short windows get a kernel unrolled for L <= 16
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP>
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, typename TL = TC>
 static cudaError_t launch_mamba2(const KArgs &a, cudaStream_t s) {
-  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, RT, NCW, NGRP, 16>(a, s)
-                   : launch_mamba2_l<DV, DK, TC, RT, NCW, NGRP, RS_MAX_L>(a, s);
+  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 16>(a, s)
+                   : launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, RS_MAX_L>(a, s);
 }
 
 template <typename RT>
-static LaunchFn find_mamba2_t(int d_v, int d_k, int ckpt_dtype) {
-  if (ckpt_dtype == kF32) {
+static LaunchFn find_mamba2_t(int d_v, int d_k, int ckpt_dtype, int lp_dtype) {
+  if (ckpt_dtype == kF32 && lp_dtype == kF16) {
+    if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1, __half>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __half>;
+    if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1, __half>;
+  } else if (ckpt_dtype == kF32 && lp_dtype == kBF16) {
+    if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1, __nv_bfloat16>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __nv_bfloat16>;
+    if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1, __nv_bfloat16>;
+  } else if (lp_dtype >= 0) {
+    return nullptr;
+  } else if (ckpt_dtype == kF32) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1>;
     if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1>;
@@ -463,9 +503,9 @@ static LaunchFn find_mamba2_t(int d_v, int d_k, int ckpt_dtype) {
   return nullptr;
 }
 
-LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype) {
-  return in_dtype == kF32 ? find_mamba2_t<float>(d_v, d_k, ckpt_dtype)
-                          : find_mamba2_t<__nv_bfloat16>(d_v, d_k, ckpt_dtype);
+LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype, int lp_dtype) {
+  return in_dtype == kF32 ? find_mamba2_t<float>(d_v, d_k, ckpt_dtype, lp_dtype)
+                          : find_mamba2_t<__nv_bfloat16>(d_v, d_k, ckpt_dtype, lp_dtype);
 }
 
 }  // namespace rs

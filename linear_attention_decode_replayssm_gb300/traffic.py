@@ -20,8 +20,12 @@ ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
 
 
 def step_bytes(*, variant, H, d_v, d_k, ckpt_dtype, in_dtype, ring_dtype, slot_idx, write_pos=None,
-               is_flush=None, replay=True):
-    """Bytes one launch moves for the given per-row cursors (NumPy arrays [B])."""
+               is_flush=None, replay=True, lp_dtype=None):
+    """Bytes one launch moves for the given per-row cursors (NumPy arrays [B]).
+
+    With a two-precision checkpoint (``lp_dtype``), a non-flush row reads the
+    read copy instead of the checkpoint, and a flush row reads the checkpoint
+    and writes both copies."""
     slot_idx = np.asarray(slot_idx)
     live = slot_idx >= 0
     n_live = int(live.sum())
@@ -29,14 +33,17 @@ def step_bytes(*, variant, H, d_v, d_k, ckpt_dtype, in_dtype, ring_dtype, slot_i
     state = d_v * d_k * ESIZE[ckpt_dtype]
     io = (d_v + 2 * d_k) * ESIZE[in_dtype] + 4 + (4 if variant == "gdn" else 0) + 4 * d_v
     meta = 4 + (5 if replay else 0)
-    total = n_live * (H * (state + io) + meta) + n_pad * (4 + H * 4 * d_v)
     if not replay:
-        return total + n_live * H * state
+        return n_live * (H * (2 * state + io) + meta) + n_pad * (4 + H * 4 * d_v)
+    total = n_live * (H * io + meta) + n_pad * (4 + H * 4 * d_v)
     rec = (d_v + d_k) * ESIZE[ring_dtype] + 4
     p = np.asarray(write_pos, dtype=np.int64)[live]
     fl = np.asarray(is_flush)[live] != 0
+    n_fl, n_nf = int(fl.sum()), int((~fl).sum())
+    read_nf = state if lp_dtype is None else d_v * d_k * ESIZE[lp_dtype]
+    write_fl = state if lp_dtype is None else state + d_v * d_k * ESIZE[lp_dtype]
     total += int(p.sum()) * H * rec
-    total += int(fl.sum()) * H * state + int((~fl).sum()) * H * rec
+    total += n_fl * H * (state + write_fl) + n_nf * H * (read_nf + rec)
     return total
 
 
@@ -53,3 +60,38 @@ def step_flops(*, variant, H, d_v, d_k, slot_idx, write_pos=None, is_flush=None,
     nonflush = dots * 2 * mn + (p + 1) * (2 * d_k * dots + 2 * d_v * dots)
     flush = 2 * mn + (p + 1) * 2 * mn + 2 * mn + (2 * mn if variant == "gdn" else 0)
     return int(H * np.where(fl, flush, nonflush).sum())
+
+
+def materialize_bytes(*, H, d_v, d_k, ckpt_dtype, ring_dtype, slot_idx, held, dst_idx=None):
+    """Bytes one materialisation launch moves: per materialised row and head,
+    the checkpoint read once, the ``held`` ring records read once and the state
+    written once; per row, the slot, count and destination index (12 bytes).
+    Rows skipped (negative slot or destination) move their two indices only."""
+    slot_idx = np.asarray(slot_idx)
+    live = slot_idx >= 0
+    if dst_idx is not None:
+        live &= np.asarray(dst_idx) >= 0
+    state = d_v * d_k * ESIZE[ckpt_dtype]
+    rec = (d_v + d_k) * ESIZE[ring_dtype] + 4
+    p = np.asarray(held, dtype=np.int64)[live]
+    n_live = int(live.sum())
+    return n_live * (H * 2 * state + 12) + int(p.sum()) * H * rec + int((~live).sum()) * 8
+
+
+def spec_bytes(*, H, d_v, d_k, T, ckpt_dtype, in_dtype, slot_idx, committed, is_flush):
+    """Bytes one speculative-verification launch (Mamba-2) moves: per live row
+    and head, the checkpoint read once, the committed records read (on a
+    flush they are folded, and the checkpoint written), the T drafts' inputs
+    read, their T outputs and T records written; per row the slot, count and
+    flag (9 bytes).  Padded rows move their slot index and zero outputs."""
+    slot_idx = np.asarray(slot_idx)
+    live = slot_idx >= 0
+    state = d_v * d_k * ESIZE[ckpt_dtype]
+    rec = (d_v + d_k) * ESIZE[in_dtype] + 4
+    draft_in = (d_v + 2 * d_k) * ESIZE[in_dtype] + 4
+    h = np.asarray(committed, dtype=np.int64)[live]
+    fl = np.asarray(is_flush)[live] != 0
+    n_live = int(live.sum())
+    per_row = H * (state + T * (draft_in + 4 * d_v + rec)) + 9
+    total = n_live * per_row + int(h.sum()) * H * rec + int(fl.sum()) * H * state
+    return total + int((~live).sum()) * (4 + T * H * 4 * d_v)

@@ -26,11 +26,13 @@ def dev(a, dtype, device="cuda"):
 class GpuRun:
     """ReplaySSM (or conventional) state on the GPU, stepped through the C ABI."""
 
-    def __init__(self, lib, w, conventional=False, ckpt0=None):
+    def __init__(self, lib, w, conventional=False, ckpt0=None, lp_dtype=None):
         import torch
 
         self.lib, self.w, self.conventional = lib, w, conventional
         self.ckpt = dev(w.ckpt0 if ckpt0 is None else ckpt0, tdt(w.ckpt_dtype))
+        # two-precision checkpoint: the read copy starts as the checkpoint cast (RN-even)
+        self.ckpt_lp = None if lp_dtype is None else self.ckpt.to(tdt(lp_dtype))
         self.ring_v = dev(w.ring_v0, tdt(w.ring_dtype))
         self.ring_k = dev(w.ring_k0, tdt(w.ring_dtype))
         self.ring_a = dev(w.ring_a0, torch.float32)
@@ -49,10 +51,12 @@ class GpuRun:
         t["beta"] = dev(x["beta"], torch.float32) if "beta" in x else None
         return t
 
-    def step(self, x, decode_step, out=None, **override):
-        """One step; returns (o on host as float64, write_pos, is_flush)."""
+    def step(self, x, decode_step, out=None, plan=None, **override):
+        """One step; returns (o on host as float64, write_pos, is_flush).
+        ``plan`` = (write_pos, is_flush) from another host plan (align mode)
+        replaces the plan of ``decode_step``."""
         w, lib = self.w, self.lib
-        wp, fl = lib.replayssm_plan_step(decode_step, w.L)
+        wp, fl = lib.replayssm_plan_step(decode_step, w.L) if plan is None else plan
         self.wp.copy_(dev(wp, self.wp.dtype))
         self.fl.copy_(dev(fl, self.fl.dtype))
         t = self.tensors(x)
@@ -66,7 +70,7 @@ class GpuRun:
             lib.replayssm_decode_mamba2(ckpt=self.ckpt, ring_v=self.ring_v, ring_k=self.ring_k,
                                         ring_a=self.ring_a, slot_idx=self.slot_idx, write_pos=self.wp,
                                         is_flush=self.fl, v=t["v"], k=t["k"], q=t["q"], alpha=t["alpha"],
-                                        out=out, dev_err=self.dev_err)
+                                        out=out, dev_err=self.dev_err, ckpt_lp=self.ckpt_lp)
         else:
             lib.replayssm_decode_gdn(ckpt=self.ckpt, ring_v=self.ring_v, ring_k=self.ring_k, ring_a=self.ring_a,
                                      slot_idx=self.slot_idx, write_pos=self.wp, is_flush=self.fl, v=t["v"],
@@ -78,7 +82,8 @@ class GpuRun:
 class OracleRun:
     """The oracle on the same workload, optionally on a subset of heads."""
 
-    def __init__(self, w, heads=None, replay=True, exact=True, exact_state_dtype="f64", ckpt0=None):
+    def __init__(self, w, heads=None, replay=True, exact=True, exact_state_dtype="f64", ckpt0=None,
+                 lp_dtype=None):
         self.w = w
         self.heads = np.arange(w.H) if heads is None else np.asarray(heads)
         hs = self.heads
@@ -86,6 +91,8 @@ class OracleRun:
         rs = oracle.ReplayState(w.variant, c0[:, hs].astype(np.float64), w.ring_v0[:, hs].astype(np.float64),
                                 w.ring_k0[:, hs].astype(np.float64), w.ring_a0[:, hs].astype(np.float64),
                                 ckpt_dtype=w.ckpt_dtype, ring_dtype=w.ring_dtype, a_dtype="f32")
+        if lp_dtype is not None:
+            rs.with_read_copy(lp_dtype)
         self.rs = rs if replay else None
         self.ex = oracle.ExactState.from_replay(rs, w.held_records(), exact_state_dtype) if exact else None
 

@@ -159,3 +159,140 @@ def test_binding_refuses_cpu_tensors(lib):
         lib.replayssm_decode_mamba2(ckpt=torch.zeros(1, 2, 64, 128), ring_v=z, ring_k=z, ring_a=z,
                                     slot_idx=torch.zeros(1, dtype=torch.int32), write_pos=z, is_flush=z,
                                     v=z, k=z, q=z, alpha=z, out=z)
+
+
+# --------------------------------------------------------------------------
+# align-mode plan and materialisation (host side)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("L, block", [(16, 0), (16, 40), (16, 64), (8, 5), (4, 1), (64, 100)])
+def test_plan_align_matches_oracle(lib, L, block):
+    r = np.random.default_rng(L * 1000 + block)
+    start = r.integers(0, 300, 500)
+    pos = start + r.integers(0, 400, 500)
+    wp, fl = lib.replayssm_plan_align(pos, start, L, block)
+    wp_o, fl_o = oracle.plan_align(pos, start, L, block)
+    np.testing.assert_array_equal(wp, wp_o)
+    np.testing.assert_array_equal(fl, fl_o)
+
+
+def test_plan_align_rejects_bad_input(lib):
+    so = lib.load()
+    pos = np.array([5, 6, 7], dtype=np.int64)
+    st = np.array([0, 7, 0], dtype=np.int64)  # row 1 starts after its position
+    wp = np.full(3, -9, dtype=np.int32)
+    fl = np.full(3, 9, dtype=np.uint8)
+    assert so.replayssm_plan_align(pos.ctypes.data, st.ctypes.data, 8, 3, 16, wp.ctypes.data, fl.ctypes.data) \
+        == lib.RS_EINVAL
+    assert np.all(wp == -9) and np.all(fl == 9)  # outputs untouched
+    st[1] = 0
+    assert so.replayssm_plan_align(pos.ctypes.data, st.ctypes.data, -1, 3, 16, wp.ctypes.data, fl.ctypes.data) \
+        == lib.RS_EINVAL
+    assert so.replayssm_plan_align(pos.ctypes.data, st.ctypes.data, 8, 3, 65, wp.ctypes.data, fl.ctypes.data) \
+        == lib.RS_EINVAL
+    assert so.replayssm_plan_align(None, st.ctypes.data, 8, 3, 16, wp.ctypes.data, fl.ctypes.data) == lib.RS_EINVAL
+    assert so.replayssm_plan_align(None, None, 8, 0, 16, None, None) == lib.RS_OK
+
+
+def _mat_args(lib, **kw):
+    a = lib.MaterializeArgs()
+    base = dict(B=4, H=2, d_v=64, d_k=128, L=16, num_slots=8, num_dst=8, ckpt_dtype=lib.RS_F32,
+                ring_dtype=lib.RS_BF16, reserved=0, slot_idx=0x1000, held=0x2000, dst_idx=0x3000,
+                ckpt=0x9000, ring_v=0xA000, ring_k=0xB000, ring_a=0xC000, dst=0xD000, dev_err=None)
+    base.update(kw)
+    for k_, v_ in base.items():
+        setattr(a, k_, v_)
+    return a
+
+
+@pytest.mark.parametrize("change, variant, want", [
+    (dict(), 7, "RS_EINVAL"),
+    (dict(L=1), 0, "RS_EINVAL"),
+    (dict(num_dst=0), 0, "RS_EINVAL"),
+    (dict(reserved=3), 1, "RS_EINVAL"),
+    (dict(ckpt_dtype=2), 0, "RS_EUNSUPPORTED"),
+    (dict(ring_dtype=5), 0, "RS_EUNSUPPORTED"),
+    (dict(d_v=32), 0, "RS_EUNSUPPORTED"),
+    (dict(held=None), 0, "RS_EINVAL"),
+    (dict(dst=None), 1, "RS_EINVAL"),
+    (dict(dst=0xD008), 0, "RS_EALIGN"),
+    (dict(ring_v=0xA004), 1, "RS_EALIGN"),
+    (dict(dst_idx=0x3002), 0, "RS_EALIGN"),
+])
+def test_materialize_validation(lib, change, variant, want):
+    st = lib.raw_call("replayssm_materialize", _mat_args(lib, **change), variant, None)
+    assert st == getattr(lib, want), lib.status_string(st)
+
+
+def test_materialize_empty_batch_is_a_no_op(lib):
+    a = _mat_args(lib, B=0, slot_idx=None, held=None, dst_idx=None, ckpt=None, ring_v=None, ring_k=None,
+                  ring_a=None, dst=None)
+    assert lib.raw_call("replayssm_materialize", a, 0, None) == lib.RS_OK
+
+
+@pytest.mark.parametrize("change, entry, want", [
+    (dict(ckpt_lp=0xE000, lp_dtype=1), "replayssm_decode_gdn", "RS_EUNSUPPORTED"),      # Mamba-2 only
+    (dict(ckpt_lp=0xE000, lp_dtype=1, ckpt_dtype=1), "replayssm_decode_mamba2", "RS_EUNSUPPORTED"),
+    (dict(ckpt_lp=0xE000, lp_dtype=0), "replayssm_decode_mamba2", "RS_EUNSUPPORTED"),  # 16-bit read copy
+    (dict(ckpt_lp=0xE008, lp_dtype=2), "replayssm_decode_mamba2", "RS_EALIGN"),
+    (dict(reserved2=1), "replayssm_decode_mamba2", "RS_EINVAL"),
+])
+def test_two_precision_validation(lib, change, entry, want):
+    kw = dict(change)
+    if entry == "replayssm_decode_gdn":
+        kw["ring_dtype"] = lib.RS_F16
+    st = lib.raw_call(entry, _args(lib, **kw), None)
+    assert st == getattr(lib, want), lib.status_string(st)
+    a = _args(lib, ckpt_lp=0xE000, lp_dtype=1, ring_v=None, ring_k=None, ring_a=None, write_pos=None,
+              is_flush=None, L=0)
+    assert lib.raw_call("conventional_decode", a, 0, None) == lib.RS_EUNSUPPORTED
+
+
+# --------------------------------------------------------------------------
+# speculative verification (host side)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("L, T", [(16, 4), (16, 8), (8, 8), (64, 16), (4, 1)])
+def test_plan_spec_matches_oracle(lib, L, T):
+    h = np.random.default_rng(L + T).integers(0, L + 1, 300).astype(np.int32)
+    np.testing.assert_array_equal(lib.replayssm_plan_spec(h, L, T), oracle.spec.spec_plan(h, L, T))
+
+
+def test_plan_spec_rejects_bad_input(lib):
+    so = lib.load()
+    h = np.array([0, 17], dtype=np.int32)
+    fl = np.full(2, 9, dtype=np.uint8)
+    assert so.replayssm_plan_spec(h.ctypes.data, 2, 16, 4, fl.ctypes.data) == lib.RS_EINVAL  # h > L
+    assert np.all(fl == 9)
+    h[1] = 3
+    assert so.replayssm_plan_spec(h.ctypes.data, 2, 16, 17, fl.ctypes.data) == lib.RS_EINVAL  # T > 16
+    assert so.replayssm_plan_spec(h.ctypes.data, 2, 4, 5, fl.ctypes.data) == lib.RS_EINVAL   # T > L
+    assert so.replayssm_plan_spec(h.ctypes.data, 2, 16, 4, fl.ctypes.data) == lib.RS_OK
+    assert list(fl) == [0, 0]
+    assert so.replayssm_spec_commit(None, None, None, 0, 16, 4, None, None, None, None) == lib.RS_OK
+    assert so.replayssm_spec_commit(None, None, None, 3, 16, 4, None, None, None, None) == lib.RS_EINVAL
+
+
+def _spec_args(lib, **kw):
+    a = lib.SpecArgs()
+    base = dict(B=4, H=2, d_v=64, d_k=128, L=16, T=4, num_slots=8, ckpt_dtype=lib.RS_F32, in_dtype=lib.RS_BF16,
+                reserved=0, slot_idx=0x1000, committed=0x2000, is_flush=0x3000, v=0x4000, k=0x5000, q=0x6000,
+                alpha=0x7000, ckpt=0x9000, ring_v=0xA000, ring_k=0xB000, ring_a=0xC000, out=0xD000, dev_err=None)
+    base.update(kw)
+    for k_, v_ in base.items():
+        setattr(a, k_, v_)
+    return a
+
+
+@pytest.mark.parametrize("change, want", [
+    (dict(T=0), "RS_EINVAL"),
+    (dict(T=17, L=32), "RS_EINVAL"),
+    (dict(T=5, L=4), "RS_EINVAL"),
+    (dict(reserved=2), "RS_EINVAL"),
+    (dict(ckpt_dtype=2), "RS_EUNSUPPORTED"),
+    (dict(d_v=32), "RS_EUNSUPPORTED"),
+    (dict(committed=None), "RS_EINVAL"),
+    (dict(q=0x6008), "RS_EALIGN"),
+    (dict(committed=0x2002), "RS_EALIGN"),
+])
+def test_spec_verify_validation(lib, change, want):
+    st = lib.raw_call("replayssm_spec_verify_mamba2", _spec_args(lib, **change), None)
+    assert st == getattr(lib, want), lib.status_string(st)
