@@ -53,6 +53,7 @@ from .replay import (
     exact_step,
     replay_step,
     materialize,
+    heads_from_groups,
 )
 from .storage import round_to, STORAGE_DTYPES
 from . import spec, traffic
@@ -74,6 +75,7 @@ __all__ = [
     "exact_step",
     "replay_step",
     "materialize",
+    "heads_from_groups",
     "round_to",
     "STORAGE_DTYPES",
     "spec",

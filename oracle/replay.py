@@ -230,3 +230,23 @@ def materialize(rs, slot_idx, held, dst_dtype="f64"):
         out[b] = round_to(rebuild(rs.ckpt[s], rs.ring_a[s, :, :p], rs.ring_v[s, :, :p], rs.ring_k[s, :, :p]),
                           dst_dtype)
     return out
+
+
+def heads_from_groups(x, n_heads):
+    """Expand group-shared keys or queries to one per value head.
+
+    Mamba-2 layers share the key (B) and query (C) projections across groups
+    of value heads: with G groups, head h uses group h // (n_heads / G)
+    ([Ghana] §Output without a state: "a small kernel computes them once per
+    group"; §The identity prices the record of the shipped layout, x and dt
+    per head and B per group).  x [..., G, d] -> [..., n_heads, d].  With the
+    keys expanded, the group layout computes exactly what the per-head
+    recurrence computes.
+
+    Parity: pinned by a hand case in ``tests/test_oracle_pins.py``.
+    """
+    x = np.asarray(x)
+    G = x.shape[-2]
+    if n_heads % G:
+        raise ValueError("the number of heads must be a multiple of the number of groups")
+    return np.repeat(x, n_heads // G, axis=-2)

@@ -574,3 +574,15 @@ def test_two_precision_error_does_not_accumulate():
     assert two_late < 2.0 * two_early
     assert one_late > 2.5 * one_early
     assert two_late < one_late / 3.0
+
+
+def test_heads_from_groups_by_hand():
+    # 4 heads in 2 groups: heads 0, 1 read group 0; heads 2, 3 read group 1
+    x = np.array([[[1.0, 2.0], [3.0, 4.0]]])          # [B=1, G=2, d=2]
+    y = oracle.heads_from_groups(x, 4)
+    np.testing.assert_array_equal(y, [[[1, 2], [1, 2], [3, 4], [3, 4]]])
+    assert oracle.heads_from_groups(x, 2).shape == (1, 2, 2)
+    with pytest.raises(ValueError):
+        oracle.heads_from_groups(x, 3)
+    # the grouped record prices to the printed 18 944 bytes at 128 heads, 8 groups
+    assert oracle.traffic.grouped_record_bytes(128, 64, 8, 128) == 18944
