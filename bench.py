@@ -48,6 +48,11 @@ WORKLOADS = {
                               ring="bf16", lp="f16",
                               desc="Mamba-2 layer as mamba2_bs256 with a two-precision checkpoint: fp32 "
                                    "recurrence copy, fp16 read copy for non-flush rows"),
+    "mamba2_bs256_g8": dict(variant="mamba2", B=256, H=128, d_v=64, d_k=128, L=16, ckpt="f32", inp="bf16",
+                            ring="bf16", groups=8,
+                            desc="Mamba-2 layer as mamba2_bs256 with the model's own key layout: keys and queries "
+                                 "shared by 8 groups of 16 heads, key ring per group, group dots k_j.q computed "
+                                 "once per group"),
     "gdn_bs256": dict(variant="gdn", B=256, H=32, d_v=128, d_k=128, L=16, ckpt="f32", inp="bf16", ring="f16",
                       desc="Gated DeltaNet layer: batch 256, 32 value heads of 128 x 128, fp32 checkpoint, "
                            "fp16 d/k rings, fp32 g ring, L 16, staggered cursors"),
@@ -253,7 +258,10 @@ class Layer:
         self.state = self.ckpt.clone() if with_state else None  # for the conventional kernel
         self.ckpt_lp = self.ckpt.to(td[spec["lp"]]) if spec.get("lp") else None  # two-precision read copy
         self.ring_v = (randn(B, H, L, dv) / sk).to(td[spec["ring"]])
-        self.ring_k = (unit(randn(B, H, L, dk)) if gdn else randn(B, H, L, dk) / sk).to(td[spec["ring"]])
+        G = spec.get("groups", 0)
+        KH = G or H  # key / query vectors per row
+        self.ring_k = (unit(randn(B, KH, L, dk)) if gdn else randn(B, KH, L, dk) / sk).to(td[spec["ring"]])
+        self.kq = torch.empty(B * G * L, device=device) if G else None
         self.ring_a = decay(B, H, L)
         self.slot_idx = torch.arange(B, device=device, dtype=torch.int32)
         self.out = torch.empty(B, H, dv, device=device)
@@ -264,8 +272,10 @@ class Layer:
                 x.update(k=unit(randn(B, H, dk)).to(td[spec["inp"]]), q=unit(randn(B, H, dk)).to(td[spec["inp"]]),
                          alpha=decay(B, H), beta=torch.sigmoid(randn(B, H)))
             else:
-                x.update(k=(randn(B, H, dk) / sk).to(td[spec["inp"]]), q=(randn(B, H, dk) / sk).to(td[spec["inp"]]),
+                x.update(k=(randn(B, KH, dk) / sk).to(td[spec["inp"]]), q=(randn(B, KH, dk) / sk).to(td[spec["inp"]]),
                          alpha=decay(B, H), beta=None)
+            if G:  # the conventional kernel takes a key per head
+                x.update(k_h=x["k"].repeat_interleave(H // G, dim=1), q_h=x["q"].repeat_interleave(H // G, dim=1))
             self.inputs.append(x)
         rng = np.random.default_rng(seed)
         self.decode_step0 = rng.integers(0, L, size=B).astype(np.int64)
@@ -290,13 +300,13 @@ class Layer:
         if self.spec["variant"] == "gdn":
             self.lib.replayssm_decode_gdn(beta=x["beta"], **kw)
         else:
-            self.lib.replayssm_decode_mamba2(ckpt_lp=self.ckpt_lp, **kw)
+            self.lib.replayssm_decode_mamba2(ckpt_lp=self.ckpt_lp, kq_scratch=self.kq, **kw)
 
     def conventional_step(self, t, stream=None):
         x = self.inputs[t % N_INPUT_SETS]
         self.lib.conventional_decode(variant=self.variant_code, state=self.state, slot_idx=self.slot_idx, v=x["v"],
-                                     k=x["k"], q=x["q"], alpha=x["alpha"], beta=x["beta"], out=self.out,
-                                     stream=stream)
+                                     k=x.get("k_h", x["k"]), q=x.get("q_h", x["q"]), alpha=x["alpha"],
+                                     beta=x["beta"], out=self.out, stream=stream)
 
     def bytes_per_step(self, t0, t1, replay=True):
         from linear_attention_decode_replayssm_gb300 import traffic
@@ -308,7 +318,8 @@ class Layer:
             tot += traffic.step_bytes(variant=s["variant"], H=s["H"], d_v=s["d_v"], d_k=s["d_k"],
                                       ckpt_dtype=s["ckpt"], in_dtype=s["inp"], ring_dtype=s["ring"],
                                       slot_idx=slot, write_pos=self.wp_host[t], is_flush=self.fl_host[t],
-                                      replay=replay, lp_dtype=s.get("lp") if replay else None)
+                                      replay=replay, lp_dtype=s.get("lp") if replay else None,
+                                      n_groups=s.get("groups", 0) if replay else 0)
         return tot / (t1 - t0)
 
 

@@ -66,7 +66,7 @@ extern "C" {
 /* Same type as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st *rs_stream_t;
 
-#define RS_ABI_VERSION 2
+#define RS_ABI_VERSION 3
 #define RS_MAX_L 64 /* largest supported buffer length */
 
 typedef enum {
@@ -152,6 +152,15 @@ typedef struct rs_step_args {
   void *ckpt_lp;
   int32_t lp_dtype;
   int32_t reserved2; /* must be 0 */
+  /* Group-shared keys (Mamba-2 only; 0 = a key per head): with n_groups = G
+   * dividing H, k and q are [B, .. G, d_k] (head h reads group h / (H / G)),
+   * ring_k is [num_slots, G, L, d_k], and kq_scratch is caller-owned device
+   * memory of B * G * L floats that the call uses for the group dots
+   * k_j . q_t ([Ghana] §Output without a state: computed once per group by
+   * a small kernel ahead of the decode).  Not combinable with ckpt_lp. */
+  int32_t n_groups;
+  int32_t reserved3; /* must be 0 */
+  float *kq_scratch;
 } rs_step_args;
 
 /* RS_ABI_VERSION of the loaded library. */

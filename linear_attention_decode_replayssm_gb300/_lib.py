@@ -20,7 +20,7 @@ RS_OK, RS_EINVAL, RS_EUNSUPPORTED, RS_EALIGN, RS_ECUDA = 0, -1, -2, -3, -4
 RS_F32, RS_F16, RS_BF16 = 0, 1, 2
 RS_MAMBA2, RS_GDN = 0, 1
 RS_DERR_SLOT, RS_DERR_WRITE_POS, RS_DERR_TIMEOUT, RS_DERR_DST, RS_DERR_ACCEPTED = 1, 2, 4, 8, 16
-RS_ABI_VERSION = 2
+RS_ABI_VERSION = 3
 RS_MAX_L = 64
 
 # every symbol include/replayssm.h declares
@@ -56,6 +56,7 @@ class StepArgs(ctypes.Structure):
         ("stride_q_row", ctypes.c_int64), ("stride_out_row", ctypes.c_int64),
         ("dev_err", ctypes.c_void_p),
         ("ckpt_lp", ctypes.c_void_p), ("lp_dtype", ctypes.c_int32), ("reserved2", ctypes.c_int32),
+        ("n_groups", ctypes.c_int32), ("reserved3", ctypes.c_int32), ("kq_scratch", ctypes.c_void_p),
     ]
 
 
@@ -235,7 +236,7 @@ def _rows(t, name, H, d):
 
 
 def _fill(args, *, variant, ckpt, slot_idx, v, k, q, alpha, out, beta=None, ring_v=None, ring_k=None,
-          ring_a=None, write_pos=None, is_flush=None, dev_err=None, ckpt_lp=None):
+          ring_a=None, write_pos=None, is_flush=None, dev_err=None, ckpt_lp=None, kq_scratch=None):
     torch = _torch()
     _need(ckpt, "ckpt", ndim=4)
     if not ckpt.is_contiguous():
@@ -261,9 +262,22 @@ def _fill(args, *, variant, ckpt, slot_idx, v, k, q, alpha, out, beta=None, ring
     args.slot_idx, args.ckpt = slot_idx.data_ptr(), ckpt.data_ptr()
     args.v, args.k, args.q = v.data_ptr(), k.data_ptr(), q.data_ptr()
     args.alpha, args.out = alpha.data_ptr(), out.data_ptr()
+    # group-shared keys and queries: k, q [B, G, d_k] with G dividing H
+    KH = k.shape[1]
+    G = 0 if KH == H else KH
+    if G and (H % G or q.shape[1] != G):
+        raise ValueError(f"k and q must have H = {H} heads or a number of groups dividing it")
     args.stride_v_row = _rows(v, "v", H, d_v)
-    args.stride_k_row = _rows(k, "k", H, d_k)
-    args.stride_q_row = _rows(q, "q", H, d_k)
+    args.stride_k_row = _rows(k, "k", KH, d_k)
+    args.stride_q_row = _rows(q, "q", KH, d_k)
+    args.n_groups, args.reserved3 = G, 0
+    if G:
+        _need(kq_scratch, "kq_scratch", torch.float32)
+        if kq_scratch.numel() < B * G * ring_a.shape[2] or not kq_scratch.is_contiguous():
+            raise ValueError("kq_scratch must be a contiguous float32 buffer of at least B * G * L elements")
+        args.kq_scratch = kq_scratch.data_ptr()
+    else:
+        args.kq_scratch = None
     args.stride_out_row = _rows(out, "out", H, d_v)
     if variant == RS_GDN:
         _need(beta, "beta", torch.float32, 2)
@@ -273,7 +287,7 @@ def _fill(args, *, variant, ckpt, slot_idx, v, k, q, alpha, out, beta=None, ring
     else:
         args.beta = None
     if ring_v is not None:
-        for name, t, shp in (("ring_v", ring_v, (S, H, None, d_v)), ("ring_k", ring_k, (S, H, None, d_k)),
+        for name, t, shp in (("ring_v", ring_v, (S, H, None, d_v)), ("ring_k", ring_k, (S, k.shape[1], None, d_k)),
                              ("ring_a", ring_a, (S, H, None))):
             _need(t, name)
             if not t.is_contiguous() or t.dim() != len(shp) or any(
@@ -318,13 +332,15 @@ def _stream(stream):
 
 
 def replayssm_decode_mamba2(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos, is_flush, v, k, q, alpha,
-                            out, dev_err=None, stream=None, ckpt_lp=None):
+                            out, dev_err=None, stream=None, ckpt_lp=None, kq_scratch=None):
     """One ReplaySSM Mamba-2 decode step in place on ckpt and the rings; o in
     ``out``.  ``ckpt_lp`` (fp16 or bf16, shape of ckpt) makes ckpt the
-    recurrence copy of a two-precision checkpoint and ckpt_lp its read copy."""
+    recurrence copy of a two-precision checkpoint and ckpt_lp its read copy.
+    k and q of shape [B, G, d_k] (G < H groups) select group-shared keys,
+    with ring_k [slots, G, L, d_k] and a float32 ``kq_scratch`` of B * G * L."""
     args = _fill(StepArgs(), variant=RS_MAMBA2, ckpt=ckpt, slot_idx=slot_idx, v=v, k=k, q=q, alpha=alpha,
                  out=out, ring_v=ring_v, ring_k=ring_k, ring_a=ring_a, write_pos=write_pos,
-                 is_flush=is_flush, dev_err=dev_err, ckpt_lp=ckpt_lp)
+                 is_flush=is_flush, dev_err=dev_err, ckpt_lp=ckpt_lp, kq_scratch=kq_scratch)
     return _check(load().replayssm_decode_mamba2(ctypes.byref(args), _stream(stream)), "replayssm_decode_mamba2")
 
 

@@ -149,7 +149,9 @@ int validate(const rs_step_args *a, bool replay, bool gdn) {
   if (gdn && !a->beta) return RS_EINVAL;
   if (replay && (!a->write_pos || !a->is_flush || !a->ring_v || !a->ring_k || !a->ring_a)) return RS_EINVAL;
   const int64_t H = a->H;
-  if (a->stride_v_row < H * a->d_v || a->stride_k_row < H * a->d_k || a->stride_q_row < H * a->d_k ||
+  if (a->n_groups < 0 || a->reserved3 != 0) return RS_EINVAL;
+  const int64_t KH = a->n_groups > 0 ? a->n_groups : H;  // key / query vectors per row
+  if (a->stride_v_row < H * a->d_v || a->stride_k_row < KH * a->d_k || a->stride_q_row < KH * a->d_k ||
       a->stride_out_row < H * a->d_v)
     return RS_EINVAL;
   const size_t ie = esize(a->in_dtype);
@@ -163,6 +165,13 @@ int validate(const rs_step_args *a, bool replay, bool gdn) {
   }
   if ((int64_t)a->B * a->H > 0x7fffffffLL) return RS_EINVAL;
   if (a->reserved2 != 0) return RS_EINVAL;
+  if (a->n_groups > 0) {
+    // group-shared keys: Mamba-2 replay only, with its scratch
+    if (!replay || gdn || a->ckpt_lp) return RS_EUNSUPPORTED;
+    if (a->H % a->n_groups != 0) return RS_EINVAL;
+    if (!a->kq_scratch) return RS_EINVAL;
+    if (!aligned4(a->kq_scratch)) return RS_EALIGN;
+  }
   if (a->ckpt_lp) {
     // two-precision checkpoint: Mamba-2 replay, fp32 recurrence copy, 16-bit read copy
     if (!replay || gdn) return RS_EUNSUPPORTED;
@@ -193,6 +202,8 @@ rs::KArgs to_kargs(const rs_step_args *a) {
   k.ring_k = a->ring_k;
   k.ring_a = a->ring_a;
   k.ckpt_lp = a->ckpt_lp;
+  k.n_groups = a->n_groups;
+  k.kq = a->kq_scratch;
   k.out = a->out;
   k.sv = a->stride_v_row;
   k.sk = a->stride_k_row;
@@ -216,7 +227,7 @@ int replayssm_abi_version(void) { return RS_ABI_VERSION; }
 
 int replayssm_supported(int variant, int d_v, int d_k, int ckpt_dtype) {
   if (variant != RS_MAMBA2 && variant != RS_GDN) return 0;
-  if (variant == RS_MAMBA2) return rs::find_mamba2(d_v, d_k, ckpt_dtype, RS_BF16, -1) != nullptr;
+  if (variant == RS_MAMBA2) return rs::find_mamba2(d_v, d_k, ckpt_dtype, RS_BF16, -1, false) != nullptr;
   return rs::find_gdn(d_v, d_k, ckpt_dtype, RS_F16, RS_BF16) != nullptr;
 }
 
@@ -325,7 +336,8 @@ int replayssm_decode_mamba2(const rs_step_args *args, rs_stream_t stream) {
   const int st = validate(args, /*replay=*/true, /*gdn=*/false);
   if (st != RS_OK || args->B == 0) return st;
   const int lp = args->ckpt_lp ? args->lp_dtype : -1;
-  return run(rs::find_mamba2(args->d_v, args->d_k, args->ckpt_dtype, args->in_dtype, lp), args, stream);
+  return run(rs::find_mamba2(args->d_v, args->d_k, args->ckpt_dtype, args->in_dtype, lp, args->n_groups > 0), args,
+             stream);
 }
 
 int replayssm_decode_gdn(const rs_step_args *args, rs_stream_t stream) {

@@ -32,6 +32,8 @@ struct KArgs {
   const float *alpha, *beta;
   void *ckpt, *ring_v, *ring_k;
   void *ckpt_lp;  // read copy of a two-precision checkpoint, or nullptr
+  int n_groups;   // 0: a key per head; > 0: keys and queries shared by groups
+  float *kq;      // [B, n_groups, L] scratch for the group dots k_j . q_t
   float *ring_a, *out;
   long long sv, sk, sq, so;  // row strides in elements
   int32_t *dev_err;

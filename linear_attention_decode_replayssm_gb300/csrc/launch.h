@@ -11,8 +11,9 @@ namespace rs {
 using LaunchFn = cudaError_t (*)(const KArgs &, cudaStream_t);
 
 // nullptr when the (d_v, d_k, checkpoint dtype) combination is not built in.
-// lp_dtype: read-copy type of a two-precision checkpoint, or -1 for none
-LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype, int lp_dtype);
+// lp_dtype: read-copy type of a two-precision checkpoint, or -1 for none;
+// grouped: keys and queries shared by groups of heads
+LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype, int lp_dtype, bool grouped);
 LaunchFn find_gdn(int d_v, int d_k, int ckpt_dtype, int ring_dtype, int in_dtype);
 LaunchFn find_conventional(int variant, int d_v, int d_k, int ckpt_dtype);
 

@@ -70,7 +70,11 @@ __host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(
 // LMAX bounds the buffer length at compile time (L <= LMAX): loops over a
 // window's records unroll to a fixed count with predicated bodies.
 // TL is the read-copy type of a two-precision checkpoint (TL == TC: one copy).
-template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX>
+// GRP: group-shared keys and queries (k, q [B, G, d_k], ring_k [slots, G, L,
+// d_k]); the window's k_j . q_t were computed once per group by
+// mamba2_group_kq_kernel into a.kq, and non-flush units read those instead of
+// key records.
+template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP>
 __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr bool TWO = !std::is_same<TC, TL>::value;
@@ -182,19 +186,33 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
           }
           constexpr uint32_t kb = DK * RES, vb = DV * RES;
           constexpr int KC = kb / 16, VC = vb / 16;  // 16-byte chunks per k / v record
-          const unsigned char *rk = static_cast<const unsigned char *>(a.ring_k) + unit * L * kb;
+          // key and query of the unit: its own (per-head layout) or its group's
+          const int kh = GRP ? h / (a.H / a.n_groups) : h;
+          const size_t kunit = GRP ? (size_t)slot * a.n_groups + kh : unit;
+          const unsigned char *rk = static_cast<const unsigned char *>(a.ring_k) + kunit * L * kb;
           const unsigned char *rv = static_cast<const unsigned char *>(a.ring_v) + unit * L * vb;
           const unsigned char *kin =
-              static_cast<const unsigned char *>(a.k) + ((size_t)b * a.sk + (size_t)h * DK) * RES;
+              static_cast<const unsigned char *>(a.k) + ((size_t)b * a.sk + (size_t)kh * DK) * RES;
           const unsigned char *vin =
               static_cast<const unsigned char *>(a.v) + ((size_t)b * a.sv + (size_t)h * DV) * RES;
           const unsigned char *qin =
-              static_cast<const unsigned char *>(a.q) + ((size_t)b * a.sq + (size_t)h * DK) * RES;
+              static_cast<const unsigned char *>(a.q) + ((size_t)b * a.sq + (size_t)kh * DK) * RES;
+          if (!GRP || fl) {
 #pragma unroll
-          for (int i = 0; i < (LMAX * KC + 31) / 32; ++i) {
-            const int cc = lane + 32 * i;
-            if (cc < (p + 1) * KC)
-              cp_async16(st + lay.k + cc * 16, (cc < p * KC ? rk + cc * 16 : kin + (cc - p * KC) * 16));
+            for (int i = 0; i < (LMAX * KC + 31) / 32; ++i) {
+              const int cc = lane + 32 * i;
+              if (cc < (p + 1) * KC)
+                cp_async16(st + lay.k + cc * 16, (cc < p * KC ? rk + cc * 16 : kin + (cc - p * KC) * 16));
+            }
+          } else {
+            // the group's k_j . q_t of the window, into the dots scratch of the slot
+            float *ss = reinterpret_cast<float *>(st + lay.scr) + L;
+            const float *kq = a.kq + ((size_t)b * a.n_groups + kh) * L;
+#pragma unroll
+            for (int i = 0; i < (LMAX + 31) / 32; ++i) {
+              const int jj = lane + 32 * i;
+              if (jj <= p) cp_async4(ss + jj, kq + jj);
+            }
           }
 #pragma unroll
           for (int i = 0; i < (LMAX * VC + 31) / 32; ++i) {
@@ -300,8 +318,9 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       lds_cols<E>(st + lay.q, cv * E, RDT, qv);
       // s_j = k_j . q: a warp takes records four at a time; each lane holds
       // its 4-column chunk of q and accumulates four partial dots, and one
-      // transposed reduction finishes the chunk
-      {
+      // transposed reduction finishes the chunk (group-shared keys: the
+      // producer brought the group's dots instead)
+      if constexpr (!GRP) {
         constexpr int QPL = (DK + 127) / 128;  // 4-column chunks of q per lane
         float qq[QPL][4];
 #pragma unroll
@@ -392,8 +411,9 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
           for (int e = 0; e < 8; ++e) orow[rg * 8 + e] = fmaf(gam, sC[rg * 8 + e], acc[e]);
         }
       }
-      // append the current record (k, v verbatim, alpha) at ring slot p
-      constexpr int KCH = DK * RES / 16, VCH = DV * RES / 16;
+      // append the current record (k, v verbatim, alpha) at ring slot p; a
+      // group-shared key was appended by the group's dot kernel
+      constexpr int KCH = GRP ? 0 : DK * RES / 16, VCH = DV * RES / 16;
       constexpr int APP0 = NCW > 1 ? 32 : 0;  // warp 0 is busy with the output
       for (int c = ctid - APP0; c >= 0 && c < KCH + VCH; c += NC - APP0) {
         if (c < KCH) {
@@ -459,9 +479,81 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
 }
 
-template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX>
+// Group-shared keys ([Ghana] §Output without a state: the released kernel
+// reads precomputed k_j . q from a small kernel that runs once per group):
+// one warp per (row, group) computes s_j = k_j . q_t for the window's records
+// j < p and the current key (j = p) into a.kq[b, g, :], and on a non-flush
+// row appends the current key to the group's ring at slot p.  Rows whose
+// slot or cursor is out of range are left to the decode kernel to report.
+template <int DK, typename RT>
+__global__ void __launch_bounds__(256) mamba2_group_kq_kernel(const KArgs a) {
+  constexpr int RES = (int)sizeof(RT);
+  constexpr int RDT = Rec<RT>::kDtype;
+  constexpr int KPL = (DK + 127) / 128;  // 4-column chunks per lane
+  const int lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (pair >= a.B * a.n_groups) return;
+  const int b = pair / a.n_groups, g = pair - (pair / a.n_groups) * a.n_groups;
+  const int slot = __ldg(a.slot_idx + b), p = __ldg(a.write_pos + b), L = a.L;
+  if (slot < 0 || slot >= a.num_slots || p < 0 || p >= L) return;
+  const bool flush = __ldg(a.is_flush + b) != 0;
+  const size_t kunit = (size_t)slot * a.n_groups + g;
+  const unsigned char *rk = static_cast<const unsigned char *>(a.ring_k) + kunit * L * DK * RES;
+  const unsigned char *kin = static_cast<const unsigned char *>(a.k) + ((size_t)b * a.sk + (size_t)g * DK) * RES;
+  const unsigned char *qin = static_cast<const unsigned char *>(a.q) + ((size_t)b * a.sq + (size_t)g * DK) * RES;
+  float qq[KPL][4];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int col = lane * 4 + i * 128;
+    if (col < DK) {
+      lds_cols<4>(qin, col, RDT, qq[i]);
+    } else {
+      qq[i][0] = qq[i][1] = qq[i][2] = qq[i][3] = 0.f;
+    }
+  }
+  float *kq = a.kq + (size_t)pair * L;
+  for (int j0 = 0; j0 <= p; j0 += 4) {
+    float part[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int j = j0 + r;
+      float acc = 0.f;
+      if (j <= p) {
+        const unsigned char *rec = j < p ? rk + (size_t)j * DK * RES : kin;
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) {
+          const int col = lane * 4 + i * 128;
+          if (col < DK) {
+            float kk[4];
+            lds_cols<4>(rec, col, RDT, kk);
+            acc = fmaf(kk[0], qq[i][0], fmaf(kk[1], qq[i][1], fmaf(kk[2], qq[i][2], fmaf(kk[3], qq[i][3], acc))));
+          }
+        }
+      }
+      part[r] = acc;
+    }
+    group_reduce<4, 32>(part, lane);
+    if (group_reduce_writer<4, 32>(lane)) {
+      const int j = j0 + group_reduce_index<4, 32>(lane);
+      if (j <= p) kq[j] = part[0];
+    }
+  }
+  if (!flush) {
+    constexpr int KC = DK * RES / 16;
+    for (int c = lane; c < KC; c += 32)
+      reinterpret_cast<uint4 *>(const_cast<unsigned char *>(rk) + (size_t)p * DK * RES)[c] =
+          reinterpret_cast<const uint4 *>(kin)[c];
+  }
+}
+
+template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP = false>
 static cudaError_t launch_mamba2_l(const KArgs &a, cudaStream_t s) {
-  auto kern = mamba2_replay_kernel<DV, DK, TC, TL, RT, NCW, NGRP, LMAX>;
+  if (GRP) {
+    mamba2_group_kq_kernel<DK, RT><<<(unsigned)(((size_t)a.B * a.n_groups + 7) / 8), 256, 0, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = mamba2_replay_kernel<DV, DK, TC, TL, RT, NCW, NGRP, LMAX, GRP>;
   constexpr int threads = NGRP * NCW * 32 + 32;
   const size_t ckb = (size_t)DV * DK * sizeof(TC);
   const size_t rb = m2_rec(DV, DK, (int)sizeof(RT), a.L).bytes;
@@ -477,6 +569,13 @@ template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, typename 
 static cudaError_t launch_mamba2(const KArgs &a, cudaStream_t s) {
   return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 16>(a, s)
                    : launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, RS_MAX_L>(a, s);
+}
+
+// group-shared keys: the group dot kernel, then the decode
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP>
+static cudaError_t launch_mamba2_grp(const KArgs &a, cudaStream_t s) {
+  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, 16, true>(a, s)
+                   : launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, RS_MAX_L, true>(a, s);
 }
 
 template <typename RT>
@@ -503,7 +602,23 @@ static LaunchFn find_mamba2_t(int d_v, int d_k, int ckpt_dtype, int lp_dtype) {
   return nullptr;
 }
 
-LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype, int lp_dtype) {
+template <typename RT>
+static LaunchFn find_mamba2_grp_t(int d_v, int d_k, int ckpt_dtype) {
+  if (ckpt_dtype == kF32) {
+    if (d_v == 16 && d_k == 32) return launch_mamba2_grp<16, 32, float, RT, 4, 1>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2_grp<64, 128, float, RT, 4, 2>;
+  } else if (ckpt_dtype == kF16) {
+    if (d_v == 64 && d_k == 128) return launch_mamba2_grp<64, 128, __half, RT, 8, 1>;
+  }
+  return nullptr;
+}
+
+LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype, int lp_dtype, bool grouped) {
+  if (grouped) {
+    if (lp_dtype >= 0) return nullptr;
+    return in_dtype == kF32 ? find_mamba2_grp_t<float>(d_v, d_k, ckpt_dtype)
+                            : find_mamba2_grp_t<__nv_bfloat16>(d_v, d_k, ckpt_dtype);
+  }
   return in_dtype == kF32 ? find_mamba2_t<float>(d_v, d_k, ckpt_dtype, lp_dtype)
                           : find_mamba2_t<__nv_bfloat16>(d_v, d_k, ckpt_dtype, lp_dtype);
 }

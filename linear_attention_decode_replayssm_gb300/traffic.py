@@ -20,30 +20,38 @@ ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
 
 
 def step_bytes(*, variant, H, d_v, d_k, ckpt_dtype, in_dtype, ring_dtype, slot_idx, write_pos=None,
-               is_flush=None, replay=True, lp_dtype=None):
+               is_flush=None, replay=True, lp_dtype=None, n_groups=0):
     """Bytes one launch moves for the given per-row cursors (NumPy arrays [B]).
 
     With a two-precision checkpoint (``lp_dtype``), a non-flush row reads the
     read copy instead of the checkpoint, and a flush row reads the checkpoint
-    and writes both copies."""
+    and writes both copies.  With group-shared keys (``n_groups`` > 0) a row's
+    keys, queries and key records are counted once per group: a record is
+    H (d_v + 1 decay) values plus G d_k keys (the group dots exchanged through
+    the small scratch between the two kernels are not counted)."""
     slot_idx = np.asarray(slot_idx)
     live = slot_idx >= 0
     n_live = int(live.sum())
     n_pad = int((~live).sum())
     state = d_v * d_k * ESIZE[ckpt_dtype]
-    io = (d_v + 2 * d_k) * ESIZE[in_dtype] + 4 + (4 if variant == "gdn" else 0) + 4 * d_v
+    ie, re = ESIZE[in_dtype], ESIZE[ring_dtype]
     meta = 4 + (5 if replay else 0)
+    if n_groups:
+        io_row = H * (d_v * ie + 4 + 4 * d_v) + n_groups * 2 * d_k * ie
+        rec_row = H * (d_v * re + 4) + n_groups * d_k * re
+    else:
+        io_row = H * ((d_v + 2 * d_k) * ie + 4 + (4 if variant == "gdn" else 0) + 4 * d_v)
+        rec_row = H * ((d_v + d_k) * re + 4)
     if not replay:
-        return n_live * (H * (2 * state + io) + meta) + n_pad * (4 + H * 4 * d_v)
-    total = n_live * (H * io + meta) + n_pad * (4 + H * 4 * d_v)
-    rec = (d_v + d_k) * ESIZE[ring_dtype] + 4
+        return n_live * (H * 2 * state + io_row + meta) + n_pad * (4 + H * 4 * d_v)
+    total = n_live * (io_row + meta) + n_pad * (4 + H * 4 * d_v)
     p = np.asarray(write_pos, dtype=np.int64)[live]
     fl = np.asarray(is_flush)[live] != 0
     n_fl, n_nf = int(fl.sum()), int((~fl).sum())
     read_nf = state if lp_dtype is None else d_v * d_k * ESIZE[lp_dtype]
     write_fl = state if lp_dtype is None else state + d_v * d_k * ESIZE[lp_dtype]
-    total += int(p.sum()) * H * rec
-    total += n_fl * H * (state + write_fl) + n_nf * H * (read_nf + rec)
+    total += int(p.sum()) * rec_row
+    total += n_fl * H * (state + write_fl) + n_nf * (H * read_nf + rec_row)
     return total
 
 

@@ -296,3 +296,25 @@ def _spec_args(lib, **kw):
 def test_spec_verify_validation(lib, change, want):
     st = lib.raw_call("replayssm_spec_verify_mamba2", _spec_args(lib, **change), None)
     assert st == getattr(lib, want), lib.status_string(st)
+
+
+@pytest.mark.parametrize("change, entry, want", [
+    (dict(n_groups=3, H=4, kq_scratch=0xF000), "replayssm_decode_mamba2", "RS_EINVAL"),     # must divide H
+    (dict(n_groups=2, H=4, kq_scratch=None), "replayssm_decode_mamba2", "RS_EINVAL"),       # scratch needed
+    (dict(n_groups=2, H=4, kq_scratch=0xF002), "replayssm_decode_mamba2", "RS_EALIGN"),
+    (dict(n_groups=2, H=4, kq_scratch=0xF000, ckpt_lp=0xE000, lp_dtype=1), "replayssm_decode_mamba2",
+     "RS_EUNSUPPORTED"),
+    (dict(n_groups=2, H=4, kq_scratch=0xF000, ring_dtype=1), "replayssm_decode_gdn", "RS_EUNSUPPORTED"),
+    (dict(n_groups=-1), "replayssm_decode_mamba2", "RS_EINVAL"),
+    (dict(reserved3=1), "replayssm_decode_mamba2", "RS_EINVAL"),
+    (dict(n_groups=2, H=4, kq_scratch=0xF000, stride_k_row=128), "replayssm_decode_mamba2", "RS_EINVAL"),
+])
+def test_grouped_key_validation(lib, change, entry, want):
+    kw = dict(stride_v_row=4 * 64, stride_k_row=4 * 128, stride_q_row=4 * 128, stride_out_row=4 * 64)
+    kw.update(change)
+    st = lib.raw_call(entry, _args(lib, **kw), None)
+    assert st == getattr(lib, want), lib.status_string(st)
+    # with 2 groups of 2 heads the key rows may be as short as G * d_k
+    ok = _args(lib, H=4, n_groups=2, kq_scratch=0xF000, stride_v_row=4 * 64, stride_k_row=2 * 128,
+               stride_q_row=2 * 128, stride_out_row=4 * 64)
+    assert lib.raw_call("conventional_decode", ok, 0, None) == lib.RS_EUNSUPPORTED

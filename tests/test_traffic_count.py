@@ -90,3 +90,14 @@ def test_two_precision_window_by_hand():
     io = (d_v + 2 * d_k) * 2 + 4 + 4 * d_v
     per_head_window = (L - 1) * lp + hp + hp + lp + (L * (L - 1) // 2) * r + (L - 1) * r
     assert tot == B * H * (per_head_window + L * io) + L * B * 9
+
+
+def test_grouped_records_match_the_printed_record():
+    """Group-shared keys: a step's record traffic is the 18 944-byte layer
+    record the pages price ([Ghana] §The identity) per held record and row."""
+    H, d_v, d_k, G = 128, 64, 128, 8
+    kw = dict(variant="mamba2", H=H, d_v=d_v, d_k=d_k, ckpt_dtype="f32", in_dtype="bf16", ring_dtype="bf16",
+              slot_idx=np.array([0]), is_flush=np.array([0]), n_groups=G)
+    one = traffic.step_bytes(write_pos=np.array([1]), **kw)
+    zero = traffic.step_bytes(write_pos=np.array([0]), **kw)
+    assert one - zero == model.grouped_record_bytes(H, d_v, G, d_k) == 18944
