@@ -323,6 +323,24 @@ int replayssm_spec_commit(const int32_t *committed, const uint8_t *is_flush, con
  * launch (beta unused). */
 int replayssm_decode_mamba2(const rs_step_args *args, rs_stream_t stream);
 
+/* Capacity, in floats, of the library-owned group-dot scratch that
+ * replayssm_decode_mamba2_noalloc uses (B * n_groups * L must fit). */
+#define RS_NOALLOC_KQ_FLOATS (1 << 20)
+
+/*
+ * replayssm_decode_mamba2 for callers that keep no scratch buffer: with
+ * group-shared keys (n_groups > 0) the group dots go to a device array the
+ * library owns (one per device, RS_NOALLOC_KQ_FLOATS floats, created with
+ * the library's module; its address is looked up once per device), so the
+ * call allocates nothing.  kq_scratch must be NULL.  Calls that use the
+ * library scratch must not run concurrently on one device (different
+ * streams, or graphs replayed side by side, would share it).  With
+ * n_groups == 0 this is replayssm_decode_mamba2.  Returns RS_EINVAL when
+ * kq_scratch is set or B * n_groups * L exceeds the capacity; otherwise as
+ * replayssm_decode_mamba2.
+ */
+int replayssm_decode_mamba2_noalloc(const rs_step_args *args, rs_stream_t stream);
+
 /* ReplaySSM Gated DeltaNet cached decode step (alpha = log-gate g, beta used). */
 int replayssm_decode_gdn(const rs_step_args *args, rs_stream_t stream);
 

@@ -22,6 +22,7 @@ RS_MAMBA2, RS_GDN = 0, 1
 RS_DERR_SLOT, RS_DERR_WRITE_POS, RS_DERR_TIMEOUT, RS_DERR_DST, RS_DERR_ACCEPTED = 1, 2, 4, 8, 16
 RS_ABI_VERSION = 3
 RS_MAX_L = 64
+RS_NOALLOC_KQ_FLOATS = 1 << 20
 
 # every symbol include/replayssm.h declares
 EXPORTS = (
@@ -34,6 +35,7 @@ EXPORTS = (
     "replayssm_plan_spec",
     "replayssm_spec_commit",
     "replayssm_decode_mamba2",
+    "replayssm_decode_mamba2_noalloc",
     "replayssm_decode_gdn",
     "conventional_decode",
     "replayssm_status_string",
@@ -119,7 +121,7 @@ def load():
                                         ctypes.c_void_p]
     lib.replayssm_spec_commit.restype = ctypes.c_int
     lib.replayssm_spec_commit.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int32] * 3 + [ctypes.c_void_p] * 4
-    for name in ("replayssm_decode_mamba2", "replayssm_decode_gdn"):
+    for name in ("replayssm_decode_mamba2", "replayssm_decode_mamba2_noalloc", "replayssm_decode_gdn"):
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
         fn.argtypes = [P(StepArgs), ctypes.c_void_p]
@@ -236,7 +238,8 @@ def _rows(t, name, H, d):
 
 
 def _fill(args, *, variant, ckpt, slot_idx, v, k, q, alpha, out, beta=None, ring_v=None, ring_k=None,
-          ring_a=None, write_pos=None, is_flush=None, dev_err=None, ckpt_lp=None, kq_scratch=None):
+          ring_a=None, write_pos=None, is_flush=None, dev_err=None, ckpt_lp=None, kq_scratch=None,
+          library_scratch=False):
     torch = _torch()
     _need(ckpt, "ckpt", ndim=4)
     if not ckpt.is_contiguous():
@@ -271,7 +274,9 @@ def _fill(args, *, variant, ckpt, slot_idx, v, k, q, alpha, out, beta=None, ring
     args.stride_k_row = _rows(k, "k", KH, d_k)
     args.stride_q_row = _rows(q, "q", KH, d_k)
     args.n_groups, args.reserved3 = G, 0
-    if G:
+    if G and library_scratch:
+        args.kq_scratch = None
+    elif G:
         _need(kq_scratch, "kq_scratch", torch.float32)
         if kq_scratch.numel() < B * G * ring_a.shape[2] or not kq_scratch.is_contiguous():
             raise ValueError("kq_scratch must be a contiguous float32 buffer of at least B * G * L elements")
@@ -342,6 +347,17 @@ def replayssm_decode_mamba2(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos
                  out=out, ring_v=ring_v, ring_k=ring_k, ring_a=ring_a, write_pos=write_pos,
                  is_flush=is_flush, dev_err=dev_err, ckpt_lp=ckpt_lp, kq_scratch=kq_scratch)
     return _check(load().replayssm_decode_mamba2(ctypes.byref(args), _stream(stream)), "replayssm_decode_mamba2")
+
+
+def replayssm_decode_mamba2_noalloc(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos, is_flush, v, k, q,
+                                    alpha, out, dev_err=None, stream=None):
+    """As ``replayssm_decode_mamba2``; group-shared keys use the library's
+    own scratch (no caller buffer)."""
+    args = _fill(StepArgs(), variant=RS_MAMBA2, ckpt=ckpt, slot_idx=slot_idx, v=v, k=k, q=q, alpha=alpha,
+                 out=out, ring_v=ring_v, ring_k=ring_k, ring_a=ring_a, write_pos=write_pos,
+                 is_flush=is_flush, dev_err=dev_err, library_scratch=True)
+    return _check(load().replayssm_decode_mamba2_noalloc(ctypes.byref(args), _stream(stream)),
+                  "replayssm_decode_mamba2_noalloc")
 
 
 def replayssm_decode_gdn(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos, is_flush, v, k, q, alpha, beta,

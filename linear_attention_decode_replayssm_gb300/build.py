@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libreplayssm.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["abi.cu", "mamba2.cu", "gdn.cu", "conventional.cu", "materialize.cu", "spec.cu"]
+SOURCES = ["abi.cu", "mamba2.cu", "gdn.cu", "conventional.cu", "materialize.cu", "spec.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
