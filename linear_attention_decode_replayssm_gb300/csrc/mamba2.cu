@@ -74,12 +74,16 @@ __host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(
 // d_k]); the window's k_j . q_t were computed once per group by
 // mamba2_group_kq_kernel into a.kq, and non-flush units read those instead of
 // key records.
-template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP>
+// CPR: 16-byte checkpoint chunks a consumer lane holds per state row; its
+// chunks are cv, cv + G, cv + 2G, ... so that a warp's loads of one chunk
+// index cover whole 128-byte lines of the row.
+template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP, int CPR>
 __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr bool TWO = !std::is_same<TC, TL>::value;
   constexpr int E = V::E;
-  constexpr int G = DK / E;          // lanes per state row
+  constexpr int NCH = DK / E;        // 16-byte chunks per state row
+  constexpr int G = NCH / CPR;       // lanes per state row
   constexpr int NC = NCW * 32;       // consumer threads per group
   constexpr int RPP = NC / G;        // state rows per pass of a group
   constexpr int VPT = DV / RPP;      // state rows per consumer thread
@@ -89,7 +93,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   constexpr uint32_t CKB = DV * DK * (uint32_t)sizeof(TC);
   constexpr uint32_t CKB_LP = DV * DK * (uint32_t)sizeof(TL);
   static_assert(!TWO || (E == 4 && sizeof(TL) == 2), "read copy: 16-bit elements under an fp32 checkpoint");
-  static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
+  static_assert(G <= 32 && 32 % G == 0 && NCH % CPR == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && DV % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
   static_assert(DK % 8 == 0 && DV % 8 == 0, "head dims must be multiples of 8");
 
@@ -134,6 +138,8 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       }
     };
     int c_sl, c_wp, c_fl;
+    int ps = 0, pc = 0;         // record and checkpoint slot of unit `it`
+    uint32_t phs = 0, phc = 0;  // parity of it / nsr and it / nsc
     fetch(blockIdx.x, c_sl, c_wp, c_fl);
     bool ok = true;
     for (int ub = blockIdx.x; ok && ub < n_units; ub += 32 * stride) {
@@ -145,12 +151,12 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
         const int slot = __shfl_sync(0xffffffffu, c_sl, j);
         const int p = __shfl_sync(0xffffffffu, c_wp, j);
         const int fl = __shfl_sync(0xffffffffu, c_fl, j);
-        const int s = it % nsr, c = it % nsc;
+        const int s = ps, c = pc;
         if (it >= nsr || it >= nsc) {
           int w = 1;
           if (lane == 0) {
-            if (it >= nsr) w = mbar_wait(&rec_empty[s], ((uint32_t)(it / nsr) & 1u) ^ 1u) ? 1 : 0;
-            if (w && it >= nsc) w = mbar_wait(&ck_empty[c], ((uint32_t)(it / nsc) & 1u) ^ 1u) ? 1 : 0;
+            if (it >= nsr) w = mbar_wait(&rec_empty[s], phs ^ 1u) ? 1 : 0;
+            if (w && it >= nsc) w = mbar_wait(&ck_empty[c], phc ^ 1u) ? 1 : 0;
           }
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w || *(volatile int *)s_abort) {
@@ -234,6 +240,14 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
         if (lane == 0) mbar_arrive(&full[s]);  // releases the meta words
         cp_async_arrive(&full[s]);
         ++it;
+        if (++ps == nsr) {
+          ps = 0;
+          phs ^= 1u;
+        }
+        if (++pc == nsc) {
+          pc = 0;
+          phc ^= 1u;
+        }
       }
       c_sl = n_sl; c_wp = n_wp; c_fl = n_fl;
     }
@@ -258,15 +272,26 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   const int step_b = ustep / a.H, step_h = ustep - (ustep / a.H) * a.H;
   int b = (int)(blockIdx.x + grp * stride) / a.H;
   int h = (int)(blockIdx.x + grp * stride) - b * a.H;
+  // slot indices and the full-barrier phase, stepped instead of divided
+  int s = grp % nsr, c = grp % nsc;
+  uint32_t ph = (uint32_t)(grp / nsr) & 1u;
   for (int it = grp; ; it += NGRP, h += step_h, b += step_b) {
     if (h >= a.H) {
       h -= a.H;
       ++b;
     }
+    if (it != grp) {
+      s += NGRP;
+      if (s >= nsr) {
+        s -= nsr;
+        ph ^= 1u;
+      }
+      c += NGRP;
+      if (c >= nsc) c -= nsc;
+    }
     const int u = blockIdx.x + it * stride;
     if (u >= n_units) break;
-    const int s = it % nsr, c = it % nsc;
-    if (lane == 0 && !mbar_wait(&full[s], (uint32_t)(it / nsr) & 1u)) *(volatile int *)s_abort = 1;
+    if (lane == 0 && !mbar_wait(&full[s], ph)) *(volatile int *)s_abort = 1;
     gsync();
     if (*(volatile int *)s_abort) break;
 
@@ -309,13 +334,17 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       // two-precision checkpoint) into registers and hand the slot straight
       // back to the producer
       using Raw = typename std::conditional<TWO, uint2, uint4>::type;
-      Raw raw[VPT];
+      Raw raw[VPT][CPR];
 #pragma unroll
-      for (int r = 0; r < VPT; ++r) raw[r] = reinterpret_cast<const Raw *>(ck_slot)[(row0 + r * RPP) * G + cv];
+      for (int r = 0; r < VPT; ++r)
+#pragma unroll
+        for (int i = 0; i < CPR; ++i)
+          raw[r][i] = reinterpret_cast<const Raw *>(ck_slot)[(row0 + r * RPP) * NCH + cv + G * i];
       mbar_arrive(&ck_empty[c]);
       weights();
-      float qv[E];
-      lds_cols<E>(st + lay.q, cv * E, RDT, qv);
+      float qv[CPR][E];
+#pragma unroll
+      for (int i = 0; i < CPR; ++i) lds_cols<E>(st + lay.q, (cv + G * i) * E, RDT, qv[i]);
       // s_j = k_j . q: a warp takes records four at a time; each lane holds
       // its 4-column chunk of q and accumulates four partial dots, and one
       // transposed reduction finishes the chunk (group-shared keys: the
@@ -363,15 +392,18 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       // checkpoint GEMV partials from the stage
 #pragma unroll
       for (int r = 0; r < VPT; ++r) {
-        float f[E];
-        if constexpr (TWO) {
-          LpVec<TL>::unpack(raw[r], f);
-        } else {
-          V::unpack(raw[r], f);
-        }
         float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc = fmaf(f[e], qv[e], acc);
+        for (int i = 0; i < CPR; ++i) {
+          float f[E];
+          if constexpr (TWO) {
+            LpVec<TL>::unpack(raw[r][i], f);
+          } else {
+            V::unpack(raw[r][i], f);
+          }
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc = fmaf(f[e], qv[i][e], acc);
+        }
         part[r] = acc;
       }
       group_reduce<VPT, G>(part, lane);
@@ -426,48 +458,61 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       }
       if (ctid == NC - 1) a.ring_a[unit * L + p] = sa[p];
     } else {
-      uint4 raw[VPT];
+      uint4 raw[VPT][CPR];
 #pragma unroll
-      for (int r = 0; r < VPT; ++r) raw[r] = reinterpret_cast<const uint4 *>(ck_slot)[(row0 + r * RPP) * G + cv];
+      for (int r = 0; r < VPT; ++r)
+#pragma unroll
+        for (int i = 0; i < CPR; ++i)
+          raw[r][i] = reinterpret_cast<const uint4 *>(ck_slot)[(row0 + r * RPP) * NCH + cv + G * i];
       mbar_arrive(&ck_empty[c]);
       weights();
-      float qv[E];
-      lds_cols<E>(st + lay.q, cv * E, RDT, qv);
+      float qv[CPR][E];
+#pragma unroll
+      for (int i = 0; i < CPR; ++i) lds_cols<E>(st + lay.q, (cv + G * i) * E, RDT, qv[i]);
       gsync();  // weights ready
       const float gam = sGam[0];
       TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK);
-      float f[VPT][E];
+      float f[VPT][CPR][E];
 #pragma unroll
-      for (int r = 0; r < VPT; ++r) {
-        V::unpack(raw[r], f[r]);
+      for (int r = 0; r < VPT; ++r)
 #pragma unroll
-        for (int e = 0; e < E; ++e) f[r][e] *= gam;
-      }
+        for (int i = 0; i < CPR; ++i) {
+          V::unpack(raw[r][i], f[r][i]);
+#pragma unroll
+          for (int e = 0; e < E; ++e) f[r][i][e] *= gam;
+        }
 #pragma unroll 4
       for (int j = 0; j <= p; ++j) {
-        float kk[E];
-        lds_cols<E>(sk, j * DK + cv * E, RDT, kk);
+        float kk[CPR][E];
+#pragma unroll
+        for (int i = 0; i < CPR; ++i) lds_cols<E>(sk, j * DK + (cv + G * i) * E, RDT, kk[i]);
         const float wj = sW[j];
 #pragma unroll
         for (int r = 0; r < VPT; ++r) {
           const float vv = wj * lds_elem(sv, j * DV + row0 + r * RPP, RDT);
 #pragma unroll
-          for (int e = 0; e < E; ++e) f[r][e] = fmaf(vv, kk[e], f[r][e]);
+          for (int i = 0; i < CPR; ++i)
+#pragma unroll
+            for (int e = 0; e < E; ++e) f[r][i][e] = fmaf(vv, kk[i][e], f[r][i][e]);
         }
       }
 #pragma unroll
       for (int r = 0; r < VPT; ++r) {
         float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc = fmaf(f[r][e], qv[e], acc);
-        part[r] = acc;
-        st_vec(ckg + (size_t)(row0 + r * RPP) * DK + cv * E, V::pack(f[r]));
-        if constexpr (TWO) {
-          // the read copy: an independent rounding of the same fp32 matrix
-          TL *lpg = static_cast<TL *>(a.ckpt_lp) + unit * (DV * DK);
-          float g4[4] = {f[r][0], f[r][1], f[r][2], f[r][3]};
-          st_vec2(lpg + (size_t)(row0 + r * RPP) * DK + cv * E, LpVec<TL>::pack(g4));
+        for (int i = 0; i < CPR; ++i) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc = fmaf(f[r][i][e], qv[i][e], acc);
+          const size_t off = (size_t)(row0 + r * RPP) * DK + (cv + G * i) * E;
+          st_vec(ckg + off, V::pack(f[r][i]));
+          if constexpr (TWO) {
+            // the read copy: an independent rounding of the same fp32 matrix
+            TL *lpg = static_cast<TL *>(a.ckpt_lp) + unit * (DV * DK);
+            float g4[4] = {f[r][i][0], f[r][i][1], f[r][i][2], f[r][i][3]};
+            st_vec2(lpg + off, LpVec<TL>::pack(g4));
+          }
         }
+        part[r] = acc;
       }
       group_reduce<VPT, G>(part, lane);
       if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
@@ -546,14 +591,15 @@ __global__ void __launch_bounds__(256) mamba2_group_kq_kernel(const KArgs a) {
   }
 }
 
-template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP = false>
+template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP = false,
+          int CPR = 1>
 static cudaError_t launch_mamba2_l(const KArgs &a, cudaStream_t s) {
   if (GRP) {
     mamba2_group_kq_kernel<DK, RT><<<(unsigned)(((size_t)a.B * a.n_groups + 7) / 8), 256, 0, s>>>(a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto kern = mamba2_replay_kernel<DV, DK, TC, TL, RT, NCW, NGRP, LMAX, GRP>;
+  auto kern = mamba2_replay_kernel<DV, DK, TC, TL, RT, NCW, NGRP, LMAX, GRP, CPR>;
   constexpr int threads = NGRP * NCW * 32 + 32;
   const size_t ckb = (size_t)DV * DK * sizeof(TC);
   const size_t rb = m2_rec(DV, DK, (int)sizeof(RT), a.L).bytes;
@@ -565,34 +611,34 @@ static cudaError_t launch_mamba2_l(const KArgs &a, cudaStream_t s) {
 }
 
 // the common short windows get a kernel unrolled for L <= 16
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, typename TL = TC>
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, typename TL = TC, int CPR = 1>
 static cudaError_t launch_mamba2(const KArgs &a, cudaStream_t s) {
-  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 16>(a, s)
-                   : launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, RS_MAX_L>(a, s);
+  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 16, false, CPR>(a, s)
+                   : launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, RS_MAX_L, false, CPR>(a, s);
 }
 
 // group-shared keys: the group dot kernel, then the decode
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP>
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, int CPR = 1>
 static cudaError_t launch_mamba2_grp(const KArgs &a, cudaStream_t s) {
-  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, 16, true>(a, s)
-                   : launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, RS_MAX_L, true>(a, s);
+  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, 16, true, CPR>(a, s)
+                   : launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, RS_MAX_L, true, CPR>(a, s);
 }
 
 template <typename RT>
 static LaunchFn find_mamba2_t(int d_v, int d_k, int ckpt_dtype, int lp_dtype) {
   if (ckpt_dtype == kF32 && lp_dtype == kF16) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1, __half>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __half>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __half, 4>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1, __half>;
   } else if (ckpt_dtype == kF32 && lp_dtype == kBF16) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1, __nv_bfloat16>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __nv_bfloat16>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __nv_bfloat16, 4>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1, __nv_bfloat16>;
   } else if (lp_dtype >= 0) {
     return nullptr;
   } else if (ckpt_dtype == kF32) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, float, 2>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1>;
   } else if (ckpt_dtype == kF16) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, __half, RT, 2, 1>;
