@@ -86,7 +86,7 @@ cudaError_t plan_rings(const void *kernel, int threads, size_t ck_bytes, size_t 
     // preferred shapes, best first: two CTAs per SM each with two
     // checkpoint slots (two producers per SM keep bulk-copy issue off the
     // critical path), then one CTA per SM with fewer or more slots
-    static const int shapes[][3] = {{2, 2, 4}, {2, 2, 3}, {1, 4, 8}, {1, 3, 6}, {1, 2, 4}, {1, 2, 3}, {1, 1, 2}};
+    static const int shapes[][3] = {{2, 2, 4}, {2, 2, 3}, {2, 2, 2}, {1, 4, 8}, {1, 3, 6}, {1, 2, 4}, {1, 2, 3}, {1, 1, 2}};
     int ctas = 0;
     for (const auto &sh : shapes) {
       const size_t budget = (size_t)std::min<long>(d.smem_sm / sh[0] - 1024, d.smem_block);
