@@ -466,7 +466,7 @@ def measure_materialize(lib, torch, layer, args, sampler, launches=32):
     return dict(ms_per_launch=ms / launches, bytes_per_launch=nbytes, launches=launches)
 
 
-def measure_spec(lib, torch, layer, args, sampler, T, steps=256, n_sets=4):
+def measure_spec(lib, torch, layer, args, sampler, T, n_sets=4):
     """Speculative verification of T drafts per row on the layer, with the
     device-side commit of a seeded random number of accepted drafts (1..T),
     both inside one CUDA graph of ``steps`` steps."""
@@ -475,6 +475,7 @@ def measure_spec(lib, torch, layer, args, sampler, T, steps=256, n_sets=4):
     from linear_attention_decode_replayssm_gb300 import traffic
 
     s, dev = layer.spec, layer.device
+    steps = min(256, max(16, args.steps))
     B, H, dv, dk, L = (s[k] for k in ("B", "H", "d_v", "d_k", "L"))
     td = {"f32": torch.float32, "bf16": torch.bfloat16}[s["inp"]]
     g = torch.Generator(device=dev)
@@ -656,7 +657,7 @@ def run_native(args):
         layer = Layer(_lib, spec, device, rank, args.warmup + args.e2e_steps + 4)
     mat, specs = None, []
     if not args.no_extras:
-        mat = measure_materialize(_lib, torch, layer, args, sampler)
+        mat = measure_materialize(_lib, torch, layer, args, sampler, launches=min(32, max(4, args.steps)))
         torch.cuda.empty_cache()
         if spec["variant"] == "mamba2" and not spec.get("lp"):
             for T in (4, 8):
