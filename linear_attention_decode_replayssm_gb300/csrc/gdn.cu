@@ -62,18 +62,21 @@ __host__ __device__ inline uint32_t gdn_head(int nsr, int nsc) { return align128
 
 // LMAX bounds the buffer length at compile time (L <= LMAX): loops over a
 // window's records unroll to a fixed count with predicated bodies.
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP, int LMAX>
+// CPR: 16-byte checkpoint chunks a consumer lane holds per state row (chunks
+// cv, cv + G, ...), so the row reductions run over G = DK / (E CPR) lanes.
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP, int LMAX, int CPR>
 __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr int RB = DV / NSPLIT;    // state rows per unit
   constexpr int E = V::E;
-  constexpr int G = DK / E;          // lanes per state row
+  constexpr int NCH = DK / E;        // 16-byte chunks per state row
+  constexpr int G = NCH / CPR;       // lanes per state row
   constexpr int NC = NCW * 32;       // consumer threads per group
   constexpr int RPP = NC / G;        // state rows per pass
   constexpr int VPT = RB / RPP;      // state rows per consumer thread
   constexpr int PROD = NGRP * NCW;   // warp index of the producer
   constexpr uint32_t CKB = RB * DK * (uint32_t)sizeof(TC);
-  static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
+  static_assert(G <= 32 && 32 % G == 0 && NCH % CPR == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && RB % RPP == 0 && VPT >= 1 && 2 * VPT <= G, "bad tiling");
   static_assert(DK % 8 == 0 && RB % 8 == 0, "head dims must be multiples of 8");
 
@@ -224,11 +227,22 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
   const int lw = warp - grp * NCW, ctid = tid - grp * NC;
   const int row0 = ctid / G, cv = ctid - (ctid / G) * G;
   auto gsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(NC) : "memory"); };
+  // slot indices and the full-barrier phase, stepped instead of divided
+  int s = grp % nsr, c = grp % nsc;
+  uint32_t ph = (uint32_t)(grp / nsr) & 1u;
   for (int it = grp; ; it += NGRP) {
+    if (it != grp) {
+      s += NGRP;
+      if (s >= nsr) {
+        s -= nsr;
+        ph ^= 1u;
+      }
+      c += NGRP;
+      if (c >= nsc) c -= nsc;
+    }
     const int u = blockIdx.x + it * stride;
     if (u >= n_units) break;
-    const int s = it % nsr, c = it % nsc;
-    if (lane == 0 && !mbar_wait(&full[s], (uint32_t)(it / nsr) & 1u)) *(volatile int *)s_abort = 1;
+    if (lane == 0 && !mbar_wait(&full[s], ph)) *(volatile int *)s_abort = 1;
     gsync();
     if (*(volatile int *)s_abort) break;
 
@@ -246,11 +260,13 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
       mbar_arrive(&rec_empty[s]);
       continue;
     }
-    uint4 raw[VPT];
+    uint4 raw[VPT][CPR];
     {
       const uint4 *ck = reinterpret_cast<const uint4 *>(ck_slots + (size_t)c * CKB);
 #pragma unroll
-      for (int r = 0; r < VPT; ++r) raw[r] = ck[(row0 + r * RPP) * G + cv];
+      for (int r = 0; r < VPT; ++r)
+#pragma unroll
+        for (int i = 0; i < CPR; ++i) raw[r][i] = ck[(row0 + r * RPP) * NCH + cv + G * i];
     }
     mbar_arrive(&ck_empty[c]);
 
@@ -335,20 +351,26 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
       }
     }
     // S_ckpt k_t and S_ckpt q_t for this thread's rows
-    float ktc[E], qc[E];
-    lds_cols<E>(skt, cv * E, idt, ktc);
-    lds_cols<E>(sq, cv * E, idt, qc);
+    float ktc[CPR][E], qc[CPR][E];
+#pragma unroll
+    for (int i = 0; i < CPR; ++i) {
+      lds_cols<E>(skt, (cv + G * i) * E, idt, ktc[i]);
+      lds_cols<E>(sq, (cv + G * i) * E, idt, qc[i]);
+    }
     {
       float part[2 * VPT];
 #pragma unroll
       for (int r = 0; r < VPT; ++r) {
-        float f[E];
-        V::unpack(raw[r], f);
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          s0 = fmaf(f[e], ktc[e], s0);
-          s1 = fmaf(f[e], qc[e], s1);
+        for (int i = 0; i < CPR; ++i) {
+          float f[E];
+          V::unpack(raw[r][i], f);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            s0 = fmaf(f[e], ktc[i][e], s0);
+            s1 = fmaf(f[e], qc[i][e], s1);
+          }
         }
         part[r] = s0;
         part[VPT + r] = s1;
@@ -422,23 +444,28 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
       gsync();  // d_t of every row ready
       TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK) + (size_t)row_off * DK;
       const float scale0 = alpha_t * gam;
-      float f[VPT][E];
+      float f[VPT][CPR][E];
 #pragma unroll
-      for (int r = 0; r < VPT; ++r) {
-        V::unpack(raw[r], f[r]);
+      for (int r = 0; r < VPT; ++r)
 #pragma unroll
-        for (int e = 0; e < E; ++e) f[r][e] *= scale0;
-      }
+        for (int i = 0; i < CPR; ++i) {
+          V::unpack(raw[r][i], f[r][i]);
+#pragma unroll
+          for (int e = 0; e < E; ++e) f[r][i][e] *= scale0;
+        }
 #pragma unroll 4
       for (int j = 0; j < p; ++j) {
-        float kk[E];
-        lds_cols<E>(sk, j * DK + cv * E, rdt, kk);
+        float kk[CPR][E];
+#pragma unroll
+        for (int i = 0; i < CPR; ++i) lds_cols<E>(sk, j * DK + (cv + G * i) * E, rdt, kk[i]);
         const float wj = alpha_t * sW[j];
 #pragma unroll
         for (int r = 0; r < VPT; ++r) {
           const float dd = wj * lds_elem(sd, j * RB + row0 + r * RPP, rdt);
 #pragma unroll
-          for (int e = 0; e < E; ++e) f[r][e] = fmaf(dd, kk[e], f[r][e]);
+          for (int i = 0; i < CPR; ++i)
+#pragma unroll
+            for (int e = 0; e < E; ++e) f[r][i][e] = fmaf(dd, kk[i][e], f[r][i][e]);
         }
       }
       float po[VPT];
@@ -447,12 +474,15 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
         const float dd = sDt[row0 + r * RPP];
         float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          f[r][e] = fmaf(dd, ktc[e], f[r][e]);
-          acc = fmaf(f[r][e], qc[e], acc);
+        for (int i = 0; i < CPR; ++i) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            f[r][i][e] = fmaf(dd, ktc[i][e], f[r][i][e]);
+            acc = fmaf(f[r][i][e], qc[i][e], acc);
+          }
+          st_vec(ckg + (size_t)(row0 + r * RPP) * DK + (cv + G * i) * E, V::pack(f[r][i]));
         }
         po[r] = acc;
-        st_vec(ckg + (size_t)(row0 + r * RPP) * DK + cv * E, V::pack(f[r]));
       }
       group_reduce<VPT, G>(po, lane);
       if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = po[0];
@@ -464,9 +494,9 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
   if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
 }
 
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP, int LMAX>
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP, int LMAX, int CPR>
 static cudaError_t launch_gdn_l(const KArgs &a, cudaStream_t s) {
-  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, LMAX>;
+  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, LMAX, CPR>;
   constexpr int threads = NGRP * NCW * 32 + 32;
   const size_t ckb = (size_t)(DV / NSPLIT) * DK * sizeof(TC);
   const size_t rb = gdn_rec(DV / NSPLIT, DK, (int)sizeof(RT), (int)sizeof(IT), a.L).bytes;
@@ -479,10 +509,10 @@ static cudaError_t launch_gdn_l(const KArgs &a, cudaStream_t s) {
 }
 
 // the common short windows get a kernel unrolled for L <= 16
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP = 1>
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP = 1, int CPR = 1>
 static cudaError_t launch_gdn(const KArgs &a, cudaStream_t s) {
-  return a.L <= 16 ? launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, 16>(a, s)
-                   : launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, RS_MAX_L>(a, s);
+  return a.L <= 16 ? launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, 16, CPR>(a, s)
+                   : launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, RS_MAX_L, CPR>(a, s);
 }
 
 template <typename TC, typename RT, typename IT>
@@ -490,7 +520,7 @@ static LaunchFn find_gdn_t(int d_v, int d_k) {
   constexpr bool f32 = sizeof(TC) == 4;
   if (d_v == 16 && d_k == 32) return launch_gdn<16, 32, TC, RT, IT, f32 ? 4 : 2, 1>;
   if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, TC, RT, IT, 8, 1>;
-  if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, TC, RT, IT, 8, f32 ? 2 : 1>;
+  if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, TC, RT, IT, 8, f32 ? 2 : 1, 1, 2>;
   return nullptr;
 }
 
