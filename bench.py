@@ -221,7 +221,7 @@ def _kernel_traffic(kernel, workload):
 
 
 def source_hash(kernel):
-    files = {"mamba2_replay": ["mamba2.cu"], "gdn_replay": ["gdn.cu"], "conventional": ["conventional.cu"]}[kernel]
+    files = {"mamba2_replay": ["mamba2.cuh", "mamba2.cu"], "gdn_replay": ["gdn.cu"], "conventional": ["conventional.cu"]}[kernel]
     h = hashlib.sha256()
     for name in files + ["common.cuh"]:
         with open(os.path.join(ROOT, "linear_attention_decode_replayssm_gb300", "csrc", name), "rb") as f:
@@ -384,49 +384,70 @@ def measure_layer(lib, torch, spec, device, args, dist, sampler, seed):
 def measure_e2e(lib, torch, layer, steps, dist):
     """Tokens/s through the public API with host buffers: every step copies its
     inputs from pinned host memory, plans the step on the host, launches the
-    decode, and reads the output back to host memory."""
+    decode, and reads the output back to host memory.  Two steps are in
+    flight: step t+1's inputs go up on a copy stream while step t decodes, and
+    the host reads step t's output while step t+1 runs."""
     import numpy as np
 
     dev = layer.device
     B = layer.spec["B"]
     host_in = []
     for x in layer.inputs:
-        host_in.append({n: (t.cpu().pin_memory() if t is not None else None) for n, t in x.items()})
-    d_in = {n: (t.clone() if t is not None else None) for n, t in layer.inputs[0].items()}
-    wp_h = torch.empty(B, dtype=torch.int32).pin_memory()
-    fl_h = torch.empty(B, dtype=torch.uint8).pin_memory()
-    wp_d = torch.empty(B, dtype=torch.int32, device=dev)
-    fl_d = torch.empty(B, dtype=torch.uint8, device=dev)
-    o_h = torch.empty(layer.out.shape, dtype=torch.float32).pin_memory()
+        host_in.append({n: (t.cpu().pin_memory() if t is not None and not n.endswith("_h") else None)
+                        for n, t in x.items()})
+    d_in = [{n: (t.clone() if t is not None and not n.endswith("_h") else None) for n, t in layer.inputs[0].items()}
+            for _ in range(2)]
+    wp_h = [torch.empty(B, dtype=torch.int32).pin_memory() for _ in range(2)]
+    fl_h = [torch.empty(B, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    wp_d = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(2)]
+    fl_d = [torch.empty(B, dtype=torch.uint8, device=dev) for _ in range(2)]
+    o_h = [torch.empty(layer.out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in[0].values() if t is not None)
-    h2d += wp_h.numel() * 4 + fl_h.numel()
-    d2h = o_h.numel() * 4
-    stream = torch.cuda.Stream(device=dev)
-    wp_np, fl_np = wp_h.numpy(), fl_h.numpy()
+    h2d += wp_h[0].numel() * 4 + fl_h[0].numel()
+    d2h = o_h[0].numel() * 4
+    cp = torch.cuda.Stream(device=dev)
+    comp = torch.cuda.Stream(device=dev)
+    up = [torch.cuda.Event() for _ in range(2)]     # inputs of a buffer landed
+    used = [torch.cuda.Event() for _ in range(2)]   # the decode that read a buffer is done
+    back = [torch.cuda.Event() for _ in range(2)]   # output of a step is in host memory
     ds = layer.decode_step0.copy()
 
-    def one(t):
+    def launch(t):
+        i = t % 2
         x = host_in[t % N_INPUT_SETS]
-        with torch.cuda.stream(stream):
+        lib.replayssm_plan_step(ds + t, layer.spec["L"], write_pos=wp_h[i].numpy(), is_flush=fl_h[i].numpy())
+        with torch.cuda.stream(cp):
+            cp.wait_event(used[i])
             for n, t_h in x.items():
                 if t_h is not None:
-                    d_in[n].copy_(t_h, non_blocking=True)
-            lib.replayssm_plan_step(ds + t, layer.spec["L"], write_pos=wp_np, is_flush=fl_np)
-            wp_d.copy_(wp_h, non_blocking=True)
-            fl_d.copy_(fl_h, non_blocking=True)
-            layer.replay_step(t, stream, x=d_in, wp=wp_d, fl=fl_d)
-            o_h.copy_(layer.out, non_blocking=True)
-        stream.synchronize()  # the host holds this step's output
-        return float(o_h[0, 0, 0])
+                    d_in[i][n].copy_(t_h, non_blocking=True)
+            wp_d[i].copy_(wp_h[i], non_blocking=True)
+            fl_d[i].copy_(fl_h[i], non_blocking=True)
+            up[i].record(cp)
+        with torch.cuda.stream(comp):
+            comp.wait_event(up[i])
+            layer.replay_step(t, comp, x=d_in[i], wp=wp_d[i], fl=fl_d[i])
+            used[i].record(comp)
+            o_h[i].copy_(layer.out, non_blocking=True)
+            back[i].record(comp)
 
-    for t in range(3):
-        one(t)
+    def read(t):
+        back[t % 2].synchronize()  # the host holds this step's output
+        return float(o_h[t % 2][0, 0, 0])
+
+    def run(n):
+        launch(0)
+        for t in range(n):
+            if t + 1 < n:
+                launch(t + 1)
+            read(t)
+
+    run(3)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     t0 = time.perf_counter()
-    for t in range(steps):
-        one(t)
+    run(steps)
     el = time.perf_counter() - t0
     if dist is not None:
         tt = torch.tensor([el], device=dev)
@@ -737,8 +758,8 @@ def run_native(args):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "steps": args.e2e_steps,
-            "how": "C ABI with pinned host buffers: H2D of v/k/q/alpha and the host plan, decode, D2H of o, "
-                   "stream sync per step",
+            "how": "C ABI with pinned host buffers: per step the host plan, H2D of v/k/q/alpha and the plan, "
+                   "decode, D2H of o and a host read of it; the next step's H2D overlaps this step's decode",
         },
         "gpu_launches": K,
         "clocks": clocks,

@@ -386,49 +386,33 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
     }
     gsync();
 
-    // per row: S_{t-1} k_t, S_{t-1} q_t, then d_t.  Warp lw takes RW rows
-    // (one vector load of a d record); its lanes split the records, one
-    // transposed reduction folds the 2 x RW sums, and lane r finishes row r.
+    // per row: S_{t-1} k_t, S_{t-1} q_t, then d_t, one thread per row (the
+    // window's weights and key dots are shared-memory broadcasts, the d
+    // records are read row-contiguous, and no cross-lane reduction is needed)
     const float gam = sScal[0], kq = sScal[1];
     const float g_t = sa[L], beta_t = sa[L + 1];
     const float alpha_t = expf(g_t);
-    {
-      constexpr int RW = RB / NCW;  // rows per warp
-      static_assert(RB % NCW == 0 && (RW == 4 || RW == 8 || RW == 16), "bad row layout");
-      const int r0 = lw * RW;
-      float acc[2 * RW];  // [0, RW): S_{t-1} k_t terms, [RW, 2 RW): S_{t-1} q_t terms
+    static_assert(RB <= NC, "one consumer thread per state row");
+    if (ctid < RB) {
+      const int i = ctid;
+      float accK = 0.f, accQ = 0.f;
 #pragma unroll
-      for (int e = 0; e < 2 * RW; ++e) acc[e] = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < (LMAX + 31) / 32; ++jj) {
-        const int j = lane + 32 * jj;
+      for (int j = 0; j < LMAX; ++j) {
         if (j >= p) break;
-        const float ck = sW[j] * sDk[j], cq = sW[j] * sDq[j];
-        float dd[RW];
-        lds_cols<RW>(sd, j * RB + r0, rdt, dd);
-#pragma unroll
-        for (int e = 0; e < RW; ++e) {
-          acc[e] = fmaf(ck, dd[e], acc[e]);
-          acc[RW + e] = fmaf(cq, dd[e], acc[RW + e]);
-        }
+        const float w = sW[j];
+        const float dd = lds_elem(sd, j * RB + i, rdt);
+        accK = fmaf(w * sDk[j], dd, accK);
+        accQ = fmaf(w * sDq[j], dd, accQ);
       }
-      group_reduce<2 * RW, 32>(acc, lane);
-      float *sRow = sC + r0 * 2;  // sC (2 RB floats of scratch) holds this warp's sums
-      if (group_reduce_writer<2 * RW, 32>(lane)) sRow[group_reduce_index<2 * RW, 32>(lane)] = acc[0];
-      __syncwarp();
-      if (lane < RW) {
-        const int i = r0 + lane;
-        const float Ak = fmaf(gam, sAk[i], sRow[lane]);
-        const float Aq = fmaf(gam, sAq[i], sRow[RW + lane]);
-        const float d_t = beta_t * (lds_elem(st + lay.vt, i, idt) - alpha_t * Ak);
-        if (!flush) {
-          orow[i] = fmaf(alpha_t, Aq, d_t * kq);
-          store1(a.ring_v, (unit * L + p) * DV + row_off + i, rdt, d_t);
-        } else {
-          sDt[i] = d_t;
-        }
+      const float Ak = fmaf(gam, sAk[i], accK);
+      const float Aq = fmaf(gam, sAq[i], accQ);
+      const float d_t = beta_t * (lds_elem(st + lay.vt, i, idt) - alpha_t * Ak);
+      if (!flush) {
+        orow[i] = fmaf(alpha_t, Aq, d_t * kq);
+        store1(a.ring_v, (unit * L + p) * DV + row_off + i, rdt, d_t);
+      } else {
+        sDt[i] = d_t;
       }
-      __syncwarp();
     }
     if (!flush) {
       if (half == 0) {

@@ -1,672 +1,34 @@
-// ReplaySSM Mamba-2 cached decode step: non-flush and flush rows in one launch.
-//
-// Sources:
-//   [Ghana] S. Ghana, "ReplaySSM: an SSM decoder that writes its state once
-//           every 16 tokens", §The identity and §Output without a state.
-//   [PR48792] vLLM PR 48792, "[Kernel] ReplaySSM: cache SSM inputs for faster
-//           Gated DeltaNet standard decode", §CUDA graphs and continuous
-//           batching (the flush flag is per-row runtime data).
-//
-// A work unit is one (row b, head h).  With p = write_pos[b] ring records held
-// and the current token as record p (0-based), w_j = prod_{l=j+1..p} alpha_l
-// and gamma = prod_{l=0..p} alpha_l:
-//   non-flush: o = gamma * (S_ckpt q) + sum_{j<=p} w_j (k_j . q) v_j, and the
-//              record (alpha, v, k) is copied into ring slot p;
-//   flush:     S_new = gamma * S_ckpt + sum_{j<=p} w_j v_j k_j^T, o = S_new q
-//              from the fp32 registers, S_new stored (cast) over S_ckpt.
-//
-// Persistent, warp-specialised kernel, two CTAs per SM.  A producer warp
-// streams each unit's checkpoint into a checkpoint slot with one 1-D bulk
-// copy (cp.async.bulk, completion counted on an mbarrier) and its ring
-// records, this token's k, v, q and the decays into a record slot with
-// per-lane cp.async.  It prefetches the per-row slot, cursor and flag 32
-// units ahead, so no dependent global load sits on the streaming path.
-// Consumer groups (two groups of four warps for the 64 x 128 fp32 layer)
-// take alternate units: a group waits for its unit, takes its share of the
-// checkpoint into registers (freeing that slot for the next load at once),
-// computes from the record slot and releases it.  The step is bound by
-// instruction issue as much as by bandwidth, so the per-warp fixed costs of a
-// unit are paid by four warps rather than eight.  The units a CTA owns are
-// strided across the batch, so the ~1/L flush rows (which also write their
-// state) spread evenly over the CTAs.  Every wait is bounded: on a timeout
-// the kernel reports RS_DERR_TIMEOUT, drains its own copies and returns.
-// No tensor cores: the step is a bandwidth-bound GEMV (about 0.6 FLOP/byte).
-#include <type_traits>
-
-#include "common.cuh"
-#include "launch.h"
-#include "replayssm.h"
+// ReplaySSM Mamba-2 cached decode step: the launch table.  The kernels are in
+// mamba2.cuh; their instantiations are spread over three translation units
+// (this one: one checkpoint copy, bf16 inputs; mamba2_variants.cu: read
+// copies and group-shared keys; mamba2_f32in.cu: fp32 inputs) so that they
+// compile in parallel.
+#include "mamba2.cuh"
 
 namespace rs {
 
+LaunchFn find_mamba2_read_copy(int d_v, int d_k, int lp_dtype, int in_dtype);  // mamba2_variants.cu
+LaunchFn find_mamba2_grouped(int d_v, int d_k, int ckpt_dtype, int in_dtype);  // mamba2_variants.cu
+LaunchFn find_mamba2_f32_inputs(int d_v, int d_k, int ckpt_dtype);             // mamba2_f32in.cu
 
-// Shared memory holds two rings: checkpoint slots (the 32 KiB-class state
-// block of a unit, released as soon as the consumers hold it in registers)
-// and record slots (ring records, query, decays, per-unit metadata and
-// scratch, released when the unit is done).  Small record slots are cheap, so
-// there are more of them, and the checkpoint slots turn over at the speed of
-// the memory system rather than of the arithmetic.
-struct M2Rec {
-  uint32_t k, v, q, a, meta, scr, bytes;
-};
-
-__host__ __device__ inline M2Rec m2_rec(int DV, int DK, int rec_es, int L) {
-  M2Rec s;
-  uint32_t o = 0;
-  s.k = o;    o = align128(o + L * DK * rec_es);   // records 0..p, current token at p
-  s.v = o;    o = align128(o + L * DV * rec_es);
-  s.q = o;    o = align128(o + DK * rec_es);
-  s.a = o;    o = align128(o + L * 4);             // decays of records 0..p
-  s.meta = o; o = align128(o + 16);                // slot, p, flush, status
-  s.scr = o;  o = align128(o + (2 * L + DV + 4) * 4);  // w_j, k_j.q, row dots, gamma
-  s.bytes = o;
-  return s;
-}
-
-// barriers full/rec_empty[nsr], ck_empty[nsc] and the abort flag
-__host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(8 * (2 * nsr + nsc) + 16); }
-
-
-// LMAX bounds the buffer length at compile time (L <= LMAX): loops over a
-// window's records unroll to a fixed count with predicated bodies.
-// TL is the read-copy type of a two-precision checkpoint (TL == TC: one copy).
-// GRP: group-shared keys and queries (k, q [B, G, d_k], ring_k [slots, G, L,
-// d_k]); the window's k_j . q_t were computed once per group by
-// mamba2_group_kq_kernel into a.kq, and non-flush units read those instead of
-// key records.
-// CPR: 16-byte checkpoint chunks a consumer lane holds per state row; its
-// chunks are cv, cv + G, cv + 2G, ... so that a warp's loads of one chunk
-// index cover whole 128-byte lines of the row.
-template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP, int CPR>
-__global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
-  using V = CkVec<TC>;
-  constexpr bool TWO = !std::is_same<TC, TL>::value;
-  constexpr int E = V::E;
-  constexpr int NCH = DK / E;        // 16-byte chunks per state row
-  constexpr int G = NCH / CPR;       // lanes per state row
-  constexpr int NC = NCW * 32;       // consumer threads per group
-  constexpr int RPP = NC / G;        // state rows per pass of a group
-  constexpr int VPT = DV / RPP;      // state rows per consumer thread
-  constexpr int RDT = Rec<RT>::kDtype;
-  constexpr int RES = (int)sizeof(RT);
-  constexpr int PROD = NGRP * NCW;   // warp index of the producer
-  constexpr uint32_t CKB = DV * DK * (uint32_t)sizeof(TC);
-  constexpr uint32_t CKB_LP = DV * DK * (uint32_t)sizeof(TL);
-  static_assert(!TWO || (E == 4 && sizeof(TL) == 2), "read copy: 16-bit elements under an fp32 checkpoint");
-  static_assert(G <= 32 && 32 % G == 0 && NCH % CPR == 0, "a state row must fit in one warp");
-  static_assert(NC % G == 0 && DV % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
-  static_assert(DK % 8 == 0 && DV % 8 == 0, "head dims must be multiples of 8");
-
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // per record slot: all bytes of a unit landed
-  uint64_t *rec_empty = full + nsr;                     // per record slot: the unit is done
-  uint64_t *ck_empty = rec_empty + nsr;                 // per checkpoint slot: consumers hold it in registers
-  int *s_abort = reinterpret_cast<int *>(ck_empty + nsc);
-  const int L = a.L;
-  const M2Rec lay = m2_rec(DV, DK, RES, L);
-  unsigned char *ck_slots = smem + m2_head(nsr, nsc);
-  unsigned char *rec_slots = ck_slots + (size_t)nsc * CKB;
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_units = a.B * a.H;
-  const int stride = gridDim.x;
-
-  if (tid == 0) {
-    for (int s = 0; s < nsr; ++s) {
-      mbar_init(&full[s], 33);       // 32 producer-lane cp.async arrivals + lane 0 (+ bulk bytes)
-      mbar_init(&rec_empty[s], NC);  // every thread of the consuming group
-    }
-    for (int c = 0; c < nsc; ++c) mbar_init(&ck_empty[c], NC);
-    *s_abort = 0;
-    mbar_init_fence();
-  }
-  __syncthreads();
-
-  if (warp == PROD) {
-    // ----------------------------------------------------------------- producer
-    const uint64_t pol_stream = policy_evict_first();
-    int it = 0;
-    auto fetch = [&](int ub, int &sl, int &wp, int &fl) {
-      const int u = ub + lane * stride;
-      if (u < n_units) {
-        const int b = u / a.H;
-        sl = __ldg(a.slot_idx + b);
-        wp = __ldg(a.write_pos + b);
-        fl = __ldg(a.is_flush + b);
-      } else {
-        sl = -1; wp = 0; fl = 0;
-      }
-    };
-    int c_sl, c_wp, c_fl;
-    int ps = 0, pc = 0;         // record and checkpoint slot of unit `it`
-    uint32_t phs = 0, phc = 0;  // parity of it / nsr and it / nsc
-    fetch(blockIdx.x, c_sl, c_wp, c_fl);
-    bool ok = true;
-    for (int ub = blockIdx.x; ok && ub < n_units; ub += 32 * stride) {
-      int n_sl, n_wp, n_fl;
-      fetch(ub + 32 * stride, n_sl, n_wp, n_fl);  // next batch, in flight meanwhile
-      for (int j = 0; j < 32; ++j) {
-        const int u = ub + j * stride;
-        if (u >= n_units) break;
-        const int slot = __shfl_sync(0xffffffffu, c_sl, j);
-        const int p = __shfl_sync(0xffffffffu, c_wp, j);
-        const int fl = __shfl_sync(0xffffffffu, c_fl, j);
-        const int s = ps, c = pc;
-        if (it >= nsr || it >= nsc) {
-          int w = 1;
-          if (lane == 0) {
-            if (it >= nsr) w = mbar_wait(&rec_empty[s], phs ^ 1u) ? 1 : 0;
-            if (w && it >= nsc) w = mbar_wait(&ck_empty[c], phc ^ 1u) ? 1 : 0;
-          }
-          w = __shfl_sync(0xffffffffu, w, 0);
-          if (!w || *(volatile int *)s_abort) {
-            if (lane == 0) *(volatile int *)s_abort = 1;
-            ok = false;
-            break;
-          }
-        }
-        __syncwarp();
-        const int b = u / a.H, h = u - (u / a.H) * a.H;
-        const int status = slot < 0 ? kStatusPad
-                           : slot >= a.num_slots ? kStatusBadSlot
-                           : (p < 0 || p >= L) ? kStatusBadPos
-                           : kStatusOk;
-        unsigned char *st = rec_slots + (size_t)s * lay.bytes;
-        int *meta = reinterpret_cast<int *>(st + lay.meta);
-        if (status == kStatusOk) {
-          // The checkpoint, the only large operand, is one bulk copy from lane
-          // 0.  The small pieces -- ring records, this token's k, v, q and the
-          // decays -- go as 16- and 4-byte cp.async over the 32 lanes: a bulk
-          // copy carries a fixed cost of ~0.2 us that five small copies per
-          // unit would pay five times.
-          const size_t unit = (size_t)slot * a.H + h;
-          if (lane == 0) {
-            meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
-            // a two-precision non-flush row reads only the read copy
-            const bool lp = TWO && !fl;
-            const uint32_t nb = lp ? CKB_LP : CKB;
-            const void *src = lp ? static_cast<const void *>(static_cast<const TL *>(a.ckpt_lp) + unit * (DV * DK))
-                                 : static_cast<const void *>(static_cast<const TC *>(a.ckpt) + unit * (DV * DK));
-            mbar_expect_tx(&full[s], nb);
-            bulk_load(ck_slots + (size_t)c * CKB, src, nb, &full[s], pol_stream);
-          }
-          constexpr uint32_t kb = DK * RES, vb = DV * RES;
-          constexpr int KC = kb / 16, VC = vb / 16;  // 16-byte chunks per k / v record
-          // key and query of the unit: its own (per-head layout) or its group's
-          const int kh = GRP ? h / (a.H / a.n_groups) : h;
-          const size_t kunit = GRP ? (size_t)slot * a.n_groups + kh : unit;
-          const unsigned char *rk = static_cast<const unsigned char *>(a.ring_k) + kunit * L * kb;
-          const unsigned char *rv = static_cast<const unsigned char *>(a.ring_v) + unit * L * vb;
-          const unsigned char *kin =
-              static_cast<const unsigned char *>(a.k) + ((size_t)b * a.sk + (size_t)kh * DK) * RES;
-          const unsigned char *vin =
-              static_cast<const unsigned char *>(a.v) + ((size_t)b * a.sv + (size_t)h * DV) * RES;
-          const unsigned char *qin =
-              static_cast<const unsigned char *>(a.q) + ((size_t)b * a.sq + (size_t)kh * DK) * RES;
-          if (!GRP || fl) {
-#pragma unroll
-            for (int i = 0; i < (LMAX * KC + 31) / 32; ++i) {
-              const int cc = lane + 32 * i;
-              if (cc < (p + 1) * KC)
-                cp_async16(st + lay.k + cc * 16, (cc < p * KC ? rk + cc * 16 : kin + (cc - p * KC) * 16));
-            }
-          } else {
-            // the group's k_j . q_t of the window, into the dots scratch of the slot
-            float *ss = reinterpret_cast<float *>(st + lay.scr) + L;
-            const float *kq = a.kq + ((size_t)b * a.n_groups + kh) * L;
-#pragma unroll
-            for (int i = 0; i < (LMAX + 31) / 32; ++i) {
-              const int jj = lane + 32 * i;
-              if (jj <= p) cp_async4(ss + jj, kq + jj);
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < (LMAX * VC + 31) / 32; ++i) {
-            const int cc = lane + 32 * i;
-            if (cc < (p + 1) * VC)
-              cp_async16(st + lay.v + cc * 16, (cc < p * VC ? rv + cc * 16 : vin + (cc - p * VC) * 16));
-          }
-          for (int cc = lane; cc < KC; cc += 32) cp_async16(st + lay.q + cc * 16, qin + cc * 16);
-          float *sa = reinterpret_cast<float *>(st + lay.a);
-#pragma unroll
-          for (int i = 0; i < (LMAX + 31) / 32; ++i) {
-            const int jj = lane + 32 * i;
-            if (jj < p) cp_async4(sa + jj, a.ring_a + unit * L + jj);
-          }
-          if (lane == 31) cp_async4(sa + p, a.alpha + (size_t)b * a.H + h);
-        } else if (lane == 0) {
-          meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
-        }
-        if (lane == 0) mbar_arrive(&full[s]);  // releases the meta words
-        cp_async_arrive(&full[s]);
-        ++it;
-        if (++ps == nsr) {
-          ps = 0;
-          phs ^= 1u;
-        }
-        if (++pc == nsc) {
-          pc = 0;
-          phc ^= 1u;
-        }
-      }
-      c_sl = n_sl; c_wp = n_wp; c_fl = n_fl;
-    }
-    // drain: every copy this warp issued has landed before the CTA may exit
-    if (lane == 0) {
-      for (int k = it > nsr ? it - nsr : 0; k < it; ++k) mbar_wait(&full[k % nsr], (uint32_t)(k / nsr) & 1u);
-    }
-    __syncwarp();
-    return;
-  }
-
-  // ------------------------------------------------------------------ consumers
-  // group g takes the CTA's units g, g + NGRP, ...; each group has its own
-  // named barrier, so the groups run independently of each other
-  const int grp = warp / NCW;
-  const int lw = warp - grp * NCW;  // warp within the group
-  const int ctid = tid - grp * NC;  // 0 .. NC-1
-  const int row0 = ctid / G, cv = ctid - (ctid / G) * G;
-  auto gsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(NC) : "memory"); };
-  // row and head of the unit, stepped instead of divided
-  const int ustep = NGRP * stride;
-  const int step_b = ustep / a.H, step_h = ustep - (ustep / a.H) * a.H;
-  int b = (int)(blockIdx.x + grp * stride) / a.H;
-  int h = (int)(blockIdx.x + grp * stride) - b * a.H;
-  // slot indices and the full-barrier phase, stepped instead of divided
-  int s = grp % nsr, c = grp % nsc;
-  uint32_t ph = (uint32_t)(grp / nsr) & 1u;
-  for (int it = grp; ; it += NGRP, h += step_h, b += step_b) {
-    if (h >= a.H) {
-      h -= a.H;
-      ++b;
-    }
-    if (it != grp) {
-      s += NGRP;
-      if (s >= nsr) {
-        s -= nsr;
-        ph ^= 1u;
-      }
-      c += NGRP;
-      if (c >= nsc) c -= nsc;
-    }
-    const int u = blockIdx.x + it * stride;
-    if (u >= n_units) break;
-    if (lane == 0 && !mbar_wait(&full[s], ph)) *(volatile int *)s_abort = 1;
-    gsync();
-    if (*(volatile int *)s_abort) break;
-
-    const unsigned char *st = rec_slots + (size_t)s * lay.bytes;
-    const int4 m = *reinterpret_cast<const int4 *>(st + lay.meta);
-    const int slot = m.x, p = m.y, flush = m.z, status = m.w;
-    float *orow = a.out + (size_t)b * a.so + (size_t)h * DV;
-    if (status != kStatusOk) {
-      for (int i = ctid; i < DV; i += NC) orow[i] = 0.f;
-      if (ctid == 0 && status != kStatusPad) report(a.dev_err, status == kStatusBadSlot ? 1 : 2);
-      mbar_arrive(&ck_empty[c]);
-      mbar_arrive(&rec_empty[s]);
-      continue;
-    }
-    const size_t unit = (size_t)slot * a.H + h;
-    const float *sa = reinterpret_cast<const float *>(st + lay.a);
-    float *scr = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + lay.scr);
-    float *sW = scr, *sS = scr + L, *sC = scr + 2 * L, *sGam = scr + 2 * L + DV;
-    const unsigned char *sk = st + lay.k, *sv = st + lay.v;
-    const unsigned char *ck_slot = ck_slots + (size_t)c * CKB;
-
-    // window weights w_j (suffix products of the decays) and gamma
-    auto weights = [&]() {
-      if (lw == 0) {
-        float x0 = lane <= p ? sa[lane] : 1.f;
-        float x1 = lane + 32 <= p ? sa[lane + 32] : 1.f;
-        suffix_scan64(x0, x1, lane, [](float x, float y) { return x * y; });
-        const float n0 = __shfl_down_sync(0xffffffffu, x0, 1);
-        const float n1 = __shfl_down_sync(0xffffffffu, x1, 1);
-        const float hi0 = __shfl_sync(0xffffffffu, x1, 0);
-        if (lane <= p) sW[lane] = lane == 31 ? hi0 : n0;
-        if (lane + 32 <= p) sW[lane + 32] = lane == 31 ? 1.f : n1;
-        if (lane == 0) sGam[0] = x0;
-      }
-    };
-
-    float part[VPT];
-    if (!flush) {
-      // take this thread's share of the checkpoint (the read copy of a
-      // two-precision checkpoint) into registers and hand the slot straight
-      // back to the producer
-      using Raw = typename std::conditional<TWO, uint2, uint4>::type;
-      Raw raw[VPT][CPR];
-#pragma unroll
-      for (int r = 0; r < VPT; ++r)
-#pragma unroll
-        for (int i = 0; i < CPR; ++i)
-          raw[r][i] = reinterpret_cast<const Raw *>(ck_slot)[(row0 + r * RPP) * NCH + cv + G * i];
-      mbar_arrive(&ck_empty[c]);
-      weights();
-      float qv[CPR][E];
-#pragma unroll
-      for (int i = 0; i < CPR; ++i) lds_cols<E>(st + lay.q, (cv + G * i) * E, RDT, qv[i]);
-      // s_j = k_j . q: a warp takes records four at a time; each lane holds
-      // its 4-column chunk of q and accumulates four partial dots, and one
-      // transposed reduction finishes the chunk (group-shared keys: the
-      // producer brought the group's dots instead)
-      if constexpr (!GRP) {
-        constexpr int QPL = (DK + 127) / 128;  // 4-column chunks of q per lane
-        float qq[QPL][4];
-#pragma unroll
-        for (int i = 0; i < QPL; ++i) {
-          if (lane * 4 + i * 128 < DK) {
-            lds_cols<4>(st + lay.q, lane * 4 + i * 128, RDT, qq[i]);
-          } else {
-            qq[i][0] = qq[i][1] = qq[i][2] = qq[i][3] = 0.f;
-          }
-        }
-#pragma unroll
-        for (int ci = 0; ci < (LMAX / 4 + NCW - 1) / NCW; ++ci) {
-          const int ch = lw + ci * NCW;
-          if (ch * 4 > p) break;
-          float part4[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int j = ch * 4 + r;
-            float acc = 0.f;
-            if (j <= p) {
-#pragma unroll
-              for (int i = 0; i < QPL; ++i) {
-                const int cc = lane * 4 + i * 128;
-                if (cc < DK) {
-                  float kk[4];
-                  lds_cols<4>(sk, j * DK + cc, RDT, kk);
-                  acc = fmaf(kk[0], qq[i][0], fmaf(kk[1], qq[i][1], fmaf(kk[2], qq[i][2], fmaf(kk[3], qq[i][3], acc))));
-                }
-              }
-            }
-            part4[r] = acc;
-          }
-          group_reduce<4, 32>(part4, lane);
-          if (group_reduce_writer<4, 32>(lane)) {
-            const int j = ch * 4 + group_reduce_index<4, 32>(lane);
-            if (j <= p) sS[j] = part4[0];
-          }
-        }
-      }
-      // checkpoint GEMV partials from the stage
-#pragma unroll
-      for (int r = 0; r < VPT; ++r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < CPR; ++i) {
-          float f[E];
-          if constexpr (TWO) {
-            LpVec<TL>::unpack(raw[r][i], f);
-          } else {
-            V::unpack(raw[r][i], f);
-          }
-#pragma unroll
-          for (int e = 0; e < E; ++e) acc = fmaf(f[e], qv[i][e], acc);
-        }
-        part[r] = acc;
-      }
-      group_reduce<VPT, G>(part, lane);
-      if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
-      gsync();
-
-      // o = gamma c + sum_j w_j s_j v_j, by one warp: a lane covers 8 output
-      // rows (one 16-byte load of a v record) for every OG-th record, then
-      // lanes sharing rows add up; the other warps append the record
-      if (lw == 0) {
-        constexpr int RG = DV / 8;   // 8-row groups
-        constexpr int OG = 32 / RG;  // record groups
-        static_assert(DV % 8 == 0 && 32 % RG == 0 && OG >= 1, "bad output layout");
-        const int rg = lane % RG, og = lane / RG;
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-        for (int i = 0; i < (LMAX + OG - 1) / OG; ++i) {
-          const int j = og + i * OG;
-          if (j <= p) {
-            const float cj = sW[j] * sS[j];
-            float vv[8];
-            lds_cols<8>(sv, j * DV + rg * 8, RDT, vv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(cj, vv[e], acc[e]);
-          }
-        }
-#pragma unroll
-        for (int off = RG; off < 32; off <<= 1) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
-        }
-        if (og == 0) {
-          const float gam = sGam[0];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) orow[rg * 8 + e] = fmaf(gam, sC[rg * 8 + e], acc[e]);
-        }
-      }
-      // append the current record (k, v verbatim, alpha) at ring slot p; a
-      // group-shared key was appended by the group's dot kernel
-      constexpr int KCH = GRP ? 0 : DK * RES / 16, VCH = DV * RES / 16;
-      constexpr int APP0 = NCW > 1 ? 32 : 0;  // warp 0 is busy with the output
-      for (int c = ctid - APP0; c >= 0 && c < KCH + VCH; c += NC - APP0) {
-        if (c < KCH) {
-          const uint4 x = reinterpret_cast<const uint4 *>(sk + (size_t)p * DK * RES)[c];
-          reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.ring_k) + (unit * L + p) * DK * RES)[c] = x;
-        } else {
-          const uint4 x = reinterpret_cast<const uint4 *>(sv + (size_t)p * DV * RES)[c - KCH];
-          reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.ring_v) + (unit * L + p) * DV * RES)[c - KCH] = x;
-        }
-      }
-      if (ctid == NC - 1) a.ring_a[unit * L + p] = sa[p];
-    } else {
-      uint4 raw[VPT][CPR];
-#pragma unroll
-      for (int r = 0; r < VPT; ++r)
-#pragma unroll
-        for (int i = 0; i < CPR; ++i)
-          raw[r][i] = reinterpret_cast<const uint4 *>(ck_slot)[(row0 + r * RPP) * NCH + cv + G * i];
-      mbar_arrive(&ck_empty[c]);
-      weights();
-      float qv[CPR][E];
-#pragma unroll
-      for (int i = 0; i < CPR; ++i) lds_cols<E>(st + lay.q, (cv + G * i) * E, RDT, qv[i]);
-      gsync();  // weights ready
-      const float gam = sGam[0];
-      TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK);
-      float f[VPT][CPR][E];
-#pragma unroll
-      for (int r = 0; r < VPT; ++r)
-#pragma unroll
-        for (int i = 0; i < CPR; ++i) {
-          V::unpack(raw[r][i], f[r][i]);
-#pragma unroll
-          for (int e = 0; e < E; ++e) f[r][i][e] *= gam;
-        }
-#pragma unroll 4
-      for (int j = 0; j <= p; ++j) {
-        float kk[CPR][E];
-#pragma unroll
-        for (int i = 0; i < CPR; ++i) lds_cols<E>(sk, j * DK + (cv + G * i) * E, RDT, kk[i]);
-        const float wj = sW[j];
-#pragma unroll
-        for (int r = 0; r < VPT; ++r) {
-          const float vv = wj * lds_elem(sv, j * DV + row0 + r * RPP, RDT);
-#pragma unroll
-          for (int i = 0; i < CPR; ++i)
-#pragma unroll
-            for (int e = 0; e < E; ++e) f[r][i][e] = fmaf(vv, kk[i][e], f[r][i][e]);
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < VPT; ++r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < CPR; ++i) {
-#pragma unroll
-          for (int e = 0; e < E; ++e) acc = fmaf(f[r][i][e], qv[i][e], acc);
-          const size_t off = (size_t)(row0 + r * RPP) * DK + (cv + G * i) * E;
-          st_vec(ckg + off, V::pack(f[r][i]));
-          if constexpr (TWO) {
-            // the read copy: an independent rounding of the same fp32 matrix
-            TL *lpg = static_cast<TL *>(a.ckpt_lp) + unit * (DV * DK);
-            float g4[4] = {f[r][i][0], f[r][i][1], f[r][i][2], f[r][i][3]};
-            st_vec2(lpg + off, LpVec<TL>::pack(g4));
-          }
-        }
-        part[r] = acc;
-      }
-      group_reduce<VPT, G>(part, lane);
-      if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
-      gsync();
-      for (int i = ctid; i < DV; i += NC) orow[i] = sC[i];
-    }
-    mbar_arrive(&rec_empty[s]);
-  }
-  if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
-}
-
-// Group-shared keys ([Ghana] §Output without a state: the released kernel
-// reads precomputed k_j . q from a small kernel that runs once per group):
-// one warp per (row, group) computes s_j = k_j . q_t for the window's records
-// j < p and the current key (j = p) into a.kq[b, g, :], and on a non-flush
-// row appends the current key to the group's ring at slot p.  Rows whose
-// slot or cursor is out of range are left to the decode kernel to report.
-template <int DK, typename RT>
-__global__ void __launch_bounds__(256) mamba2_group_kq_kernel(const KArgs a) {
-  constexpr int RES = (int)sizeof(RT);
-  constexpr int RDT = Rec<RT>::kDtype;
-  constexpr int KPL = (DK + 127) / 128;  // 4-column chunks per lane
-  const int lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (pair >= a.B * a.n_groups) return;
-  const int b = pair / a.n_groups, g = pair - (pair / a.n_groups) * a.n_groups;
-  const int slot = __ldg(a.slot_idx + b), p = __ldg(a.write_pos + b), L = a.L;
-  if (slot < 0 || slot >= a.num_slots || p < 0 || p >= L) return;
-  const bool flush = __ldg(a.is_flush + b) != 0;
-  const size_t kunit = (size_t)slot * a.n_groups + g;
-  const unsigned char *rk = static_cast<const unsigned char *>(a.ring_k) + kunit * L * DK * RES;
-  const unsigned char *kin = static_cast<const unsigned char *>(a.k) + ((size_t)b * a.sk + (size_t)g * DK) * RES;
-  const unsigned char *qin = static_cast<const unsigned char *>(a.q) + ((size_t)b * a.sq + (size_t)g * DK) * RES;
-  float qq[KPL][4];
-#pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    const int col = lane * 4 + i * 128;
-    if (col < DK) {
-      lds_cols<4>(qin, col, RDT, qq[i]);
-    } else {
-      qq[i][0] = qq[i][1] = qq[i][2] = qq[i][3] = 0.f;
-    }
-  }
-  float *kq = a.kq + (size_t)pair * L;
-  for (int j0 = 0; j0 <= p; j0 += 4) {
-    float part[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int j = j0 + r;
-      float acc = 0.f;
-      if (j <= p) {
-        const unsigned char *rec = j < p ? rk + (size_t)j * DK * RES : kin;
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) {
-          const int col = lane * 4 + i * 128;
-          if (col < DK) {
-            float kk[4];
-            lds_cols<4>(rec, col, RDT, kk);
-            acc = fmaf(kk[0], qq[i][0], fmaf(kk[1], qq[i][1], fmaf(kk[2], qq[i][2], fmaf(kk[3], qq[i][3], acc))));
-          }
-        }
-      }
-      part[r] = acc;
-    }
-    group_reduce<4, 32>(part, lane);
-    if (group_reduce_writer<4, 32>(lane)) {
-      const int j = j0 + group_reduce_index<4, 32>(lane);
-      if (j <= p) kq[j] = part[0];
-    }
-  }
-  if (!flush) {
-    constexpr int KC = DK * RES / 16;
-    for (int c = lane; c < KC; c += 32)
-      reinterpret_cast<uint4 *>(const_cast<unsigned char *>(rk) + (size_t)p * DK * RES)[c] =
-          reinterpret_cast<const uint4 *>(kin)[c];
-  }
-}
-
-template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP = false,
-          int CPR = 1>
-static cudaError_t launch_mamba2_l(const KArgs &a, cudaStream_t s) {
-  if (GRP) {
-    mamba2_group_kq_kernel<DK, RT><<<(unsigned)(((size_t)a.B * a.n_groups + 7) / 8), 256, 0, s>>>(a);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  auto kern = mamba2_replay_kernel<DV, DK, TC, TL, RT, NCW, NGRP, LMAX, GRP, CPR>;
-  constexpr int threads = NGRP * NCW * 32 + 32;
-  const size_t ckb = (size_t)DV * DK * sizeof(TC);
-  const size_t rb = m2_rec(DV, DK, (int)sizeof(RT), a.L).bytes;
-  RingPlan plan;
-  cudaError_t e = plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, m2_head, a.B * a.H, &plan);
-  if (e != cudaSuccess) return e;
-  kern<<<plan.grid, threads, plan.smem, s>>>(a, plan.nsr, plan.nsc);
-  return cudaGetLastError();
-}
-
-// the common short windows get a kernel unrolled for L <= 16
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, typename TL = TC, int CPR = 1>
-static cudaError_t launch_mamba2(const KArgs &a, cudaStream_t s) {
-  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 16, false, CPR>(a, s)
-                   : launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, RS_MAX_L, false, CPR>(a, s);
-}
-
-// group-shared keys: the group dot kernel, then the decode
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, int CPR = 1>
-static cudaError_t launch_mamba2_grp(const KArgs &a, cudaStream_t s) {
-  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, 16, true, CPR>(a, s)
-                   : launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, RS_MAX_L, true, CPR>(a, s);
-}
-
-template <typename RT>
-static LaunchFn find_mamba2_t(int d_v, int d_k, int ckpt_dtype, int lp_dtype) {
-  if (ckpt_dtype == kF32 && lp_dtype == kF16) {
-    if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1, __half>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __half, 4>;
-    if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1, __half>;
-  } else if (ckpt_dtype == kF32 && lp_dtype == kBF16) {
-    if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1, __nv_bfloat16>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __nv_bfloat16, 4>;
-    if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1, __nv_bfloat16>;
-  } else if (lp_dtype >= 0) {
-    return nullptr;
-  } else if (ckpt_dtype == kF32) {
+static LaunchFn find_mamba2_bf16_inputs(int d_v, int d_k, int ckpt_dtype) {
+  using RT = __nv_bfloat16;
+  if (ckpt_dtype == kF32) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, float, 2>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, float, 2, true>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1>;
   } else if (ckpt_dtype == kF16) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, __half, RT, 2, 1>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, __half, RT, 4, 2>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, __half, RT, 4, 2, __half, 1, true>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, __half, RT, 8, 1>;
   }
   return nullptr;
 }
 
-template <typename RT>
-static LaunchFn find_mamba2_grp_t(int d_v, int d_k, int ckpt_dtype) {
-  if (ckpt_dtype == kF32) {
-    if (d_v == 16 && d_k == 32) return launch_mamba2_grp<16, 32, float, RT, 4, 1>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2_grp<64, 128, float, RT, 4, 2>;
-  } else if (ckpt_dtype == kF16) {
-    if (d_v == 64 && d_k == 128) return launch_mamba2_grp<64, 128, __half, RT, 8, 1>;
-  }
-  return nullptr;
-}
-
 LaunchFn find_mamba2(int d_v, int d_k, int ckpt_dtype, int in_dtype, int lp_dtype, bool grouped) {
-  if (grouped) {
-    if (lp_dtype >= 0) return nullptr;
-    return in_dtype == kF32 ? find_mamba2_grp_t<float>(d_v, d_k, ckpt_dtype)
-                            : find_mamba2_grp_t<__nv_bfloat16>(d_v, d_k, ckpt_dtype);
-  }
-  return in_dtype == kF32 ? find_mamba2_t<float>(d_v, d_k, ckpt_dtype, lp_dtype)
-                          : find_mamba2_t<__nv_bfloat16>(d_v, d_k, ckpt_dtype, lp_dtype);
+  if (grouped) return lp_dtype >= 0 ? nullptr : find_mamba2_grouped(d_v, d_k, ckpt_dtype, in_dtype);
+  if (lp_dtype >= 0) return ckpt_dtype == kF32 ? find_mamba2_read_copy(d_v, d_k, lp_dtype, in_dtype) : nullptr;
+  return in_dtype == kF32 ? find_mamba2_f32_inputs(d_v, d_k, ckpt_dtype) : find_mamba2_bf16_inputs(d_v, d_k, ckpt_dtype);
 }
 
 }  // namespace rs

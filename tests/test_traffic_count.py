@@ -101,3 +101,17 @@ def test_grouped_records_match_the_printed_record():
     one = traffic.step_bytes(write_pos=np.array([1]), **kw)
     zero = traffic.step_bytes(write_pos=np.array([0]), **kw)
     assert one - zero == model.grouped_record_bytes(H, d_v, G, d_k) == 18944
+
+
+def test_spec_bytes_by_hand():
+    """Speculative verification: per live row and head the checkpoint once,
+    the committed records, T drafts in (v, k, q bf16 + decay), T fp32
+    outputs and T records out; a flush row also writes the checkpoint."""
+    H, d_v, d_k, T = 2, 64, 128, 4
+    got = traffic.spec_bytes(H=H, d_v=d_v, d_k=d_k, T=T, ckpt_dtype="f32", in_dtype="bf16",
+                             slot_idx=[0, 1, -1], committed=[3, 14, 5], is_flush=[0, 1, 0])
+    state, rec = 64 * 128 * 4, 2 * (64 + 128) + 4
+    draft_in, out = 2 * (64 + 2 * 128) + 4, 4 * 64
+    per_row = H * (state + T * (draft_in + out + rec)) + 9
+    want = 2 * per_row + (3 + 14) * H * rec + 1 * H * state + (4 + T * H * 4 * d_v)
+    assert got == want
