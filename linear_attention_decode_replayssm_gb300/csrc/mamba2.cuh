@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   constexpr uint32_t CKB = DV * DK * (uint32_t)sizeof(TC);
   constexpr uint32_t CKB_LP = DV * DK * (uint32_t)sizeof(TL);
   static_assert(!TWO || (E == 4 && sizeof(TL) == 2), "read copy: 16-bit elements under an fp32 checkpoint");
+  // flush fold on the tensor cores: fp32 checkpoint, one warp per 16 state rows
+  constexpr bool MMAF = std::is_same<TC, float>::value && DV == 16 * NCW && DK % 16 == 0;
   static_assert(G <= 32 && 32 % G == 0 && NCH % CPR == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && DV % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
   static_assert(DK % 8 == 0 && DV % 8 == 0, "head dims must be multiples of 8");
@@ -459,6 +461,103 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
         }
       }
       if (ctid == NC - 1) a.ring_a[unit * L + p] = sa[p];
+    } else if constexpr (MMAF) {
+      // Flush on the tensor cores.  Warp lw holds state rows rA = 16 lw + g
+      // and rB = rA + 8 in accumulator layout: four consecutive columns per
+      // 16-column block (columns 4t, 4t+1 form one 8-column tile, 4t+2, 4t+3
+      // the other).  The window folds in as a rank-(p+1) product, m16n8k8
+      // tf32 with each weighted value split into two tf32 terms (the 16-bit
+      // keys are exact), so S_new keeps fp32 accuracy.
+      constexpr int NB = DK / 16;
+      const int g8 = lane >> 2, t4 = lane & 3;
+      const int rA = 16 * lw + g8, rB = rA + 8;
+      float4 xa[NB], xb[NB];
+#pragma unroll
+      for (int bk = 0; bk < NB; ++bk) {
+        xa[bk] = *reinterpret_cast<const float4 *>(ck_slot + ((size_t)rA * DK + 16 * bk + 4 * t4) * 4);
+        xb[bk] = *reinterpret_cast<const float4 *>(ck_slot + ((size_t)rB * DK + 16 * bk + 4 * t4) * 4);
+      }
+      mbar_arrive(&ck_empty[c]);
+      weights();
+      gsync();  // weights ready
+      const float gam = sGam[0];
+#pragma unroll
+      for (int bk = 0; bk < NB; ++bk) {
+        xa[bk].x *= gam; xa[bk].y *= gam; xa[bk].z *= gam; xa[bk].w *= gam;
+        xb[bk].x *= gam; xb[bk].y *= gam; xb[bk].z *= gam; xb[bk].w *= gam;
+      }
+      for (int j0 = 0; j0 <= p; j0 += 8) {
+        // records j0 + t and j0 + t + 4 of the window; past p they weigh 0
+        // (and read record 0, so no stale ring slot enters the product)
+        const int ja = j0 + t4, jb = ja + 4;
+        const int ra = ja <= p ? ja : 0, rb = jb <= p ? jb : 0;
+        const float wa = ja <= p ? sW[ja] : 0.f, wb = jb <= p ? sW[jb] : 0.f;
+        uint32_t ah[4], al[4];
+        split_tf32(wa * lds_elem(sv, ra * DV + rA, RDT), ah[0], al[0]);
+        split_tf32(wa * lds_elem(sv, ra * DV + rB, RDT), ah[1], al[1]);
+        split_tf32(wb * lds_elem(sv, rb * DV + rA, RDT), ah[2], al[2]);
+        split_tf32(wb * lds_elem(sv, rb * DV + rB, RDT), ah[3], al[3]);
+#pragma unroll
+        for (int bk = 0; bk < NB; ++bk) {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int col = 16 * bk + 4 * (g8 >> 1) + (g8 & 1) + 2 * hf;  // column of tile index n = g
+            float d[4] = {hf ? xa[bk].z : xa[bk].x, hf ? xa[bk].w : xa[bk].y, hf ? xb[bk].z : xb[bk].x,
+                          hf ? xb[bk].w : xb[bk].y};
+            if constexpr (sizeof(RT) == 2) {
+              const uint32_t bb[2] = {__float_as_uint(lds_elem(sk, ra * DK + col, RDT)),
+                                      __float_as_uint(lds_elem(sk, rb * DK + col, RDT))};
+              mma_tf32(d, ah, bb);
+              mma_tf32(d, al, bb);
+            } else {
+              uint32_t bh[2], bl[2];
+              split_tf32(lds_elem(sk, ra * DK + col, RDT), bh[0], bl[0]);
+              split_tf32(lds_elem(sk, rb * DK + col, RDT), bh[1], bl[1]);
+              mma_tf32(d, ah, bh);
+              mma_tf32(d, al, bh);
+              mma_tf32(d, ah, bl);
+            }
+            if (hf) {
+              xa[bk].z = d[0]; xa[bk].w = d[1]; xb[bk].z = d[2]; xb[bk].w = d[3];
+            } else {
+              xa[bk].x = d[0]; xa[bk].y = d[1]; xb[bk].x = d[2]; xb[bk].y = d[3];
+            }
+          }
+        }
+      }
+      // store S_new (and its read copy), and o = S_new q from the same registers
+      TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK);
+      float oA = 0.f, oB = 0.f;
+#pragma unroll
+      for (int bk = 0; bk < NB; ++bk) {
+        const size_t offA = (size_t)rA * DK + 16 * bk + 4 * t4, offB = (size_t)rB * DK + 16 * bk + 4 * t4;
+        const float fa[4] = {xa[bk].x, xa[bk].y, xa[bk].z, xa[bk].w};
+        const float fb[4] = {xb[bk].x, xb[bk].y, xb[bk].z, xb[bk].w};
+        st_vec(ckg + offA, V::pack(fa));
+        st_vec(ckg + offB, V::pack(fb));
+        if constexpr (TWO) {
+          TL *lpg = static_cast<TL *>(a.ckpt_lp) + unit * (DV * DK);
+          st_vec2(lpg + offA, LpVec<TL>::pack(fa));
+          st_vec2(lpg + offB, LpVec<TL>::pack(fb));
+        }
+        float q4[4];
+        lds_cols<4>(st + lay.q, 16 * bk + 4 * t4, RDT, q4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          oA = fmaf(fa[e], q4[e], oA);
+          oB = fmaf(fb[e], q4[e], oB);
+        }
+      }
+      oA += __shfl_xor_sync(0xffffffffu, oA, 1);
+      oB += __shfl_xor_sync(0xffffffffu, oB, 1);
+      oA += __shfl_xor_sync(0xffffffffu, oA, 2);
+      oB += __shfl_xor_sync(0xffffffffu, oB, 2);
+      if (t4 == 0) {
+        sC[rA] = oA;
+        sC[rB] = oB;
+      }
+      gsync();
+      for (int i = ctid; i < DV; i += NC) orow[i] = sC[i];
     } else {
       uint4 raw[VPT][CPR];
 #pragma unroll
