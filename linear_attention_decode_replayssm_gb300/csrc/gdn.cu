@@ -306,46 +306,35 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
           for (int e = 0; e < 4; ++e) kt4[i][e] = q4[i][e] = 0.f;
         }
       }
+      // one record per warp, so the records of a window are done in
+      // parallel: the two dots of a record finish in one 2-value reduction
+      for (int j = lw; j <= p; j += NCW) {
+        float part2[2] = {0.f, 0.f};  // k_j . k_t, k_j . q_t
 #pragma unroll
-      for (int ci = 0; ci < (LMAX / 4 + NCW - 1) / NCW; ++ci) {
-        const int ch = lw + ci * NCW;
-        if (ch * 4 > p) break;
-        float part8[8];  // [0..3]: k_j . k_t, [4..7]: k_j . q_t
+        for (int i = 0; i < QPL; ++i) {
+          const int cc = lane * 4 + i * 128;
+          if (cc < DK) {
+            float kk[4];
+            if (j < p) {
+              lds_cols<4>(sk, j * DK + cc, rdt, kk);
+            } else {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int j = ch * 4 + r;
-          float dk = 0.f, dq = 0.f;
-          if (j <= p) {
+              for (int e = 0; e < 4; ++e) kk[e] = kt4[i][e];
+            }
 #pragma unroll
-            for (int i = 0; i < QPL; ++i) {
-              const int cc = lane * 4 + i * 128;
-              if (cc < DK) {
-                float kk[4];
-                if (j < p) {
-                  lds_cols<4>(sk, j * DK + cc, rdt, kk);
-                } else {
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) kk[e] = kt4[i][e];
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  dk = fmaf(kk[e], kt4[i][e], dk);
-                  dq = fmaf(kk[e], q4[i][e], dq);
-                }
-              }
+            for (int e = 0; e < 4; ++e) {
+              part2[0] = fmaf(kk[e], kt4[i][e], part2[0]);
+              part2[1] = fmaf(kk[e], q4[i][e], part2[1]);
             }
           }
-          part8[r] = dk;
-          part8[4 + r] = dq;
         }
-        group_reduce<8, 32>(part8, lane);
-        if (group_reduce_writer<8, 32>(lane)) {
-          const int vi = group_reduce_index<8, 32>(lane);
-          const int j = ch * 4 + (vi & 3);
+        group_reduce<2, 32>(part2, lane);
+        if (group_reduce_writer<2, 32>(lane)) {
+          const int vi = group_reduce_index<2, 32>(lane);
           if (j < p) {
-            if (vi < 4) sDk[j] = part8[0]; else sDq[j] = part8[0];
-          } else if (j == p && vi >= 4) {
-            sScal[1] = part8[0];
+            if (vi == 0) sDk[j] = part2[0]; else sDq[j] = part2[0];
+          } else if (vi == 1) {
+            sScal[1] = part2[0];  // k_t . q_t
           }
         }
       }
