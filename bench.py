@@ -220,13 +220,29 @@ def _kernel_traffic(kernel, workload):
     return rec.get("dram_bytes_per_launch")
 
 
-def source_hash(kernel):
-    files = {"mamba2_replay": ["mamba2.cuh", "mamba2.cu"], "gdn_replay": ["gdn.cu"], "conventional": ["conventional.cu"]}[kernel]
+KERNEL_SOURCES = {"mamba2_replay": ["mamba2.cuh", "mamba2.cu"], "gdn_replay": ["gdn.cu"],
+                  "conventional": ["conventional.cu"]}
+
+
+def code_digest(texts):
+    """SHA-256 of CUDA sources with comments and blank space removed, so that
+    an edit to comments alone does not count as a kernel change."""
+    import re
+
     h = hashlib.sha256()
-    for name in files + ["common.cuh"]:
-        with open(os.path.join(ROOT, "linear_attention_decode_replayssm_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    for t in texts:
+        t = re.sub(r"/\*.*?\*/", "", t, flags=re.S)
+        t = re.sub(r"//[^\n]*", "", t)
+        h.update("\n".join(line.strip() for line in t.splitlines() if line.strip()).encode())
     return h.hexdigest()
+
+
+def source_hash(kernel):
+    texts = []
+    for name in KERNEL_SOURCES[kernel] + ["common.cuh"]:
+        with open(os.path.join(ROOT, "linear_attention_decode_replayssm_gb300", "csrc", name)) as f:
+            texts.append(f.read())
+    return code_digest(texts)
 
 
 class Layer:

@@ -30,7 +30,9 @@
 // strided across the batch, so the ~1/L flush rows (which also write their
 // state) spread evenly over the CTAs.  Every wait is bounded: on a timeout
 // the kernel reports RS_DERR_TIMEOUT, drains its own copies and returns.
-// No tensor cores: the step is a bandwidth-bound GEMV (about 0.6 FLOP/byte).
+// The per-step products stay on the CUDA cores (a bandwidth-bound GEMV, about
+// 0.6 FLOP/byte); the flush fold of an fp32 checkpoint, a rank-(p+1) update of
+// the whole state held in registers, runs on the tensor cores.
 #pragma once
 
 #include <type_traits>
