@@ -27,11 +27,19 @@
 // Same pipeline as the Mamba-2 kernel: persistent, two CTAs per SM, one
 // producer warp (the unit's checkpoint rows as one bulk copy into a
 // checkpoint slot, the ring records, this token's inputs and the gates as
-// per-lane cp.async into a record slot), eight consumer warps that take the
-// checkpoint into registers, free its slot at once and compute from the
-// record slot.  One streaming pass over the checkpoint yields S_ckpt k_t and
-// S_ckpt q_t together through one transposed group reduction.  All waits are
-// bounded and report RS_DERR_TIMEOUT instead of hanging.
+// per-lane cp.async into a record slot).  A window warp takes each record
+// slot as it lands and computes everything that does not touch the
+// checkpoint: the gate weights G_j and Gamma, the key dots k_j . k_t and
+// k_j . q_t (four records per reduction), the window terms
+// sum_j G_j (k_j . k_t) d_j and sum_j G_j (k_j . q_t) d_j of every state row,
+// and the key and gate append; it signals the consumers on a second barrier.
+// The consumer warps take the checkpoint into registers, free its slot at
+// once, and form S_ckpt k_t and S_ckpt q_t in one pass with one transposed
+// group reduction; the lanes that finish a row add the window terms, form
+// d_t and the output, or fold the window into the row on a flush.  A state
+// row never leaves its warp, so the consumer warps never wait for each
+// other.  All waits are bounded and report RS_DERR_TIMEOUT instead of
+// hanging.
 #include "common.cuh"
 #include "launch.h"
 #include "replayssm.h"
@@ -53,36 +61,39 @@ __host__ __device__ inline GdnRec gdn_rec(int RB, int DK, int res, int ies, int 
   s.vt = o;   o = align128(o + RB * ies);
   s.a = o;    o = align128(o + (L + 4) * 4);     // g_0..g_{p-1}; [L] = g_t, [L+1] = beta_t
   s.meta = o; o = align128(o + 16);
-  s.scr = o;  o = align128(o + (3 * L + 5 * RB + 4) * 4);  // G_j, k_j.k_t, k_j.q_t, row dots, d_t, o / row sums
+  s.scr = o;  o = align128(o + (3 * L + 3 * RB + 4) * 4);  // G_j, weighted key dots, row window terms, d_t, scalars
   s.bytes = o;
   return s;
 }
 
-__host__ __device__ inline uint32_t gdn_head(int nsr, int nsc) { return align128(8 * (2 * nsr + nsc) + 16); }
+// barriers: full, ready and empty per record slot, empty per checkpoint slot
+__host__ __device__ inline uint32_t gdn_head(int nsr, int nsc) { return align128(8 * (3 * nsr + nsc) + 16); }
 
-// LMAX bounds the buffer length at compile time (L <= LMAX): loops over a
-// window's records unroll to a fixed count with predicated bodies.
+// LMAX bounds the buffer length at compile time (L <= LMAX).
 // CPR: 16-byte checkpoint chunks a consumer lane holds per state row (chunks
 // cv, cv + G, ...), so the row reductions run over G = DK / (E CPR) lanes.
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP, int LMAX, int CPR>
-__global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int LMAX, int CPR>
+__global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr int RB = DV / NSPLIT;    // state rows per unit
   constexpr int E = V::E;
   constexpr int NCH = DK / E;        // 16-byte chunks per state row
   constexpr int G = NCH / CPR;       // lanes per state row
-  constexpr int NC = NCW * 32;       // consumer threads per group
+  constexpr int NC = NCW * 32;       // consumer threads
   constexpr int RPP = NC / G;        // state rows per pass
   constexpr int VPT = RB / RPP;      // state rows per consumer thread
-  constexpr int PROD = NGRP * NCW;   // warp index of the producer
+  constexpr int WIN = NCW;           // warp index of the window warp
+  constexpr int PROD = NCW + 1;      // warp index of the producer
+  constexpr int RPL = (RB + 31) / 32;  // state rows per window-warp lane
   constexpr uint32_t CKB = RB * DK * (uint32_t)sizeof(TC);
   static_assert(G <= 32 && 32 % G == 0 && NCH % CPR == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && RB % RPP == 0 && VPT >= 1 && 2 * VPT <= G, "bad tiling");
-  static_assert(DK % 8 == 0 && RB % 8 == 0, "head dims must be multiples of 8");
+  static_assert(DK % 8 == 0 && RB % 8 == 0 && DK <= 128 && RB <= 32 * RPL, "bad head dims");
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-  uint64_t *rec_empty = full + nsr;
+  uint64_t *ready = full + nsr;
+  uint64_t *rec_empty = ready + nsr;
   uint64_t *ck_empty = rec_empty + nsr;
   int *s_abort = reinterpret_cast<int *>(ck_empty + nsc);
   const int L = a.L;
@@ -96,11 +107,19 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
   const int per_row = a.H * NSPLIT;
   const int n_units = a.B * per_row;
   const int stride = gridDim.x;
+  // a wait that ran out: flag every warp to stop and report it once per warp
+  auto fail = [&]() {
+    if (lane == 0) {
+      *(volatile int *)s_abort = 1;
+      report(a.dev_err, kDerrTimeout);
+    }
+  };
 
   if (tid == 0) {
     for (int s = 0; s < nsr; ++s) {
       mbar_init(&full[s], 33);
-      mbar_init(&rec_empty[s], NC);  // every thread of the consuming group
+      mbar_init(&ready[s], 32);           // the window warp's lanes
+      mbar_init(&rec_empty[s], NC + 32);  // every consumer thread and the window warp
     }
     for (int c = 0; c < nsc; ++c) mbar_init(&ck_empty[c], NC);
     *s_abort = 0;
@@ -144,7 +163,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
           }
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w || *(volatile int *)s_abort) {
-            if (lane == 0) *(volatile int *)s_abort = 1;
+            fail();
             ok = false;
             break;
           }
@@ -220,42 +239,170 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
     return;
   }
 
-  // ------------------------------------------------------------------ consumers
-  // group g takes the CTA's units g, g + NGRP, ...; each group has its own
-  // named barrier, so the groups run independently of each other
-  const int grp = warp / NCW;
-  const int lw = warp - grp * NCW, ctid = tid - grp * NC;
-  const int row0 = ctid / G, cv = ctid - (ctid / G) * G;
-  auto gsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(NC) : "memory"); };
-  // slot indices and the full-barrier phase, stepped instead of divided
-  int s = grp % nsr, c = grp % nsc;
-  uint32_t ph = (uint32_t)(grp / nsr) & 1u;
-  for (int it = grp; ; it += NGRP) {
-    if (it != grp) {
-      s += NGRP;
-      if (s >= nsr) {
-        s -= nsr;
+
+  if (warp == WIN) {
+    // --------------------------------------------------------------- window
+    int s = 0;
+    uint32_t ph = 0;
+    for (int it = 0;; ++it) {
+      if (it && ++s == nsr) {
+        s = 0;
         ph ^= 1u;
       }
-      c += NGRP;
-      if (c >= nsc) c -= nsc;
+      const int u = blockIdx.x + it * stride;
+      if (u >= n_units) break;
+      const bool w = mbar_wait(&full[s], ph);
+      if (!__all_sync(0xffffffffu, w) || *(volatile int *)s_abort) {
+        fail();
+        break;
+      }
+      unsigned char *st = rec_slots + (size_t)s * lay.bytes;
+      const int *meta = reinterpret_cast<const int *>(st + lay.meta);
+      const int slot = meta[0], p = meta[1], flush = meta[2], status = meta[3];
+      const float *sa = reinterpret_cast<const float *>(st + lay.a);
+      float *scr = reinterpret_cast<float *>(st + lay.scr);
+      float *sW = scr, *sDk = scr + L, *sDq = scr + 2 * L;
+      float *sCk = scr + 3 * L, *sCq = sCk + RB, *sScal = sCq + 2 * RB;
+      const unsigned char *sk = st + lay.k, *skt = st + lay.kt, *sq = st + lay.q, *sd = st + lay.d;
+      if (status == kStatusOk) {
+        // gate weights: G_j = exp(sum of the gates after record j), Gamma = exp(sum of all)
+        float x0 = lane < p ? sa[lane] : 0.f;
+        float x1 = lane + 32 < p ? sa[lane + 32] : 0.f;
+        suffix_scan64(x0, x1, lane, [](float x, float y) { return x + y; });
+        const float n0 = __shfl_down_sync(0xffffffffu, x0, 1);
+        const float n1 = __shfl_down_sync(0xffffffffu, x1, 1);
+        const float hi0 = __shfl_sync(0xffffffffu, x1, 0);
+        if (lane < p) sW[lane] = expf(lane == 31 ? hi0 : n0);
+        if (lane + 32 < p) sW[lane + 32] = expf(lane == 31 ? 0.f : n1);
+        if (lane == 0) {
+          sScal[0] = expf(x0);
+          sScal[2] = expf(sa[L]);  // alpha_t
+        }
+        __syncwarp();
+        // k_j . k_t and k_j . q_t, four records per transposed reduction;
+        // record p is this token's key (its q-dot is k_t . q_t)
+        float kt4[4], q4[4];
+        const int col = lane * 4;
+        if (col < DK) {
+          lds_cols<4>(skt, col, idt, kt4);
+          lds_cols<4>(sq, col, idt, q4);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) kt4[e] = q4[e] = 0.f;
+        }
+#pragma unroll 1
+        for (int j0 = 0; j0 <= p; j0 += 4) {
+          float part[8];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int j = j0 + r;
+            float kk[4] = {0.f, 0.f, 0.f, 0.f};
+            if (col < DK) {
+              if (j < p) {
+                lds_cols<4>(sk, j * DK + col, rdt, kk);
+              } else if (j == p) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) kk[e] = kt4[e];
+              }
+            }
+            float dk = 0.f, dq = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              dk = fmaf(kk[e], kt4[e], dk);
+              dq = fmaf(kk[e], q4[e], dq);
+            }
+            part[r] = dk;
+            part[4 + r] = dq;
+          }
+          group_reduce<8, 32>(part, lane);
+          if (group_reduce_writer<8, 32>(lane)) {
+            const int vi = group_reduce_index<8, 32>(lane);
+            const int j = j0 + (vi & 3);
+            if (j < p) {
+              if (vi < 4)
+                sDk[j] = sW[j] * part[0];
+              else
+                sDq[j] = sW[j] * part[0];
+            } else if (j == p && vi >= 4) {
+              sScal[1] = part[0];  // k_t . q_t
+            }
+          }
+        }
+        __syncwarp();
+        // window terms of S_{t-1} k_t and S_{t-1} q_t for this lane's rows
+        if (lane * RPL < RB) {
+          float cK[RPL], cQ[RPL];
+#pragma unroll
+          for (int e = 0; e < RPL; ++e) cK[e] = cQ[e] = 0.f;
+#pragma unroll 4
+          for (int j = 0; j < p; ++j) {
+            const float wk = sDk[j], wq = sDq[j];
+#pragma unroll
+            for (int e = 0; e < RPL; ++e) {
+              const float dd = lds_elem(sd, j * RB + lane * RPL + e, rdt);
+              cK[e] = fmaf(wk, dd, cK[e]);
+              cQ[e] = fmaf(wq, dd, cQ[e]);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < RPL; ++e) {
+            sCk[lane * RPL + e] = cK[e];
+            sCq[lane * RPL + e] = cQ[e];
+          }
+        }
+        __syncwarp();
+      }
+      mbar_arrive(&ready[s]);
+      if (status == kStatusOk && !flush) {
+        const int rem = u - (u / per_row) * per_row;
+        if (rem - (rem / NSPLIT) * NSPLIT == 0) {
+          // append this token's key (rounded to the ring type) and gate, once per head
+          const size_t unit = (size_t)slot * a.H + rem / NSPLIT;
+          for (int cc = lane; cc < DK / 8; cc += 32) {
+            float f[8];
+            lds_cols<8>(skt, cc * 8, idt, f);
+            store8(a.ring_k, (unit * L + p) * DK + cc * 8, rdt, f);
+          }
+          if (lane == 0) a.ring_a[unit * L + p] = sa[L];
+        }
+      }
+      mbar_arrive(&rec_empty[s]);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  // every consumer warp takes every unit; the lanes of a state row are in
+  // one warp, so the warps run independently of each other
+  const int row0 = tid / G, cv = tid - (tid / G) * G;
+  int s = 0, c = 0;
+  uint32_t ph = 0;
+  for (int it = 0;; ++it) {
+    if (it) {
+      if (++s == nsr) {
+        s = 0;
+        ph ^= 1u;
+      }
+      if (++c == nsc) c = 0;
     }
     const int u = blockIdx.x + it * stride;
     if (u >= n_units) break;
-    if (lane == 0 && !mbar_wait(&full[s], ph)) *(volatile int *)s_abort = 1;
-    gsync();
-    if (*(volatile int *)s_abort) break;
+    const bool w = mbar_wait(&full[s], ph) && mbar_wait(&ready[s], ph);
+    if (!__all_sync(0xffffffffu, w) || *(volatile int *)s_abort) {
+      fail();
+      break;
+    }
 
-    const unsigned char *st = rec_slots + (size_t)s * lay.bytes;
+    unsigned char *st = rec_slots + (size_t)s * lay.bytes;
     const int *meta = reinterpret_cast<const int *>(st + lay.meta);
     const int slot = meta[0], p = meta[1], flush = meta[2], status = meta[3];
     const int b = u / per_row;
     const int rem = u - b * per_row;
-    const int h = rem / NSPLIT, half = rem - h * NSPLIT, row_off = half * RB;
+    const int h = rem / NSPLIT, row_off = (rem - h * NSPLIT) * RB;
     float *orow = a.out + (size_t)b * a.so + (size_t)h * DV + row_off;
     if (status != kStatusOk) {
-      for (int i = ctid; i < RB; i += NC) orow[i] = 0.f;
-      if (ctid == 0 && status != kStatusPad) report(a.dev_err, status == kStatusBadSlot ? 1 : 2);
+      for (int i = tid; i < RB; i += NC) orow[i] = 0.f;
+      if (tid == 0 && status != kStatusPad) report(a.dev_err, status == kStatusBadSlot ? 1 : 2);
       mbar_arrive(&ck_empty[c]);
       mbar_arrive(&rec_empty[s]);
       continue;
@@ -272,73 +419,12 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
 
     const size_t unit = (size_t)slot * a.H + h;
     const float *sa = reinterpret_cast<const float *>(st + lay.a);
-    float *scr = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + lay.scr);
-    float *sW = scr, *sDk = scr + L, *sDq = scr + 2 * L;
-    float *sAk = scr + 3 * L, *sAq = sAk + RB, *sDt = sAq + RB, *sC = sDt + RB, *sScal = sC + 2 * RB;
+    float *scr = reinterpret_cast<float *>(st + lay.scr);
+    const float *sW = scr, *sCk = scr + 3 * L, *sCq = sCk + RB;
+    float *sDt = scr + 3 * L + 2 * RB;
+    const float *sScal = sDt + RB;
     const unsigned char *sk = st + lay.k, *skt = st + lay.kt, *sq = st + lay.q, *sd = st + lay.d;
 
-    // decay weights over the held records (warp 0)
-    if (lw == 0) {
-      float x0 = lane < p ? sa[lane] : 0.f;
-      float x1 = lane + 32 < p ? sa[lane + 32] : 0.f;
-      suffix_scan64(x0, x1, lane, [](float x, float y) { return x + y; });
-      const float n0 = __shfl_down_sync(0xffffffffu, x0, 1);
-      const float n1 = __shfl_down_sync(0xffffffffu, x1, 1);
-      const float hi0 = __shfl_sync(0xffffffffu, x1, 0);
-      if (lane < p) sW[lane] = expf(lane == 31 ? hi0 : n0);
-      if (lane + 32 < p) sW[lane + 32] = expf(lane == 31 ? 0.f : n1);
-      if (lane == 0) sScal[0] = expf(x0);
-    }
-    // k_j . k_t and k_j . q_t for the held records (k_t . q_t at j == p): a
-    // warp takes records four at a time; each lane holds its 4-column chunks
-    // of k_t and q_t and accumulates 2 x 4 partial dots, and one transposed
-    // reduction finishes the chunk
-    {
-      constexpr int QPL = (DK + 127) / 128;
-      float kt4[QPL][4], q4[QPL][4];
-#pragma unroll
-      for (int i = 0; i < QPL; ++i) {
-        if (lane * 4 + i * 128 < DK) {
-          lds_cols<4>(skt, lane * 4 + i * 128, idt, kt4[i]);
-          lds_cols<4>(sq, lane * 4 + i * 128, idt, q4[i]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) kt4[i][e] = q4[i][e] = 0.f;
-        }
-      }
-      // one record per warp, so the records of a window are done in
-      // parallel: the two dots of a record finish in one 2-value reduction
-      for (int j = lw; j <= p; j += NCW) {
-        float part2[2] = {0.f, 0.f};  // k_j . k_t, k_j . q_t
-#pragma unroll
-        for (int i = 0; i < QPL; ++i) {
-          const int cc = lane * 4 + i * 128;
-          if (cc < DK) {
-            float kk[4];
-            if (j < p) {
-              lds_cols<4>(sk, j * DK + cc, rdt, kk);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) kk[e] = kt4[i][e];
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              part2[0] = fmaf(kk[e], kt4[i][e], part2[0]);
-              part2[1] = fmaf(kk[e], q4[i][e], part2[1]);
-            }
-          }
-        }
-        group_reduce<2, 32>(part2, lane);
-        if (group_reduce_writer<2, 32>(lane)) {
-          const int vi = group_reduce_index<2, 32>(lane);
-          if (j < p) {
-            if (vi == 0) sDk[j] = part2[0]; else sDq[j] = part2[0];
-          } else if (vi == 1) {
-            sScal[1] = part2[0];  // k_t . q_t
-          }
-        }
-      }
-    }
     // S_ckpt k_t and S_ckpt q_t for this thread's rows
     float ktc[CPR][E], qc[CPR][E];
 #pragma unroll
@@ -346,75 +432,44 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
       lds_cols<E>(skt, (cv + G * i) * E, idt, ktc[i]);
       lds_cols<E>(sq, (cv + G * i) * E, idt, qc[i]);
     }
-    {
-      float part[2 * VPT];
+    float part[2 * VPT];
 #pragma unroll
-      for (int r = 0; r < VPT; ++r) {
-        float s0 = 0.f, s1 = 0.f;
+    for (int r = 0; r < VPT; ++r) {
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < CPR; ++i) {
-          float f[E];
-          V::unpack(raw[r][i], f);
+      for (int i = 0; i < CPR; ++i) {
+        float f[E];
+        V::unpack(raw[r][i], f);
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            s0 = fmaf(f[e], ktc[i][e], s0);
-            s1 = fmaf(f[e], qc[i][e], s1);
-          }
+        for (int e = 0; e < E; ++e) {
+          s0 = fmaf(f[e], ktc[i][e], s0);
+          s1 = fmaf(f[e], qc[i][e], s1);
         }
-        part[r] = s0;
-        part[VPT + r] = s1;
       }
-      group_reduce<2 * VPT, G>(part, lane);
-      if (group_reduce_writer<2 * VPT, G>(lane)) {
-        const int vi = group_reduce_index<2 * VPT, G>(lane);
-        if (vi < VPT)
-          sAk[row0 + vi * RPP] = part[0];
-        else
-          sAq[row0 + (vi - VPT) * RPP] = part[0];
-      }
+      part[r] = s0;
+      part[VPT + r] = s1;
     }
-    gsync();
-
-    // per row: S_{t-1} k_t, S_{t-1} q_t, then d_t, one thread per row (the
-    // window's weights and key dots are shared-memory broadcasts, the d
-    // records are read row-contiguous, and no cross-lane reduction is needed)
-    const float gam = sScal[0], kq = sScal[1];
-    const float g_t = sa[L], beta_t = sa[L + 1];
-    const float alpha_t = expf(g_t);
-    static_assert(RB <= NC, "one consumer thread per state row");
-    if (ctid < RB) {
-      const int i = ctid;
-      float accK = 0.f, accQ = 0.f;
-#pragma unroll
-      for (int j = 0; j < LMAX; ++j) {
-        if (j >= p) break;
-        const float w = sW[j];
-        const float dd = lds_elem(sd, j * RB + i, rdt);
-        accK = fmaf(w * sDk[j], dd, accK);
-        accQ = fmaf(w * sDq[j], dd, accQ);
-      }
-      const float Ak = fmaf(gam, sAk[i], accK);
-      const float Aq = fmaf(gam, sAq[i], accQ);
-      const float d_t = beta_t * (lds_elem(st + lay.vt, i, idt) - alpha_t * Ak);
-      if (!flush) {
-        orow[i] = fmaf(alpha_t, Aq, d_t * kq);
-        store1(a.ring_v, (unit * L + p) * DV + row_off + i, rdt, d_t);
-      } else {
-        sDt[i] = d_t;
-      }
-    }
+    group_reduce<2 * VPT, G>(part, lane);
+    // the lane holding row r's S_ckpt k_t and the one holding its S_ckpt q_t
+    // differ in lane bit G/2
+    const float gam = sScal[0], kq = sScal[1], alpha_t = sScal[2], beta_t = sa[L + 1];
+    const int vi = group_reduce_index<2 * VPT, G>(lane);
+    const bool isK = vi < VPT;
+    const int rrow = row0 + (isK ? vi : vi - VPT) * RPP;
+    const float A = fmaf(gam, part[0], isK ? sCk[rrow] : sCq[rrow]);  // S_{t-1} k_t or S_{t-1} q_t
+    const float d_t = isK ? beta_t * (lds_elem(st + lay.vt, rrow, idt) - alpha_t * A) : 0.f;
+    const float d_pair = __shfl_xor_sync(0xffffffffu, d_t, G / 2);
+    const bool wr = group_reduce_writer<2 * VPT, G>(lane);
     if (!flush) {
-      if (half == 0) {
-        // append this token's key (rounded to the ring type) and gate
-        for (int cc = ctid; cc < DK / 8; cc += NC) {
-          float f[8];
-          lds_cols<8>(skt, cc * 8, idt, f);
-          store8(a.ring_k, (unit * L + p) * DK + cc * 8, rdt, f);
-        }
-        if (ctid == NC - 1) a.ring_a[unit * L + p] = g_t;
+      if (wr) {
+        if (isK)
+          store1(a.ring_v, (unit * L + p) * DV + row_off + rrow, rdt, d_t);
+        else
+          orow[rrow] = fmaf(alpha_t, A, d_pair * kq);
       }
     } else {
-      gsync();  // d_t of every row ready
+      if (wr && isK) sDt[rrow] = d_t;
+      __syncwarp();
       TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK) + (size_t)row_off * DK;
       const float scale0 = alpha_t * gam;
       float f[VPT][CPR][E];
@@ -458,19 +513,16 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) gdn_replay_kernel(con
         po[r] = acc;
       }
       group_reduce<VPT, G>(po, lane);
-      if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = po[0];
-      gsync();
-      for (int i = ctid; i < RB; i += NC) orow[i] = sC[i];
+      if (group_reduce_writer<VPT, G>(lane)) orow[row0 + group_reduce_index<VPT, G>(lane) * RPP] = po[0];
     }
     mbar_arrive(&rec_empty[s]);
   }
-  if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
 }
 
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP, int LMAX, int CPR>
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int LMAX, int CPR>
 static cudaError_t launch_gdn_l(const KArgs &a, cudaStream_t s) {
-  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, LMAX, CPR>;
-  constexpr int threads = NGRP * NCW * 32 + 32;
+  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT, LMAX, CPR>;
+  constexpr int threads = NCW * 32 + 64;
   const size_t ckb = (size_t)(DV / NSPLIT) * DK * sizeof(TC);
   const size_t rb = gdn_rec(DV / NSPLIT, DK, (int)sizeof(RT), (int)sizeof(IT), a.L).bytes;
   RingPlan plan;
@@ -482,10 +534,10 @@ static cudaError_t launch_gdn_l(const KArgs &a, cudaStream_t s) {
 }
 
 // the common short windows get a kernel unrolled for L <= 16
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int NGRP = 1, int CPR = 1>
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int CPR = 1>
 static cudaError_t launch_gdn(const KArgs &a, cudaStream_t s) {
-  return a.L <= 16 ? launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, 16, CPR>(a, s)
-                   : launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, NGRP, RS_MAX_L, CPR>(a, s);
+  return a.L <= 16 ? launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, 16, CPR>(a, s)
+                   : launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, RS_MAX_L, CPR>(a, s);
 }
 
 template <typename TC, typename RT, typename IT>
@@ -493,7 +545,7 @@ static LaunchFn find_gdn_t(int d_v, int d_k) {
   constexpr bool f32 = sizeof(TC) == 4;
   if (d_v == 16 && d_k == 32) return launch_gdn<16, 32, TC, RT, IT, f32 ? 4 : 2, 1>;
   if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, TC, RT, IT, 8, 1>;
-  if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, TC, RT, IT, 8, f32 ? 2 : 1, 1, 2>;
+  if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, TC, RT, IT, 8, 2, f32 ? 2 : 1>;
   return nullptr;
 }
 

@@ -235,6 +235,19 @@ def test_gdn_buffer_lengths(cuda, L):
     assert r32["o_exact"] <= TOL_F32 and r32["ck_exact"] <= TOL_F32, r32
 
 
+@pytest.mark.parametrize("d_v, in_dtype, ckpt_dtype", [(64, "bf16", "f32"), (128, "f32", "f32"), (64, "f32", "f16")])
+def test_gdn_other_shapes_and_inputs(cuda, d_v, in_dtype, ckpt_dtype):
+    # 64 x 128 heads (one unit per head) and fp32 inputs, with fp32 rings so
+    # that the comparison with the exact recurrence is tight
+    w = synth.make_workload("gdn_bs256", B=5, H=3, d_v=d_v, steps=40, in_dtype=in_dtype, ring_dtype="f32",
+                            ckpt_dtype=ckpt_dtype, pad_rows=1, seed=d_v + len(in_dtype))
+    r = run_parity(cuda, w, w.steps)
+    if ckpt_dtype == "f32":
+        assert r["o_exact"] <= TOL_F32 and r["ck_exact"] <= TOL_F32, r
+    else:
+        assert r["o_exact"] <= TOL_F16 and r["o_replay"] <= TOL_F16_EMU, r
+
+
 def test_gdn_bs256_full_size_sampled(cuda):
     # batch 256, 32 value heads of 128 x 128, fp32 checkpoint, fp16 d/k rings,
     # fp32 g ring, L = 16 staggered, 256 steps; the oracle follows two heads

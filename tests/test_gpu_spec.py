@@ -165,3 +165,52 @@ def test_spec_range_checks(cuda):
                               T=T, dev_err=err)
     assert int(err.item()) == lib.RS_DERR_ACCEPTED
     assert h_d.cpu().tolist() == [5, 0, 0]
+
+
+def test_spec_verify_fp16_checkpoint(cuda):
+    """fp16 checkpoint, T = 4: against the oracle's verification with the same
+    storage rounding (the folded checkpoint rounded to fp16 at each flush),
+    max relative error 2e-3 (one fp16 rounding of the checkpoint, where the
+    fp32 and float64 folds may round a midpoint apart), and against the exact
+    recurrence 2e-2 (the fp16 checkpoint gate)."""
+    import torch
+
+    lib = cuda
+    T, steps = 4, 40
+    w = synth.make_workload("mamba2_bs256", B=6, H=3, steps=1, seed=61, ckpt_dtype="f16")
+    L, B, td = w.L, w.B, tdt(w.in_dtype)
+    ckpt = dev(w.ckpt0, torch.float16)
+    ring_v, ring_k = dev(w.ring_v0, td), dev(w.ring_k0, td)
+    ring_a = dev(w.ring_a0, torch.float32)
+    slot_idx = dev(w.slot_idx, torch.int32)
+    out = torch.empty(B, T, w.H, w.d_v, device="cuda")
+    err = torch.zeros(1, device="cuda", dtype=torch.int32)
+    h = (w.decode_step0 % L).astype(np.int32)
+    fl = spec.spec_plan(h, L, T)
+    h_d, fl_d = dev(h, torch.int32), dev(fl, torch.uint8)
+    rs = oracle.ReplayState("mamba2", w.ckpt0.astype(np.float64), w.ring_v0.astype(np.float64),
+                            w.ring_k0.astype(np.float64), w.ring_a0.astype(np.float64), ckpt_dtype="f16")
+    exact = oracle.ExactState.from_replay(rs, w.held_records()).S
+    r = np.random.default_rng(61)
+    worst_emu = worst_exact = 0.0
+    for t in range(steps):
+        v, k, q, a = _drafts(w, t, T)
+        lib.replayssm_spec_verify_mamba2(ckpt=ckpt, ring_v=ring_v, ring_k=ring_k, ring_a=ring_a, slot_idx=slot_idx,
+                                         committed=h_d, is_flush=fl_d, v=dev(v, td), k=dev(k, td), q=dev(q, td),
+                                         alpha=dev(a, torch.float32), out=out, dev_err=err)
+        o_g = out.double().cpu().numpy()
+        o_emu = spec.spec_verify_step(rs, w.slot_idx, h, fl, v, k, q, a)
+        worst_emu = max(worst_emu, rel_err(o_g, o_emu))
+        acc = r.integers(1, T + 1, B).astype(np.int32)
+        for b in range(B):
+            S = exact[w.slot_idx[b]].copy()
+            for i in range(T):
+                S, o_i = oracle.mamba2_step(S, a[b, i], v[b, i], k[b, i], q[b, i])
+                worst_exact = max(worst_exact, rel_err(o_g[b, i], o_i))
+                if i + 1 == acc[b]:
+                    exact[w.slot_idx[b]] = S.copy()
+        lib.replayssm_spec_commit(committed=h_d, is_flush=fl_d, accepted=dev(acc, torch.int32), L=L, T=T,
+                                  dev_err=err)
+        h, fl = spec.spec_commit(h, fl, acc, L, T)
+    assert int(err.item()) == 0
+    assert worst_emu <= 2e-3 and worst_exact <= 2e-2, (worst_emu, worst_exact)
