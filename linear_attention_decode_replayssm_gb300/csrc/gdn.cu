@@ -30,9 +30,9 @@
 // per-lane cp.async into a record slot).  A window warp takes each record
 // slot as it lands and computes everything that does not touch the
 // checkpoint: the gate weights G_j and Gamma, the key dots k_j . k_t and
-// k_j . q_t (four records per reduction), the window terms
-// sum_j G_j (k_j . k_t) d_j and sum_j G_j (k_j . q_t) d_j of every state row,
-// and the key and gate append; it signals the consumers on a second barrier.
+// k_j . q_t (eight records per reduction) and the window terms
+// sum_j G_j (k_j . k_t) d_j and sum_j G_j (k_j . q_t) d_j of every state row;
+// it signals the consumers on a second barrier.
 // The consumer warps take the checkpoint into registers, free its slot at
 // once, and form S_ckpt k_t and S_ckpt q_t in one pass with one transposed
 // group reduction; the lanes that finish a row add the window terms, form
@@ -258,28 +258,31 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
       }
       unsigned char *st = rec_slots + (size_t)s * lay.bytes;
       const int *meta = reinterpret_cast<const int *>(st + lay.meta);
-      const int slot = meta[0], p = meta[1], flush = meta[2], status = meta[3];
+      const int p = meta[1], status = meta[3];
       const float *sa = reinterpret_cast<const float *>(st + lay.a);
       float *scr = reinterpret_cast<float *>(st + lay.scr);
       float *sW = scr, *sDk = scr + L, *sDq = scr + 2 * L;
       float *sCk = scr + 3 * L, *sCq = sCk + RB, *sScal = sCq + 2 * RB;
       const unsigned char *sk = st + lay.k, *skt = st + lay.kt, *sq = st + lay.q, *sd = st + lay.d;
       if (status == kStatusOk) {
-        // gate weights: G_j = exp(sum of the gates after record j), Gamma = exp(sum of all)
+        // gate weights: G_j = exp(sum of the gates after record j), Gamma =
+        // exp(sum of all); lane j keeps G_j (and G_{j+32}) for the dots below
         float x0 = lane < p ? sa[lane] : 0.f;
         float x1 = lane + 32 < p ? sa[lane + 32] : 0.f;
         suffix_scan64(x0, x1, lane, [](float x, float y) { return x + y; });
         const float n0 = __shfl_down_sync(0xffffffffu, x0, 1);
         const float n1 = __shfl_down_sync(0xffffffffu, x1, 1);
         const float hi0 = __shfl_sync(0xffffffffu, x1, 0);
-        if (lane < p) sW[lane] = expf(lane == 31 ? hi0 : n0);
-        if (lane + 32 < p) sW[lane + 32] = expf(lane == 31 ? 0.f : n1);
+        const float gw0 = expf(lane == 31 ? hi0 : n0);
+        float gw1 = 0.f;
+        if constexpr (LMAX > 32) gw1 = expf(lane == 31 ? 0.f : n1);
+        if (lane < p) sW[lane] = gw0;
+        if (LMAX > 32 && lane + 32 < p) sW[lane + 32] = gw1;
         if (lane == 0) {
           sScal[0] = expf(x0);
           sScal[2] = expf(sa[L]);  // alpha_t
         }
-        __syncwarp();
-        // k_j . k_t and k_j . q_t, four records per transposed reduction;
+        // k_j . k_t and k_j . q_t, eight records per transposed reduction;
         // record p is this token's key (its q-dot is k_t . q_t)
         float kt4[4], q4[4];
         const int col = lane * 4;
@@ -291,10 +294,10 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
           for (int e = 0; e < 4; ++e) kt4[e] = q4[e] = 0.f;
         }
 #pragma unroll 1
-        for (int j0 = 0; j0 <= p; j0 += 4) {
-          float part[8];
+        for (int j0 = 0; j0 <= p; j0 += 8) {
+          float part[16];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
+          for (int r = 0; r < 8; ++r) {
             const int j = j0 + r;
             float kk[4] = {0.f, 0.f, 0.f, 0.f};
             if (col < DK) {
@@ -312,18 +315,23 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
               dq = fmaf(kk[e], q4[e], dq);
             }
             part[r] = dk;
-            part[4 + r] = dq;
+            part[8 + r] = dq;
           }
-          group_reduce<8, 32>(part, lane);
-          if (group_reduce_writer<8, 32>(lane)) {
-            const int vi = group_reduce_index<8, 32>(lane);
-            const int j = j0 + (vi & 3);
+          group_reduce<16, 32>(part, lane);
+          const int vi = group_reduce_index<16, 32>(lane);
+          const int j = j0 + (vi & 7);
+          float gj = __shfl_sync(0xffffffffu, gw0, j & 31);
+          if constexpr (LMAX > 32) {
+            const float g1 = __shfl_sync(0xffffffffu, gw1, j & 31);
+            if (j >= 32) gj = g1;
+          }
+          if (group_reduce_writer<16, 32>(lane)) {
             if (j < p) {
-              if (vi < 4)
-                sDk[j] = sW[j] * part[0];
+              if (vi < 8)
+                sDk[j] = gj * part[0];
               else
-                sDq[j] = sW[j] * part[0];
-            } else if (j == p && vi >= 4) {
+                sDq[j] = gj * part[0];
+            } else if (j == p && vi >= 8) {
               sScal[1] = part[0];  // k_t . q_t
             }
           }
@@ -353,19 +361,6 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
         __syncwarp();
       }
       mbar_arrive(&ready[s]);
-      if (status == kStatusOk && !flush) {
-        const int rem = u - (u / per_row) * per_row;
-        if (rem - (rem / NSPLIT) * NSPLIT == 0) {
-          // append this token's key (rounded to the ring type) and gate, once per head
-          const size_t unit = (size_t)slot * a.H + rem / NSPLIT;
-          for (int cc = lane; cc < DK / 8; cc += 32) {
-            float f[8];
-            lds_cols<8>(skt, cc * 8, idt, f);
-            store8(a.ring_k, (unit * L + p) * DK + cc * 8, rdt, f);
-          }
-          if (lane == 0) a.ring_a[unit * L + p] = sa[L];
-        }
-      }
       mbar_arrive(&rec_empty[s]);
     }
     return;
@@ -387,7 +382,10 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
     }
     const int u = blockIdx.x + it * stride;
     if (u >= n_units) break;
-    const bool w = mbar_wait(&full[s], ph) && mbar_wait(&ready[s], ph);
+    // the checkpoint and records have landed; the window warp's terms are
+    // awaited only after the checkpoint pass, so its latency does not hold
+    // the checkpoint slot
+    const bool w = mbar_wait(&full[s], ph);
     if (!__all_sync(0xffffffffu, w) || *(volatile int *)s_abort) {
       fail();
       break;
@@ -398,13 +396,13 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
     const int slot = meta[0], p = meta[1], flush = meta[2], status = meta[3];
     const int b = u / per_row;
     const int rem = u - b * per_row;
-    const int h = rem / NSPLIT, row_off = (rem - h * NSPLIT) * RB;
+    const int h = rem / NSPLIT, half = rem - h * NSPLIT, row_off = half * RB;
     float *orow = a.out + (size_t)b * a.so + (size_t)h * DV + row_off;
     if (status != kStatusOk) {
       for (int i = tid; i < RB; i += NC) orow[i] = 0.f;
       if (tid == 0 && status != kStatusPad) report(a.dev_err, status == kStatusBadSlot ? 1 : 2);
       mbar_arrive(&ck_empty[c]);
-      mbar_arrive(&rec_empty[s]);
+      mbar_arrive(&rec_empty[s]);  // the window warp arrives on it too before the slot is reused
       continue;
     }
     uint4 raw[VPT][CPR];
@@ -450,6 +448,13 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
       part[VPT + r] = s1;
     }
     group_reduce<2 * VPT, G>(part, lane);
+    {
+      const bool wr = mbar_wait(&ready[s], ph);
+      if (!__all_sync(0xffffffffu, wr) || *(volatile int *)s_abort) {
+        fail();
+        break;
+      }
+    }
     // the lane holding row r's S_ckpt k_t and the one holding its S_ckpt q_t
     // differ in lane bit G/2
     const float gam = sScal[0], kq = sScal[1], alpha_t = sScal[2], beta_t = sa[L + 1];
@@ -466,6 +471,15 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
           store1(a.ring_v, (unit * L + p) * DV + row_off + rrow, rdt, d_t);
         else
           orow[rrow] = fmaf(alpha_t, A, d_pair * kq);
+      }
+      if (warp == NCW - 1 && half == 0) {
+        // append this token's key (rounded to the ring type) and gate, once per head
+        for (int cc = lane; cc < DK / 8; cc += 32) {
+          float f[8];
+          lds_cols<8>(skt, cc * 8, idt, f);
+          store8(a.ring_k, (unit * L + p) * DK + cc * 8, rdt, f);
+        }
+        if (lane == 0) a.ring_a[unit * L + p] = sa[L];
       }
     } else {
       if (wr && isK) sDt[rrow] = d_t;
