@@ -15,7 +15,7 @@ static LaunchFn find_mamba2_bf16_inputs(int d_v, int d_k, int ckpt_dtype) {
   using RT = __nv_bfloat16;
   if (ckpt_dtype == kF32) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, float, 2, true>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, float, 2, true, true>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1>;
   } else if (ckpt_dtype == kF16) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, __half, RT, 2, 1>;

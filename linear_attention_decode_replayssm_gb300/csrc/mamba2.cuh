@@ -62,13 +62,15 @@ __host__ __device__ inline M2Rec m2_rec(int DV, int DK, int rec_es, int L) {
   s.q = o;    o = align128(o + DK * rec_es);
   s.a = o;    o = align128(o + L * 4);             // decays of records 0..p
   s.meta = o; o = align128(o + 16);                // slot, p, flush, status
-  s.scr = o;  o = align128(o + (2 * L + DV + 4) * 4);  // w_j, k_j.q, row dots, gamma
+  s.scr = o;  o = align128(o + (2 * L + 2 * DV + 4) * 4);  // w_j, k_j.q, row dots, gamma, window term
   s.bytes = o;
   return s;
 }
 
 // barriers full/rec_empty[nsr], ck_empty[nsc] and the abort flag
 __host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(8 * (2 * nsr + nsc) + 16); }
+// with a window warp: one more barrier per record slot (window terms ready)
+__host__ __device__ inline uint32_t m2_head_ww(int nsr, int nsc) { return align128(8 * (3 * nsr + nsc) + 16); }
 
 
 // LMAX bounds the buffer length at compile time (L <= LMAX): loops over a
@@ -81,8 +83,15 @@ __host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(
 // CPR: 16-byte checkpoint chunks a consumer lane holds per state row; its
 // chunks are cv, cv + G, cv + 2G, ... so that a warp's loads of one chunk
 // index cover whole 128-byte lines of the row.
-template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP, int CPR>
-__global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
+// WW: a window warp computes, for each record slot as it lands, everything
+// that does not touch the checkpoint -- the weights w_j and gamma, the dots
+// k_j . q and the window term sum_j w_j (k_j . q) v_j of every state row --
+// and signals the consumers on a second barrier.  The consumer warps then
+// need no named barrier: a state row never leaves its warp.
+template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP, int CPR,
+          bool WW>
+__global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
+    mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr bool TWO = !std::is_same<TC, TL>::value;
   constexpr int E = V::E;
@@ -93,7 +102,8 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   constexpr int VPT = DV / RPP;      // state rows per consumer thread
   constexpr int RDT = Rec<RT>::kDtype;
   constexpr int RES = (int)sizeof(RT);
-  constexpr int PROD = NGRP * NCW;   // warp index of the producer
+  constexpr int WINW = NGRP * NCW;   // warp index of the window warp (WW)
+  constexpr int PROD = NGRP * NCW + (WW ? 1 : 0);  // warp index of the producer
   constexpr uint32_t CKB = DV * DK * (uint32_t)sizeof(TC);
   constexpr uint32_t CKB_LP = DV * DK * (uint32_t)sizeof(TL);
   static_assert(!TWO || (E == 4 && sizeof(TL) == 2), "read copy: 16-bit elements under an fp32 checkpoint");
@@ -107,20 +117,29 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // per record slot: all bytes of a unit landed
   uint64_t *rec_empty = full + nsr;                     // per record slot: the unit is done
   uint64_t *ck_empty = rec_empty + nsr;                 // per checkpoint slot: consumers hold it in registers
-  int *s_abort = reinterpret_cast<int *>(ck_empty + nsc);
+  uint64_t *ready = ck_empty + nsc;                     // per record slot: window terms written (WW)
+  int *s_abort = reinterpret_cast<int *>(ready + (WW ? nsr : 0));
   const int L = a.L;
   const M2Rec lay = m2_rec(DV, DK, RES, L);
-  unsigned char *ck_slots = smem + m2_head(nsr, nsc);
+  unsigned char *ck_slots = smem + (WW ? m2_head_ww(nsr, nsc) : m2_head(nsr, nsc));
   unsigned char *rec_slots = ck_slots + (size_t)nsc * CKB;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_units = a.B * a.H;
   const int stride = gridDim.x;
+  // a wait that ran out: flag every warp to stop and report it
+  auto fail = [&]() {
+    if (lane == 0) {
+      *(volatile int *)s_abort = 1;
+      report(a.dev_err, kDerrTimeout);
+    }
+  };
 
   if (tid == 0) {
     for (int s = 0; s < nsr; ++s) {
       mbar_init(&full[s], 33);       // 32 producer-lane cp.async arrivals + lane 0 (+ bulk bytes)
-      mbar_init(&rec_empty[s], NC);  // every thread of the consuming group
+      mbar_init(&rec_empty[s], NC + (WW ? 32 : 0));  // every thread of the consuming group (+ window warp)
+      if (WW) mbar_init(&ready[s], 32);
     }
     for (int c = 0; c < nsc; ++c) mbar_init(&ck_empty[c], NC);
     *s_abort = 0;
@@ -166,7 +185,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
           }
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w || *(volatile int *)s_abort) {
-            if (lane == 0) *(volatile int *)s_abort = 1;
+            fail();
             ok = false;
             break;
           }
@@ -265,6 +284,109 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
     return;
   }
 
+  if constexpr (WW) {
+    if (warp == WINW) {
+      // --------------------------------------------------------------- window
+      // every unit of the CTA in order: weights w_j and gamma; on non-flush
+      // units also c_j = w_j (k_j . q) and the window term y = sum_j c_j v_j
+      constexpr int RPL = (DV + 31) / 32;  // state rows per lane of the window term
+      int s = 0;
+      uint32_t ph = 0;
+      for (int it = 0;; ++it) {
+        if (it && ++s == nsr) {
+          s = 0;
+          ph ^= 1u;
+        }
+        if (blockIdx.x + it * stride >= n_units) break;
+        const bool w = mbar_wait(&full[s], ph);
+        if (!__all_sync(0xffffffffu, w) || *(volatile int *)s_abort) {
+          fail();
+          break;
+        }
+        const unsigned char *st = rec_slots + (size_t)s * lay.bytes;
+        const int4 m = *reinterpret_cast<const int4 *>(st + lay.meta);
+        const int p = m.y, flush = m.z, status = m.w;
+        if (status == kStatusOk) {
+          const float *sa = reinterpret_cast<const float *>(st + lay.a);
+          float *scr = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + lay.scr);
+          float *sW = scr, *sS = scr + L, *sGam = scr + 2 * L + DV, *sY = sGam + 4;
+          const unsigned char *sk = st + lay.k, *sv = st + lay.v;
+          // w_j = product of the decays after record j, gamma = product of all
+          float x0 = lane <= p ? sa[lane] : 1.f;
+          float x1 = lane + 32 <= p ? sa[lane + 32] : 1.f;
+          suffix_scan64(x0, x1, lane, [](float x, float y) { return x * y; });
+          const float n0 = __shfl_down_sync(0xffffffffu, x0, 1);
+          const float n1 = __shfl_down_sync(0xffffffffu, x1, 1);
+          const float hi0 = __shfl_sync(0xffffffffu, x1, 0);
+          const float wv0 = lane == 31 ? hi0 : n0;
+          const float wv1 = lane == 31 ? 1.f : n1;
+          if (lane <= p) sW[lane] = wv0;
+          if (LMAX > 32 && lane + 32 <= p) sW[lane + 32] = wv1;
+          if (lane == 0) sGam[0] = x0;
+          if (!flush) {
+            if constexpr (GRP) {
+              // the group's dots are in sS already
+              if (lane <= p) sS[lane] *= wv0;
+              if (LMAX > 32 && lane + 32 <= p) sS[lane + 32] *= wv1;
+            } else {
+              // k_j . q for j <= p, eight records per transposed reduction
+              float q4[4];
+              const int col = lane * 4;
+              static_assert(DK <= 128, "one 4-column chunk of q per lane");
+              if (col < DK) {
+                lds_cols<4>(st + lay.q, col, RDT, q4);
+              } else {
+                q4[0] = q4[1] = q4[2] = q4[3] = 0.f;
+              }
+#pragma unroll 1
+              for (int j0 = 0; j0 <= p; j0 += 8) {
+                float part[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                  const int j = j0 + r;
+                  float acc = 0.f;
+                  if (j <= p && col < DK) {
+                    float kk[4];
+                    lds_cols<4>(sk, j * DK + col, RDT, kk);
+                    acc = fmaf(kk[0], q4[0], fmaf(kk[1], q4[1], fmaf(kk[2], q4[2], kk[3] * q4[3])));
+                  }
+                  part[r] = acc;
+                }
+                group_reduce<8, 32>(part, lane);
+                const int j = j0 + group_reduce_index<8, 32>(lane);
+                float wj = __shfl_sync(0xffffffffu, wv0, j & 31);
+                if constexpr (LMAX > 32) {
+                  const float w1 = __shfl_sync(0xffffffffu, wv1, j & 31);
+                  if (j >= 32) wj = w1;
+                }
+                if (group_reduce_writer<8, 32>(lane) && j <= p) sS[j] = wj * part[0];
+              }
+            }
+            __syncwarp();
+            // y = sum_{j <= p} c_j v_j for this lane's state rows
+            if (lane * RPL < DV) {
+              float y[RPL];
+#pragma unroll
+              for (int e = 0; e < RPL; ++e) y[e] = 0.f;
+#pragma unroll 4
+              for (int j = 0; j <= p; ++j) {
+                const float cj = sS[j];
+#pragma unroll
+                for (int e = 0; e < RPL; ++e) y[e] = fmaf(cj, lds_elem(sv, j * DV + lane * RPL + e, RDT), y[e]);
+              }
+#pragma unroll
+              for (int e = 0; e < RPL; ++e) sY[lane * RPL + e] = y[e];
+            }
+          }
+          __syncwarp();
+        }
+        mbar_arrive(&ready[s]);
+        mbar_arrive(&rec_empty[s]);
+      }
+      return;
+    }
+  }
+
   // ------------------------------------------------------------------ consumers
   // group g takes the CTA's units g, g + NGRP, ...; each group has its own
   // named barrier, so the groups run independently of each other
@@ -297,9 +419,18 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
     }
     const int u = blockIdx.x + it * stride;
     if (u >= n_units) break;
-    if (lane == 0 && !mbar_wait(&full[s], ph)) *(volatile int *)s_abort = 1;
-    gsync();
-    if (*(volatile int *)s_abort) break;
+    if constexpr (WW) {
+      // every warp waits for itself: no named barrier in this mode
+      const bool w = mbar_wait(&full[s], ph);
+      if (!__all_sync(0xffffffffu, w) || *(volatile int *)s_abort) {
+        fail();
+        break;
+      }
+    } else {
+      if (lane == 0 && !mbar_wait(&full[s], ph)) *(volatile int *)s_abort = 1;
+      gsync();
+      if (*(volatile int *)s_abort) break;
+    }
 
     const unsigned char *st = rec_slots + (size_t)s * lay.bytes;
     const int4 m = *reinterpret_cast<const int4 *>(st + lay.meta);
@@ -315,13 +446,13 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
     const size_t unit = (size_t)slot * a.H + h;
     const float *sa = reinterpret_cast<const float *>(st + lay.a);
     float *scr = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + lay.scr);
-    float *sW = scr, *sS = scr + L, *sC = scr + 2 * L, *sGam = scr + 2 * L + DV;
+    float *sW = scr, *sS = scr + L, *sC = scr + 2 * L, *sGam = scr + 2 * L + DV, *sY = sGam + 4;
     const unsigned char *sk = st + lay.k, *sv = st + lay.v;
     const unsigned char *ck_slot = ck_slots + (size_t)c * CKB;
 
     // window weights w_j (suffix products of the decays) and gamma
     auto weights = [&]() {
-      if (lw == 0) {
+      if (!WW && lw == 0) {
         float x0 = lane <= p ? sa[lane] : 1.f;
         float x1 = lane + 32 <= p ? sa[lane + 32] : 1.f;
         suffix_scan64(x0, x1, lane, [](float x, float y) { return x * y; });
@@ -332,6 +463,11 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
         if (lane + 32 <= p) sW[lane + 32] = lane == 31 ? 1.f : n1;
         if (lane == 0) sGam[0] = x0;
       }
+    };
+    // WW: the window warp's weights and terms of this unit are in the slot
+    auto window_ready = [&]() {
+      const bool w = mbar_wait(&ready[s], ph);
+      return __all_sync(0xffffffffu, w) && !*(volatile int *)s_abort;
     };
 
     float part[VPT];
@@ -355,7 +491,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       // its 4-column chunk of q and accumulates four partial dots, and one
       // transposed reduction finishes the chunk (group-shared keys: the
       // producer brought the group's dots instead)
-      if constexpr (!GRP) {
+      if constexpr (!GRP && !WW) {
         constexpr int QPL = (DK + 127) / 128;  // 4-column chunks of q per lane
         float qq[QPL][4];
 #pragma unroll
@@ -413,13 +549,26 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
         part[r] = acc;
       }
       group_reduce<VPT, G>(part, lane);
-      if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
-      gsync();
+      if constexpr (WW) {
+        // o = gamma c + the window warp's sum_j w_j s_j v_j, by the lane that
+        // finished the row
+        if (!window_ready()) {
+          fail();
+          break;
+        }
+        if (group_reduce_writer<VPT, G>(lane)) {
+          const int row = row0 + group_reduce_index<VPT, G>(lane) * RPP;
+          orow[row] = fmaf(sGam[0], part[0], sY[row]);
+        }
+      } else {
+        if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
+        gsync();
+      }
 
       // o = gamma c + sum_j w_j s_j v_j, by one warp: a lane covers 8 output
       // rows (one 16-byte load of a v record) for every OG-th record, then
       // lanes sharing rows add up; the other warps append the record
-      if (lw == 0) {
+      if (!WW && lw == 0) {
         constexpr int RG = DV / 8;   // 8-row groups
         constexpr int OG = 32 / RG;  // record groups
         static_assert(DV % 8 == 0 && 32 % RG == 0 && OG >= 1, "bad output layout");
@@ -452,7 +601,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       // append the current record (k, v verbatim, alpha) at ring slot p; a
       // group-shared key was appended by the group's dot kernel
       constexpr int KCH = GRP ? 0 : DK * RES / 16, VCH = DV * RES / 16;
-      constexpr int APP0 = NCW > 1 ? 32 : 0;  // warp 0 is busy with the output
+      constexpr int APP0 = (NCW > 1 && !WW) ? 32 : 0;  // warp 0 is busy with the output
       for (int c = ctid - APP0; c >= 0 && c < KCH + VCH; c += NC - APP0) {
         if (c < KCH) {
           const uint4 x = reinterpret_cast<const uint4 *>(sk + (size_t)p * DK * RES)[c];
@@ -480,8 +629,15 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
         xb[bk] = *reinterpret_cast<const float4 *>(ck_slot + ((size_t)rB * DK + 16 * bk + 4 * t4) * 4);
       }
       mbar_arrive(&ck_empty[c]);
-      weights();
-      gsync();  // weights ready
+      if constexpr (WW) {
+        if (!window_ready()) {
+          fail();
+          break;
+        }
+      } else {
+        weights();
+        gsync();  // weights ready
+      }
       const float gam = sGam[0];
 #pragma unroll
       for (int bk = 0; bk < NB; ++bk) {
@@ -554,12 +710,19 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       oB += __shfl_xor_sync(0xffffffffu, oB, 1);
       oA += __shfl_xor_sync(0xffffffffu, oA, 2);
       oB += __shfl_xor_sync(0xffffffffu, oB, 2);
-      if (t4 == 0) {
-        sC[rA] = oA;
-        sC[rB] = oB;
+      if constexpr (WW) {
+        if (t4 == 0) {
+          orow[rA] = oA;
+          orow[rB] = oB;
+        }
+      } else {
+        if (t4 == 0) {
+          sC[rA] = oA;
+          sC[rB] = oB;
+        }
+        gsync();
+        for (int i = ctid; i < DV; i += NC) orow[i] = sC[i];
       }
-      gsync();
-      for (int i = ctid; i < DV; i += NC) orow[i] = sC[i];
     } else {
       uint4 raw[VPT][CPR];
 #pragma unroll
@@ -572,7 +735,14 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
       float qv[CPR][E];
 #pragma unroll
       for (int i = 0; i < CPR; ++i) lds_cols<E>(st + lay.q, (cv + G * i) * E, RDT, qv[i]);
-      gsync();  // weights ready
+      if constexpr (WW) {
+        if (!window_ready()) {
+          fail();
+          break;
+        }
+      } else {
+        gsync();  // weights ready
+      }
       const float gam = sGam[0];
       TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK);
       float f[VPT][CPR][E];
@@ -618,9 +788,13 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 32, 2) mamba2_replay_kernel(
         part[r] = acc;
       }
       group_reduce<VPT, G>(part, lane);
-      if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
-      gsync();
-      for (int i = ctid; i < DV; i += NC) orow[i] = sC[i];
+      if constexpr (WW) {
+        if (group_reduce_writer<VPT, G>(lane)) orow[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
+      } else {
+        if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
+        gsync();
+        for (int i = ctid; i < DV; i += NC) orow[i] = sC[i];
+      }
     }
     mbar_arrive(&rec_empty[s]);
   }
@@ -695,19 +869,20 @@ __global__ void __launch_bounds__(256) mamba2_group_kq_kernel(const KArgs a) {
 }
 
 template <int DV, int DK, typename TC, typename TL, typename RT, int NCW, int NGRP, int LMAX, bool GRP = false,
-          int CPR = 1>
+          int CPR = 1, bool WW = false>
 static cudaError_t launch_mamba2_l(const KArgs &a, cudaStream_t s) {
   if (GRP) {
     mamba2_group_kq_kernel<DK, RT><<<(unsigned)(((size_t)a.B * a.n_groups + 7) / 8), 256, 0, s>>>(a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto kern = mamba2_replay_kernel<DV, DK, TC, TL, RT, NCW, NGRP, LMAX, GRP, CPR>;
-  constexpr int threads = NGRP * NCW * 32 + 32;
+  auto kern = mamba2_replay_kernel<DV, DK, TC, TL, RT, NCW, NGRP, LMAX, GRP, CPR, WW>;
+  constexpr int threads = NGRP * NCW * 32 + (WW ? 64 : 32);
   const size_t ckb = (size_t)DV * DK * sizeof(TC);
   const size_t rb = m2_rec(DV, DK, (int)sizeof(RT), a.L).bytes;
   RingPlan plan;
-  cudaError_t e = plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, m2_head, a.B * a.H, &plan);
+  cudaError_t e = plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, WW ? m2_head_ww : m2_head,
+                             a.B * a.H, &plan);
   if (e != cudaSuccess) return e;
   kern<<<plan.grid, threads, plan.smem, s>>>(a, plan.nsr, plan.nsc);
   return cudaGetLastError();
@@ -716,19 +891,20 @@ static cudaError_t launch_mamba2_l(const KArgs &a, cudaStream_t s) {
 // the common short windows get a kernel unrolled for L <= 16
 // FINE: the window bound is the next of 8, 16, 32 or 64 above L (fewer
 // predicated-off iterations for short and long windows), else 16 or 64
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, typename TL = TC, int CPR = 1, bool FINE = false>
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, typename TL = TC, int CPR = 1, bool FINE = false,
+          bool WW = false>
 static cudaError_t launch_mamba2(const KArgs &a, cudaStream_t s) {
-  if (FINE && a.L <= 8) return launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 8, false, CPR>(a, s);
-  if (a.L <= 16) return launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 16, false, CPR>(a, s);
-  if (FINE && a.L <= 32) return launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 32, false, CPR>(a, s);
-  return launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, RS_MAX_L, false, CPR>(a, s);
+  if (FINE && a.L <= 8) return launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 8, false, CPR, WW>(a, s);
+  if (a.L <= 16) return launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 16, false, CPR, WW>(a, s);
+  if (FINE && a.L <= 32) return launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, 32, false, CPR, WW>(a, s);
+  return launch_mamba2_l<DV, DK, TC, TL, RT, NCW, NGRP, RS_MAX_L, false, CPR, WW>(a, s);
 }
 
 // group-shared keys: the group dot kernel, then the decode
-template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, int CPR = 1>
+template <int DV, int DK, typename TC, typename RT, int NCW, int NGRP, int CPR = 1, bool WW = false>
 static cudaError_t launch_mamba2_grp(const KArgs &a, cudaStream_t s) {
-  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, 16, true, CPR>(a, s)
-                   : launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, RS_MAX_L, true, CPR>(a, s);
+  return a.L <= 16 ? launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, 16, true, CPR, WW>(a, s)
+                   : launch_mamba2_l<DV, DK, TC, TC, RT, NCW, NGRP, RS_MAX_L, true, CPR, WW>(a, s);
 }
 
 }  // namespace rs

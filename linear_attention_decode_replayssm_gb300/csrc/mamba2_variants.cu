@@ -8,11 +8,11 @@ template <typename RT>
 static LaunchFn read_copy_t(int d_v, int d_k, int lp_dtype) {
   if (lp_dtype == kF16) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1, __half>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __half, 4>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __half, 4, false, true>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1, __half>;
   } else if (lp_dtype == kBF16) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1, __nv_bfloat16>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __nv_bfloat16, 4>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __nv_bfloat16, 4, false, true>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1, __nv_bfloat16>;
   }
   return nullptr;
@@ -22,7 +22,7 @@ template <typename RT>
 static LaunchFn grouped_t(int d_v, int d_k, int ckpt_dtype) {
   if (ckpt_dtype == kF32) {
     if (d_v == 16 && d_k == 32) return launch_mamba2_grp<16, 32, float, RT, 4, 1>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2_grp<64, 128, float, RT, 4, 2>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2_grp<64, 128, float, RT, 4, 2, 1, true>;
   } else if (ckpt_dtype == kF16) {
     if (d_v == 64 && d_k == 128) return launch_mamba2_grp<64, 128, __half, RT, 8, 1>;
   }
