@@ -67,10 +67,11 @@ __host__ __device__ inline M2Rec m2_rec(int DV, int DK, int rec_es, int L) {
   return s;
 }
 
-// barriers full/rec_empty[nsr], ck_empty[nsc] and the abort flag
-__host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(8 * (2 * nsr + nsc) + 16); }
+// barriers full/rec_empty[nsr], ck_empty[2 nsc] (a read-copy kernel splits
+// each checkpoint slot into two half-slots) and the abort flag
+__host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(8 * (2 * nsr + 2 * nsc) + 16); }
 // with a window warp: one more barrier per record slot (window terms ready)
-__host__ __device__ inline uint32_t m2_head_ww(int nsr, int nsc) { return align128(8 * (3 * nsr + nsc) + 16); }
+__host__ __device__ inline uint32_t m2_head_ww(int nsr, int nsc) { return align128(8 * (3 * nsr + 2 * nsc) + 16); }
 
 
 // LMAX bounds the buffer length at compile time (L <= LMAX): loops over a
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // per record slot: all bytes of a unit landed
   uint64_t *rec_empty = full + nsr;                     // per record slot: the unit is done
   uint64_t *ck_empty = rec_empty + nsr;                 // per checkpoint slot: consumers hold it in registers
-  uint64_t *ready = ck_empty + nsc;                     // per record slot: window terms written (WW)
+  uint64_t *ready = ck_empty + 2 * nsc;                 // per record slot: window terms written (WW)
   int *s_abort = reinterpret_cast<int *>(ready + (WW ? nsr : 0));
   const int L = a.L;
   const M2Rec lay = m2_rec(DV, DK, RES, L);
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
       mbar_init(&rec_empty[s], NC + (WW ? 32 : 0));  // every thread of the consuming group (+ window warp)
       if (WW) mbar_init(&ready[s], 32);
     }
-    for (int c = 0; c < nsc; ++c) mbar_init(&ck_empty[c], NC);
+    for (int c = 0; c < (TWO ? 2 * nsc : nsc); ++c) mbar_init(&ck_empty[c], NC);
     *s_abort = 0;
     mbar_init_fence();
   }
@@ -165,6 +166,13 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
     int c_sl, c_wp, c_fl;
     int ps = 0, pc = 0;         // record and checkpoint slot of unit `it`
     uint32_t phs = 0, phc = 0;  // parity of it / nsr and it / nsc
+    // read-copy kernels: a ring of 2 nsc half-slots (CKB_LP bytes each); a
+    // non-flush row's read copy takes one, a flush row's fp32 rows take two
+    // (rows 0 .. DV/2 - 1, then the rest); per half-slot: used yet, and the
+    // parity of its use count
+    const int nhs = 2 * nsc;
+    int hc = 0;
+    uint32_t hused = 0, hpar = 0;
     fetch(blockIdx.x, c_sl, c_wp, c_fl);
     bool ok = true;
     for (int ub = blockIdx.x; ok && ub < n_units; ub += 32 * stride) {
@@ -177,11 +185,27 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
         const int p = __shfl_sync(0xffffffffu, c_wp, j);
         const int fl = __shfl_sync(0xffffffffu, c_fl, j);
         const int s = ps, c = pc;
-        if (it >= nsr || it >= nsc) {
+        int h0 = -1, h1 = -1;  // half-slots of this unit (read-copy kernels)
+        if constexpr (TWO) {
+          if (slot >= 0 && slot < a.num_slots && p >= 0 && p < L) {
+            h0 = hc;
+            hc = hc + 1 == nhs ? 0 : hc + 1;
+            if (fl) {
+              h1 = hc;
+              hc = hc + 1 == nhs ? 0 : hc + 1;
+            }
+          }
+        }
+        if (it >= nsr || (TWO ? h0 >= 0 : it >= nsc)) {
           int w = 1;
           if (lane == 0) {
             if (it >= nsr) w = mbar_wait(&rec_empty[s], phs ^ 1u) ? 1 : 0;
-            if (w && it >= nsc) w = mbar_wait(&ck_empty[c], phc ^ 1u) ? 1 : 0;
+            if constexpr (TWO) {
+              if (w && h0 >= 0 && ((hused >> h0) & 1u)) w = mbar_wait(&ck_empty[h0], ((hpar >> h0) & 1u) ^ 1u) ? 1 : 0;
+              if (w && h1 >= 0 && ((hused >> h1) & 1u)) w = mbar_wait(&ck_empty[h1], ((hpar >> h1) & 1u) ^ 1u) ? 1 : 0;
+            } else {
+              if (w && it >= nsc) w = mbar_wait(&ck_empty[c], phc ^ 1u) ? 1 : 0;
+            }
           }
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w || *(volatile int *)s_abort) {
@@ -191,6 +215,16 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
           }
         }
         __syncwarp();
+        if constexpr (TWO) {
+          if (h0 >= 0) {
+            hused |= 1u << h0;
+            hpar ^= 1u << h0;
+          }
+          if (h1 >= 0) {
+            hused |= 1u << h1;
+            hpar ^= 1u << h1;
+          }
+        }
         const int b = u / a.H, h = u - (u / a.H) * a.H;
         const int status = slot < 0 ? kStatusPad
                            : slot >= a.num_slots ? kStatusBadSlot
@@ -207,13 +241,24 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
           const size_t unit = (size_t)slot * a.H + h;
           if (lane == 0) {
             meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
-            // a two-precision non-flush row reads only the read copy
-            const bool lp = TWO && !fl;
-            const uint32_t nb = lp ? CKB_LP : CKB;
-            const void *src = lp ? static_cast<const void *>(static_cast<const TL *>(a.ckpt_lp) + unit * (DV * DK))
-                                 : static_cast<const void *>(static_cast<const TC *>(a.ckpt) + unit * (DV * DK));
-            mbar_expect_tx(&full[s], nb);
-            bulk_load(ck_slots + (size_t)c * CKB, src, nb, &full[s], pol_stream);
+            meta[4] = h0; meta[5] = h1;
+            const TC *ck32 = static_cast<const TC *>(a.ckpt) + unit * (DV * DK);
+            if constexpr (TWO) {
+              if (!fl) {
+                // a two-precision non-flush row reads only the read copy
+                mbar_expect_tx(&full[s], CKB_LP);
+                bulk_load(ck_slots + (size_t)h0 * CKB_LP, static_cast<const TL *>(a.ckpt_lp) + unit * (DV * DK),
+                          CKB_LP, &full[s], pol_stream);
+              } else {
+                static_assert(CKB == 2 * CKB_LP, "an fp32 checkpoint fills two half-slots");
+                mbar_expect_tx(&full[s], CKB);
+                bulk_load(ck_slots + (size_t)h0 * CKB_LP, ck32, CKB_LP, &full[s], pol_stream);
+                bulk_load(ck_slots + (size_t)h1 * CKB_LP, ck32 + (DV / 2) * DK, CKB_LP, &full[s], pol_stream);
+              }
+            } else {
+              mbar_expect_tx(&full[s], CKB);
+              bulk_load(ck_slots + (size_t)c * CKB, ck32, CKB, &full[s], pol_stream);
+            }
           }
           constexpr uint32_t kb = DK * RES, vb = DV * RES;
           constexpr int KC = kb / 16, VC = vb / 16;  // 16-byte chunks per k / v record
@@ -261,6 +306,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
           if (lane == 31) cp_async4(sa + p, a.alpha + (size_t)b * a.H + h);
         } else if (lane == 0) {
           meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
+          meta[4] = -1; meta[5] = -1;
         }
         if (lane == 0) mbar_arrive(&full[s]);  // releases the meta words
         cp_async_arrive(&full[s]);
@@ -439,7 +485,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
     if (status != kStatusOk) {
       for (int i = ctid; i < DV; i += NC) orow[i] = 0.f;
       if (ctid == 0 && status != kStatusPad) report(a.dev_err, status == kStatusBadSlot ? 1 : 2);
-      mbar_arrive(&ck_empty[c]);
+      if (!TWO) mbar_arrive(&ck_empty[c]);  // a read-copy kernel gave the unit no half-slot
       mbar_arrive(&rec_empty[s]);
       continue;
     }
@@ -448,7 +494,29 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
     float *scr = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + lay.scr);
     float *sW = scr, *sS = scr + L, *sC = scr + 2 * L, *sGam = scr + 2 * L + DV, *sY = sGam + 4;
     const unsigned char *sk = st + lay.k, *sv = st + lay.v;
-    const unsigned char *ck_slot = ck_slots + (size_t)c * CKB;
+    // the unit's checkpoint slot; a read-copy kernel names its half-slot(s)
+    // in the metadata: the read copy in one, or the fp32 rows 0 .. DV/2 - 1
+    // and DV/2 .. DV - 1 of a flush row in two
+    int hs0 = c, hs1 = -1;
+    if constexpr (TWO) {
+      const int2 hm = *reinterpret_cast<const int2 *>(st + lay.meta + 16);
+      hs0 = hm.x;
+      hs1 = hm.y;
+    }
+    const unsigned char *ck_slot = ck_slots + (size_t)hs0 * (TWO ? CKB_LP : CKB);
+    // fp32 state row r of a flush row
+    auto ck_row = [&](int r) -> const unsigned char * {
+      if constexpr (TWO) {
+        return r < DV / 2 ? ck_slot + (size_t)r * DK * sizeof(TC)
+                          : ck_slots + (size_t)hs1 * CKB_LP + (size_t)(r - DV / 2) * DK * sizeof(TC);
+      } else {
+        return ck_slot + (size_t)r * DK * sizeof(TC);
+      }
+    };
+    auto release_ck = [&]() {
+      mbar_arrive(&ck_empty[hs0]);
+      if (TWO && hs1 >= 0) mbar_arrive(&ck_empty[hs1]);
+    };
 
     // window weights w_j (suffix products of the decays) and gamma
     auto weights = [&]() {
@@ -482,7 +550,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
 #pragma unroll
         for (int i = 0; i < CPR; ++i)
           raw[r][i] = reinterpret_cast<const Raw *>(ck_slot)[(row0 + r * RPP) * NCH + cv + G * i];
-      mbar_arrive(&ck_empty[c]);
+      release_ck();
       weights();
       float qv[CPR][E];
 #pragma unroll
@@ -625,10 +693,10 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
       float4 xa[NB], xb[NB];
 #pragma unroll
       for (int bk = 0; bk < NB; ++bk) {
-        xa[bk] = *reinterpret_cast<const float4 *>(ck_slot + ((size_t)rA * DK + 16 * bk + 4 * t4) * 4);
-        xb[bk] = *reinterpret_cast<const float4 *>(ck_slot + ((size_t)rB * DK + 16 * bk + 4 * t4) * 4);
+        xa[bk] = *reinterpret_cast<const float4 *>(ck_row(rA) + (16 * bk + 4 * t4) * 4);
+        xb[bk] = *reinterpret_cast<const float4 *>(ck_row(rB) + (16 * bk + 4 * t4) * 4);
       }
-      mbar_arrive(&ck_empty[c]);
+      release_ck();
       if constexpr (WW) {
         if (!window_ready()) {
           fail();
@@ -729,8 +797,8 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
       for (int r = 0; r < VPT; ++r)
 #pragma unroll
         for (int i = 0; i < CPR; ++i)
-          raw[r][i] = reinterpret_cast<const uint4 *>(ck_slot)[(row0 + r * RPP) * NCH + cv + G * i];
-      mbar_arrive(&ck_empty[c]);
+          raw[r][i] = reinterpret_cast<const uint4 *>(ck_row(row0 + r * RPP))[cv + G * i];
+      release_ck();
       weights();
       float qv[CPR][E];
 #pragma unroll
