@@ -20,16 +20,21 @@
 // copy (cp.async.bulk, completion counted on an mbarrier) and its ring
 // records, this token's k, v, q and the decays into a record slot with
 // per-lane cp.async.  It prefetches the per-row slot, cursor and flag 32
-// units ahead, so no dependent global load sits on the streaming path.
+// units ahead, so no dependent global load sits on the streaming path.  A
+// read-copy kernel splits each checkpoint slot in two: a non-flush row's
+// half-size read copy fills one half-slot, a flush row's fp32 rows two.
 // Consumer groups (two groups of four warps for the 64 x 128 fp32 layer)
 // take alternate units: a group waits for its unit, takes its share of the
 // checkpoint into registers (freeing that slot for the next load at once),
 // computes from the record slot and releases it.  The step is bound by
 // instruction issue as much as by bandwidth, so the per-warp fixed costs of a
-// unit are paid by four warps rather than eight.  The units a CTA owns are
-// strided across the batch, so the ~1/L flush rows (which also write their
-// state) spread evenly over the CTAs.  Every wait is bounded: on a timeout
-// the kernel reports RS_DERR_TIMEOUT, drains its own copies and returns.
+// unit are paid by four warps rather than eight; with the window warp (WW)
+// the window's weights, key dots and per-row sums move off the consumers
+// entirely, and the consumer warps run without a named barrier.  The units a
+// CTA owns are strided across the batch, so the ~1/L flush rows (which also
+// write their state) spread evenly over the CTAs.  Every wait is bounded: on
+// a timeout the kernel reports RS_DERR_TIMEOUT, drains its own copies and
+// returns.
 // The per-step products stay on the CUDA cores (a bandwidth-bound GEMV, about
 // 0.6 FLOP/byte); the flush fold of an fp32 checkpoint, a rank-(p+1) update of
 // the whole state held in registers, runs on the tensor cores.
