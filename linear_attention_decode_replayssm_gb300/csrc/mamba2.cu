@@ -11,6 +11,9 @@ LaunchFn find_mamba2_read_copy(int d_v, int d_k, int lp_dtype, int in_dtype);  /
 LaunchFn find_mamba2_grouped(int d_v, int d_k, int ckpt_dtype, int in_dtype);  // mamba2_variants.cu
 LaunchFn find_mamba2_f32_inputs(int d_v, int d_k, int ckpt_dtype);             // mamba2_f32in.cu
 
+// launch_mamba2<d_v, d_k, checkpoint type, input type, consumer warps per
+// group, groups, read-copy type, chunks per lane and row, fine window bounds,
+// window warp>; the 64 x 128 fp32 layer runs with the window warp
 static LaunchFn find_mamba2_bf16_inputs(int d_v, int d_k, int ckpt_dtype) {
   using RT = __nv_bfloat16;
   if (ckpt_dtype == kF32) {

@@ -4,6 +4,8 @@
 
 namespace rs {
 
+// template arguments as in mamba2.cu; the 64 x 128 layer's read-copy and
+// grouped-key kernels run with the window warp
 template <typename RT>
 static LaunchFn read_copy_t(int d_v, int d_k, int lp_dtype) {
   if (lp_dtype == kF16) {
