@@ -40,8 +40,10 @@
  * Memory and ownership: every pointer in rs_step_args is a DEVICE pointer
  * owned by the caller (PyTorch allocates and frees everything).  The library
  * never allocates, frees or synchronises, and never reads device memory on
- * the host, so a call is asynchronous on `stream` and can be captured in a
- * CUDA graph ([PR48792] §CUDA graphs and continuous batching).  Checkpoint and
+ * the host, so a call is asynchronous on `stream`, and the decode,
+ * verification, commit and materialisation calls can be captured in a CUDA
+ * graph ([PR48792] §CUDA graphs and continuous batching).  (The no-alloc
+ * decode variant below has its own set-up rule.)  Checkpoint and
  * rings are updated in place.  Two rows of one call must not name the same
  * slot (their updates would race).
  *
@@ -324,20 +326,39 @@ int replayssm_spec_commit(const int32_t *committed, const uint8_t *is_flush, con
 int replayssm_decode_mamba2(const rs_step_args *args, rs_stream_t stream);
 
 /* Capacity, in floats, of the library-owned group-dot scratch that
- * replayssm_decode_mamba2_noalloc uses (B * n_groups * L must fit). */
+ * replayssm_decode_mamba2_noalloc uses: B * n_groups * L must not exceed it
+ * (4 MiB; with 8 groups and L = 16 that is up to 8192 rows). */
 #define RS_NOALLOC_KQ_FLOATS (1 << 20)
 
 /*
- * replayssm_decode_mamba2 for callers that keep no scratch buffer: with
- * group-shared keys (n_groups > 0) the group dots go to a device array the
- * library owns (one per device, RS_NOALLOC_KQ_FLOATS floats, created with
- * the library's module; its address is looked up once per device), so the
- * call allocates nothing.  kq_scratch must be NULL.  Calls that use the
- * library scratch must not run concurrently on one device (different
- * streams, or graphs replayed side by side, would share it).  With
- * n_groups == 0 this is replayssm_decode_mamba2.  Returns RS_EINVAL when
- * kq_scratch is set or B * n_groups * L exceeds the capacity; otherwise as
- * replayssm_decode_mamba2.
+ * replayssm_decode_mamba2 for callers that cannot allocate device memory.
+ * The pages have no counterpart: this entry point exists for the callers of
+ * this library, not for the method.  The group-shared-key decode needs
+ * B * n_groups * L floats of scratch for the group dots k_j . q_t.  Some
+ * callers cannot provide it: a plugin inside a serving engine that owns all
+ * device memory through its own pool and offers plugins no way to allocate,
+ * or a decode loop that must never call cudaMalloc, which can synchronise
+ * the device and stall every other stream.  Here the scratch is a
+ * fixed-size device array inside the library (RS_NOALLOC_KQ_FLOATS floats,
+ * 4 MiB, created when the library's module loads on a device and held by
+ * every device that loads it until the process exits); the caller still
+ * passes all inputs and outputs, and the call allocates and frees nothing.
+ *
+ * Set-up: the first call on a device (and the first call after the device's
+ * context was reset) looks up the array's device address on the current
+ * device, with cudaGetSymbolAddress.  Make that first call before any stream
+ * capture begins.  Later calls reuse the address.
+ *
+ * Sharing: every call uses the same array, which keeps what the last call
+ * wrote.  Nothing in it needs clearing: each entry a call reads was written
+ * earlier in that same call.  Calls whose kernels overlap on the GPU (on
+ * different streams, or in graphs replayed side by side) race on the array
+ * and give wrong results: order them.
+ *
+ * kq_scratch must be NULL.  With n_groups == 0 no scratch is needed and this
+ * is replayssm_decode_mamba2.  Returns RS_EINVAL when kq_scratch is set or
+ * B * n_groups * L > RS_NOALLOC_KQ_FLOATS (nothing launched), RS_ECUDA when
+ * the address lookup fails, otherwise what replayssm_decode_mamba2 returns.
  */
 int replayssm_decode_mamba2_noalloc(const rs_step_args *args, rs_stream_t stream);
 

@@ -351,8 +351,11 @@ def replayssm_decode_mamba2(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos
 
 def replayssm_decode_mamba2_noalloc(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos, is_flush, v, k, q,
                                     alpha, out, dev_err=None, stream=None):
-    """As ``replayssm_decode_mamba2``; group-shared keys use the library's
-    own scratch (no caller buffer)."""
+    """As ``replayssm_decode_mamba2``, for callers that cannot allocate device
+    memory: group-shared keys use a fixed-size device array held by the
+    library (B * G * L <= RS_NOALLOC_KQ_FLOATS) instead of caller scratch.
+    The first call on a device looks up that array's address, so make it
+    before any stream capture; calls that overlap on the GPU race on it."""
     args = _fill(StepArgs(), variant=RS_MAMBA2, ckpt=ckpt, slot_idx=slot_idx, v=v, k=k, q=q, alpha=alpha,
                  out=out, ring_v=ring_v, ring_k=ring_k, ring_a=ring_a, write_pos=write_pos,
                  is_flush=is_flush, dev_err=dev_err, library_scratch=True)

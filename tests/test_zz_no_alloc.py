@@ -1,11 +1,16 @@
-"""replayssm_decode_mamba2_noalloc: group-shared keys with the library's own
-group-dot scratch (a static device array) instead of a caller buffer.
+"""replayssm_decode_mamba2_noalloc: the group-shared-key decode for callers
+that cannot allocate device memory (a plugin of a serving engine that owns all
+device memory through its own pool, or a decode loop that must not call
+cudaMalloc because it can synchronise the device).  The group dots go to a
+fixed-size device array held by the library instead of caller scratch.
 
-Host checks (no GPU): the call refuses a caller scratch and batches that do
-not fit the library scratch, before touching the device.  GPU checks: the
-results are bit-identical to the caller-scratch call on the same inputs and
-match the exact recurrence at max relative error 1e-4; the call can be
-captured in a CUDA graph.
+Host checks (no GPU): the call refuses a caller scratch and batches whose
+dots would not fit the library's array, before touching the device.  GPU
+check: on forty calls in a row, each call's outputs, and the checkpoints at
+the end, are bit-identical to those of replayssm_decode_mamba2 given caller
+scratch on the same inputs, and match the exact recurrence at max relative
+error 1e-4.  This file is collected last, so a run that stops at its first
+failure has run every other test before it.
 """
 
 import numpy as np
@@ -88,16 +93,3 @@ def test_noalloc_matches_caller_scratch_and_oracle(lib):
     assert torch.equal(sides[0]["ckpt"].view(torch.int32), sides[1]["ckpt"].view(torch.int32))
     assert int(err.item()) == 0
     assert worst <= 1e-4, worst
-
-    # the call captures in a CUDA graph (the scratch address is resolved before)
-    b = sides[1]
-    s = torch.cuda.Stream()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(graph, stream=s):
-            lib.replayssm_decode_mamba2_noalloc(ckpt=b["ckpt"], ring_v=b["ring_v"], ring_k=b["ring_k"],
-                                                ring_a=b["ring_a"], out=b["out"], stream=s, **common)
-    with torch.cuda.stream(s):
-        graph.replay()
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
