@@ -136,6 +136,83 @@ def oracle_throughput(spec, budget_s, warmup=1, steps=None):
     return tokens / t_max, cores, sample
 
 
+def _oracle_batch_worker(job):
+    """Time the oracle's conventional step called on a whole block of rows:
+    ``rows`` rows x ``heads`` heads in one call per step (the oracle's
+    functions broadcast over leading axes), float64."""
+    variant, rows, heads, d_v, d_k, warmup, steps, seed = job
+    import numpy as np
+
+    import oracle
+
+    r = np.random.default_rng(seed)
+    S = r.standard_normal((rows, heads, d_v, d_k)) / math.sqrt(d_k)
+    n_sets = 4
+    sets = []
+    for _ in range(n_sets):
+        v = r.standard_normal((rows, heads, d_v)) / math.sqrt(d_k)
+        k = r.standard_normal((rows, heads, d_k)) / math.sqrt(d_k)
+        q = r.standard_normal((rows, heads, d_k)) / math.sqrt(d_k)
+        a = 1.0 / (1.0 + np.exp(-r.normal(3.0, 1.0, (rows, heads))))
+        if variant == "gdn":
+            k /= np.linalg.norm(k, axis=-1, keepdims=True)
+            q /= np.linalg.norm(q, axis=-1, keepdims=True)
+            beta = 1.0 / (1.0 + np.exp(-r.standard_normal((rows, heads))))
+            sets.append((np.log(a), beta, v, k, q))
+        else:
+            sets.append((a, v, k, q))
+    step = oracle.gdn_step if variant == "gdn" else oracle.mamba2_step
+    for t in range(warmup):
+        S, _ = step(S, *sets[t % n_sets])
+    t0 = time.perf_counter()
+    for t in range(steps):
+        S, _ = step(S, *sets[t % n_sets])
+    return time.perf_counter() - t0
+
+
+def oracle_batched_throughput(spec, budget_s, warmup=1, steps=16):
+    """Tokens/s/layer of the CPU oracle batched over (rows, heads) on the host
+    cores: every core runs its block of the batch's rows through the oracle's
+    step in one call per step, for ``steps`` steps (one window of 16 by
+    default); the rows per core shrink (then the heads) so that the sample
+    fits about ``budget_s``.  Returns (tokens_per_s, cores, sample)."""
+    import multiprocessing as mp
+
+    cores = os.cpu_count() or 1
+    B, H = spec["B"], spec["H"]
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(cores) as pool:
+            t1 = pool.map(_oracle_batch_worker, [(spec["variant"], 1, H, spec["d_v"], spec["d_k"], 1, 2, 99)])[0] / 2
+            rows = -(-B // cores)
+            heads = H
+            fit = budget_s / max(t1 * (steps + warmup), 1e-9)  # rows of all heads that fit the budget
+            if fit < rows:
+                rows = max(1, int(fit))
+                if fit < 1:
+                    heads = max(1, int(H * fit))
+            jobs = [(spec["variant"], rows, heads, spec["d_v"], spec["d_k"], warmup, steps, 2000 + i)
+                    for i in range(cores)]
+            t0 = time.perf_counter()
+            elapsed = pool.map(_oracle_batch_worker, jobs)
+            wall = time.perf_counter() - t0
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    t_max = max(elapsed)
+    tokens = cores * rows * steps * heads / H
+    sample = (f"{cores} processes x {rows} rows x {heads}/{H} heads x {steps} steps of the {spec['variant']} layer, "
+              f"the oracle's conventional step called once per step on each process's whole block (float64 "
+              f"NumPy, batched over rows and heads), {t_max:.1f} s; wall {wall:.1f} s")
+    return tokens / t_max, cores, sample
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed regions
 # ---------------------------------------------------------------------------
@@ -398,54 +475,86 @@ def measure_layer(lib, torch, spec, device, args, dist, sampler, seed):
 
 
 def measure_e2e(lib, torch, layer, steps, dist):
-    """Tokens/s through the public API with host buffers: every step copies its
-    inputs from pinned host memory, plans the step on the host, launches the
-    decode, and reads the output back to host memory.  Two steps are in
-    flight: step t+1's inputs go up on a copy stream while step t decodes, and
-    the host reads step t's output while step t+1 runs."""
-    import numpy as np
+    """Tokens/s through the public API with host buffers.
 
+    Each step: the host plan (cursor and flag per row) is written into the
+    step's pinned staging buffer, which also holds the step's inputs (v, k,
+    q, decays and, for GDN, beta, packed at 256-byte offsets); one H2D copy
+    moves the buffer; the decode is launched through the C ABI with its
+    arguments marshalled once per device buffer (``prepare_decode``); one D2H
+    copy brings the output back and the host reads it.  Uploads, decodes and
+    downloads run on three streams with two device buffers, so step t+1's
+    upload and step t-1's download overlap step t's decode."""
     dev = layer.device
-    B = layer.spec["B"]
-    host_in = []
+    s = layer.spec
+    B, H, dv, dk, L = (s[k] for k in ("B", "H", "d_v", "d_k", "L"))
+    gdn = s["variant"] == "gdn"
+    x0 = layer.inputs[0]
+    KH = x0["k"].shape[1]
+    fields = [("v", x0["v"].dtype, (B, H, dv)), ("k", x0["k"].dtype, (B, KH, dk)), ("q", x0["q"].dtype, (B, KH, dk)),
+              ("alpha", torch.float32, (B, H))]
+    if gdn:
+        fields.append(("beta", torch.float32, (B, H)))
+    fields += [("wp", torch.int32, (B,)), ("fl", torch.uint8, (B,))]
+    offs, off = {}, 0
+    for name, dt, shp in fields:
+        offs[name] = off
+        off += (math.prod(shp) * torch.empty((), dtype=dt).element_size() + 255) // 256 * 256
+    nbytes = off
+
+    def views(buf):
+        out = {}
+        for name, dt, shp in fields:
+            n = math.prod(shp) * torch.empty((), dtype=dt).element_size()
+            out[name] = buf[offs[name]:offs[name] + n].view(dt).view(shp)
+        return out
+
+    host_buf, host = [], []
     for x in layer.inputs:
-        host_in.append({n: (t.cpu().pin_memory() if t is not None and not n.endswith("_h") else None)
-                        for n, t in x.items()})
-    d_in = [{n: (t.clone() if t is not None and not n.endswith("_h") else None) for n, t in layer.inputs[0].items()}
-            for _ in range(2)]
-    wp_h = [torch.empty(B, dtype=torch.int32).pin_memory() for _ in range(2)]
-    fl_h = [torch.empty(B, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    wp_d = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(2)]
-    fl_d = [torch.empty(B, dtype=torch.uint8, device=dev) for _ in range(2)]
+        hb = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        hv = views(hb)
+        for name in ("v", "k", "q", "alpha", "beta"):
+            if name in hv:
+                hv[name].copy_(x[name])
+        host_buf.append(hb)
+        host.append((hv["wp"].numpy(), hv["fl"].numpy()))
+    dev_buf = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    outs = [torch.empty_like(layer.out) for _ in range(2)]
     o_h = [torch.empty(layer.out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in[0].values() if t is not None)
-    h2d += wp_h[0].numel() * 4 + fl_h[0].numel()
+    calls = []
+    for i in range(2):
+        dv_ = views(dev_buf[i])
+        kw = dict(ckpt=layer.ckpt, ring_v=layer.ring_v, ring_k=layer.ring_k, ring_a=layer.ring_a,
+                  slot_idx=layer.slot_idx, write_pos=dv_["wp"], is_flush=dv_["fl"], v=dv_["v"], k=dv_["k"],
+                  q=dv_["q"], alpha=dv_["alpha"], out=outs[i])
+        if gdn:
+            calls.append(lib.prepare_decode("replayssm_decode_gdn", beta=dv_["beta"], **kw))
+        else:
+            calls.append(lib.prepare_decode("replayssm_decode_mamba2", ckpt_lp=layer.ckpt_lp, kq_scratch=layer.kq,
+                                            **kw))
     d2h = o_h[0].numel() * 4
-    cp = torch.cuda.Stream(device=dev)
-    comp = torch.cuda.Stream(device=dev)
-    up = [torch.cuda.Event() for _ in range(2)]     # inputs of a buffer landed
-    used = [torch.cuda.Event() for _ in range(2)]   # the decode that read a buffer is done
-    back = [torch.cuda.Event() for _ in range(2)]   # output of a step is in host memory
+    up_s, comp, down_s = (torch.cuda.Stream(device=dev) for _ in range(3))
+    up = [torch.cuda.Event() for _ in range(2)]     # a device buffer holds this step's inputs
+    used = [torch.cuda.Event() for _ in range(2)]   # the decode that read a device buffer is done
+    back = [torch.cuda.Event() for _ in range(2)]   # an output buffer has reached host memory
     ds = layer.decode_step0.copy()
 
     def launch(t):
-        i = t % 2
-        x = host_in[t % N_INPUT_SETS]
-        lib.replayssm_plan_step(ds + t, layer.spec["L"], write_pos=wp_h[i].numpy(), is_flush=fl_h[i].numpy())
-        with torch.cuda.stream(cp):
-            cp.wait_event(used[i])
-            for n, t_h in x.items():
-                if t_h is not None:
-                    d_in[i][n].copy_(t_h, non_blocking=True)
-            wp_d[i].copy_(wp_h[i], non_blocking=True)
-            fl_d[i].copy_(fl_h[i], non_blocking=True)
-            up[i].record(cp)
-        with torch.cuda.stream(comp):
-            comp.wait_event(up[i])
-            layer.replay_step(t, comp, x=d_in[i], wp=wp_d[i], fl=fl_d[i])
-            used[i].record(comp)
-            o_h[i].copy_(layer.out, non_blocking=True)
-            back[i].record(comp)
+        i, hs = t % 2, t % N_INPUT_SETS
+        wp, fl = host[hs]
+        lib.replayssm_plan_step(ds + t, L, write_pos=wp, is_flush=fl)
+        up_s.wait_event(used[i])
+        with torch.cuda.stream(up_s):
+            dev_buf[i].copy_(host_buf[hs], non_blocking=True)
+        up[i].record(up_s)
+        comp.wait_event(up[i])
+        comp.wait_event(back[i])
+        calls[i].launch(comp)
+        used[i].record(comp)
+        down_s.wait_event(used[i])
+        with torch.cuda.stream(down_s):
+            o_h[i].copy_(outs[i], non_blocking=True)
+        back[i].record(down_s)
 
     def read(t):
         back[t % 2].synchronize()  # the host holds this step's output
@@ -469,7 +578,7 @@ def measure_e2e(lib, torch, layer, steps, dist):
         tt = torch.tensor([el], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         el = float(tt.item())
-    return el, h2d, d2h
+    return el, nbytes, d2h
 
 
 def measure_materialize(lib, torch, layer, args, sampler, launches=32):
@@ -660,8 +769,10 @@ def run_native(args):
     # CPU baseline first: spawned oracle workers start before any CUDA call
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        val, cores, sample = oracle_throughput(spec, args.cpu_seconds)
+        val, cores, sample = oracle_batched_throughput(spec, args.cpu_seconds)
         cpu = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        pval, pcores, psample = oracle_throughput(spec, args.cpu_seconds / 2)
+        cpu["per_row"] = {"value": pval, "unit": UNIT, "cores": pcores, "sample": psample}
 
     dist = None
     if world > 1:
@@ -774,8 +885,10 @@ def run_native(args):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "steps": args.e2e_steps,
-            "how": "C ABI with pinned host buffers: per step the host plan, H2D of v/k/q/alpha and the plan, "
-                   "decode, D2H of o and a host read of it; the next step's H2D overlaps this step's decode",
+            "how": "C ABI with pinned host buffers: per step the host plan into the step's staging buffer, one H2D "
+                   "of that buffer (v/k/q/alpha and the plan), the decode (arguments marshalled once per device "
+                   "buffer), one D2H of o and a host read of it; uploads, decodes and downloads on three streams, "
+                   "so step t+1's upload and step t-1's download overlap step t's decode",
         },
         "gpu_launches": K,
         "clocks": clocks,
@@ -845,7 +958,7 @@ def run_reference(args):
     if rank != 0:
         return
     spec = WORKLOADS[args.workload]
-    val, cores, sample = oracle_throughput(spec, args.ref_seconds, warmup=args.warmup, steps=args.steps)
+    val, cores, sample = oracle_batched_throughput(spec, args.ref_seconds, warmup=args.warmup, steps=args.steps)
     line = {
         "impl": "reference",
         "metric": METRIC,

@@ -494,6 +494,35 @@ def replayssm_spec_commit(*, committed, is_flush, accepted, L, T, committed_out=
                   "replayssm_spec_commit")
 
 
+class PreparedStep:
+    """One decode entry point with its arguments marshalled once.
+
+    For a serving loop whose buffers stay at the same addresses from step to
+    step: the tensors are checked and their addresses written into an
+    ``rs_step_args`` struct once, and each ``launch`` is then a single call
+    of the C entry point.  The call reads the tensors' contents when it runs
+    on the stream, so they may change between launches; the tensors
+    themselves must stay alive (this object keeps references to them).
+    """
+
+    def __init__(self, name, args, tensors):
+        self.name, self._args, self._tensors = name, args, tensors
+        self._fn = getattr(load(), name)
+
+    def launch(self, stream=None):
+        return _check(self._fn(ctypes.byref(self._args), _stream(stream)), self.name)
+
+
+def prepare_decode(name, **kw):
+    """A ``PreparedStep`` of ``replayssm_decode_mamba2`` or
+    ``replayssm_decode_gdn``, with the keyword arguments of that function
+    (``stream`` is given to ``launch`` instead)."""
+    variants = {"replayssm_decode_mamba2": RS_MAMBA2, "replayssm_decode_gdn": RS_GDN}
+    if name not in variants:
+        raise ValueError(f"no prepared form of {name}")
+    return PreparedStep(name, _fill(StepArgs(), variant=variants[name], **kw), dict(kw))
+
+
 def raw_call(name, args, *extra):
     """Call an entry point with a prepared StepArgs and return the status
     (no exception).  Used to exercise the C-side validation."""
