@@ -53,6 +53,14 @@ WORKLOADS = {
                             desc="Mamba-2 layer as mamba2_bs256 with the model's own key layout: keys and queries "
                                  "shared by 8 groups of 16 heads, key ring per group, group dots k_j.q computed "
                                  "once per group"),
+    "mamba2_bs256_L8": dict(variant="mamba2", B=256, H=128, d_v=64, d_k=128, L=8, ckpt="f32", inp="bf16",
+                            ring="bf16", desc="Mamba-2 layer as mamba2_bs256 with buffer length L 8"),
+    "mamba2_bs256_L32": dict(variant="mamba2", B=256, H=128, d_v=64, d_k=128, L=32, ckpt="f32", inp="bf16",
+                             ring="bf16", desc="Mamba-2 layer as mamba2_bs256 with buffer length L 32"),
+    "mamba2_bs512": dict(variant="mamba2", B=512, H=128, d_v=64, d_k=128, L=16, ckpt="f32", inp="bf16",
+                         ring="bf16", desc="Mamba-2 layer as mamba2_bs256 at batch 512"),
+    "mamba2_bs256_f16": dict(variant="mamba2", B=256, H=128, d_v=64, d_k=128, L=16, ckpt="f16", inp="bf16",
+                             ring="bf16", desc="Mamba-2 layer as mamba2_bs256 with an fp16 checkpoint (2 MiB per row)"),
     "gdn_bs256": dict(variant="gdn", B=256, H=32, d_v=128, d_k=128, L=16, ckpt="f32", inp="bf16", ring="f16",
                       desc="Gated DeltaNet layer: batch 256, 32 value heads of 128 x 128, fp32 checkpoint, "
                            "fp16 d/k rings, fp32 g ring, L 16, staggered cursors"),
@@ -725,6 +733,7 @@ def run_sweep(args):
     device = torch.device("cuda", 0)
     peak, _ = _peak()
     base = WORKLOADS["mamba2_bs256"]
+    sampler = ClockSampler(0)
     out = []
     for ck in ("f32", "f16"):
         for L in (8, 16, 32):
@@ -743,8 +752,8 @@ def run_sweep(args):
                     for t in range(8):
                         rep(t, stream)
                         con(t, stream)
-                ms_r = _timed_graph(torch, rep, 8, 8 + K, stream, False, None, None) / K
-                ms_c = _timed_graph(torch, con, 8, 8 + K, stream, False, None, None) / K
+                ms_r = _timed_graph(torch, rep, 8, 8 + K, stream, False, None, sampler) / K
+                ms_c = _timed_graph(torch, con, 8, 8 + K, stream, False, None, sampler) / K
                 by_r = np.mean([p.bytes_per_step(8, 8 + K) for p in pools[:1]])
                 by_c = pools[0].bytes_per_step(8, 9, replay=False)
                 row = dict(ckpt=ck, L=L, B=B, pools=n_pools, replay_us=ms_r * 1e3, conventional_us=ms_c * 1e3,
@@ -755,6 +764,7 @@ def run_sweep(args):
                 print(json.dumps(row), flush=True)
                 del pools
                 torch.cuda.empty_cache()
+    print(json.dumps({"clocks": sampler.finish()}), flush=True)
     return out
 
 

@@ -448,3 +448,31 @@ __device__ __forceinline__ float lds_elem(const unsigned char *base, int elem, i
 }
 
 }  // namespace rs
+
+namespace rs {
+
+// m16n8k16 bf16 tensor-core product with fp32 accumulate (D += A B); lane
+// 4 g + t holds A rows g and g+8 at columns 2t, 2t+1 (a0, a1) and 2t+8,
+// 2t+9 (a2, a3), each register two bf16 with the lower column in its low
+// half; B rows 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) of column g; D as for
+// mma_tf32
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (x0, x1) = hi + lo with hi and lo pairs of bf16 (round to nearest even,
+// x0 in the low halves): two bf16 products carry about 16 mantissa bits of
+// an fp32 operand, a relative error of at most 2^-17
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+}  // namespace rs

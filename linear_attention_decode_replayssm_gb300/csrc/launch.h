@@ -25,6 +25,8 @@ MatLaunchFn find_materialize(int d_v, int d_k, int ckpt_dtype);
 // Speculative verification (Mamba-2) and the device-side commit.
 using SpecLaunchFn = cudaError_t (*)(const rs_spec_args &, cudaStream_t);
 SpecLaunchFn find_spec(int d_v, int d_k, int ckpt_dtype, int in_dtype);
+// the tensor-core verification (spec_tc.cu), or nullptr where it is not built
+SpecLaunchFn find_spec_tc(int d_v, int d_k, int ckpt_dtype, int in_dtype);
 cudaError_t launch_spec_commit(const int32_t *committed, const uint8_t *is_flush, const int32_t *accepted, int B,
                                int L, int T, int32_t *committed_out, uint8_t *is_flush_out, int32_t *dev_err,
                                cudaStream_t s);

@@ -13,7 +13,7 @@ LaunchFn find_mamba2_f32_inputs(int d_v, int d_k, int ckpt_dtype);             /
 
 // launch_mamba2<d_v, d_k, checkpoint type, input type, consumer warps per
 // group, groups, read-copy type, chunks per lane and row, fine window bounds,
-// window warp>; the 64 x 128 fp32 layer runs with the window warp
+// window warp>; the 64 x 128 fp32 and fp16 layers run with the window warp
 static LaunchFn find_mamba2_bf16_inputs(int d_v, int d_k, int ckpt_dtype) {
   using RT = __nv_bfloat16;
   if (ckpt_dtype == kF32) {
@@ -22,7 +22,7 @@ static LaunchFn find_mamba2_bf16_inputs(int d_v, int d_k, int ckpt_dtype) {
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1>;
   } else if (ckpt_dtype == kF16) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, __half, RT, 2, 1>;
-    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, __half, RT, 4, 2, __half, 1, true>;
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, __half, RT, 4, 2, __half, 1, true, true>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, __half, RT, 8, 1>;
   }
   return nullptr;

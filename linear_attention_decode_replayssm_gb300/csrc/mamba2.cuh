@@ -36,7 +36,7 @@
 // a timeout the kernel reports RS_DERR_TIMEOUT, drains its own copies and
 // returns.
 // The per-step products stay on the CUDA cores (a bandwidth-bound GEMV, about
-// 0.6 FLOP/byte); the flush fold of an fp32 checkpoint, a rank-(p+1) update of
+// 0.6 FLOP/byte); the flush fold of an fp32 or fp16 checkpoint, a rank-(p+1) update of
 // the whole state held in registers, runs on the tensor cores.
 #pragma once
 
@@ -113,8 +113,10 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
   constexpr uint32_t CKB = DV * DK * (uint32_t)sizeof(TC);
   constexpr uint32_t CKB_LP = DV * DK * (uint32_t)sizeof(TL);
   static_assert(!TWO || (E == 4 && sizeof(TL) == 2), "read copy: 16-bit elements under an fp32 checkpoint");
-  // flush fold on the tensor cores: fp32 checkpoint, one warp per 16 state rows
-  constexpr bool MMAF = std::is_same<TC, float>::value && DV == 16 * NCW && DK % 16 == 0;
+  // flush fold on the tensor cores: fp32 or fp16 checkpoint, one warp per 16
+  // state rows
+  constexpr bool MMAF = (std::is_same<TC, float>::value || std::is_same<TC, __half>::value) && DV == 16 * NCW &&
+                        DK % 16 == 0;
   static_assert(G <= 32 && 32 % G == 0 && NCH % CPR == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && DV % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
   static_assert(DK % 8 == 0 && DV % 8 == 0, "head dims must be multiples of 8");
@@ -696,10 +698,20 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
       const int g8 = lane >> 2, t4 = lane & 3;
       const int rA = 16 * lw + g8, rB = rA + 8;
       float4 xa[NB], xb[NB];
+      // four consecutive checkpoint elements of a state row, widened to fp32
+      auto ld4 = [&](int r, int col) -> float4 {
+        if constexpr (sizeof(TC) == 4) {
+          return *reinterpret_cast<const float4 *>(ck_row(r) + col * 4);
+        } else {
+          float f[4];
+          LpVec<__half>::unpack(*reinterpret_cast<const uint2 *>(ck_row(r) + col * 2), f);
+          return make_float4(f[0], f[1], f[2], f[3]);
+        }
+      };
 #pragma unroll
       for (int bk = 0; bk < NB; ++bk) {
-        xa[bk] = *reinterpret_cast<const float4 *>(ck_row(rA) + (16 * bk + 4 * t4) * 4);
-        xb[bk] = *reinterpret_cast<const float4 *>(ck_row(rB) + (16 * bk + 4 * t4) * 4);
+        xa[bk] = ld4(rA, 16 * bk + 4 * t4);
+        xb[bk] = ld4(rB, 16 * bk + 4 * t4);
       }
       release_ck();
       if constexpr (WW) {
@@ -764,8 +776,13 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
         const size_t offA = (size_t)rA * DK + 16 * bk + 4 * t4, offB = (size_t)rB * DK + 16 * bk + 4 * t4;
         const float fa[4] = {xa[bk].x, xa[bk].y, xa[bk].z, xa[bk].w};
         const float fb[4] = {xb[bk].x, xb[bk].y, xb[bk].z, xb[bk].w};
-        st_vec(ckg + offA, V::pack(fa));
-        st_vec(ckg + offB, V::pack(fb));
+        if constexpr (sizeof(TC) == 4) {
+          st_vec(ckg + offA, V::pack(fa));
+          st_vec(ckg + offB, V::pack(fb));
+        } else {
+          st_vec2(ckg + offA, LpVec<__half>::pack(fa));
+          st_vec2(ckg + offB, LpVec<__half>::pack(fb));
+        }
         if constexpr (TWO) {
           TL *lpg = static_cast<TL *>(a.ckpt_lp) + unit * (DV * DK);
           st_vec2(lpg + offA, LpVec<TL>::pack(fa));

@@ -444,6 +444,7 @@ static SpecLaunchFn find_spec_t(int d_v, int d_k, int ckpt_dtype) {
 }
 
 SpecLaunchFn find_spec(int d_v, int d_k, int ckpt_dtype, int in_dtype) {
+  if (SpecLaunchFn f = find_spec_tc(d_v, d_k, ckpt_dtype, in_dtype)) return f;
   return in_dtype == kF32 ? find_spec_t<float>(d_v, d_k, ckpt_dtype)
                           : find_spec_t<__nv_bfloat16>(d_v, d_k, ckpt_dtype);
 }

@@ -247,3 +247,16 @@ def test_spec_verify_fp16_checkpoint(cuda, T):
     err, worst_o, worst_c, n_flush = spec._run(cuda, w, T, 12, heads=[0, 31], seed=T)
     assert err == 0 and n_flush > 0
     assert worst_o <= par.TOL_F16 and worst_c <= par.TOL_F16, (worst_o, worst_c)
+
+
+@pytest.mark.parametrize("d_v, d_k, H, in_dtype, T", [(128, 128, 32, "bf16", 4), (64, 128, 32, "f32", 8),
+                                                     (16, 32, 64, "bf16", 4), (128, 128, 32, "bf16", 16)])
+def test_spec_verify_other_shapes(cuda, d_v, d_k, H, in_dtype, T):
+    # the CUDA-core verification kernel: 128 x 128 and 16 x 32 heads, fp32 drafts
+    B = 40
+    assert_many_units(B, H)
+    w = synth.make_workload("mamba2_bs256", B=B, H=H, d_v=d_v, d_k=d_k, L=16, steps=1, pad_rows=1,
+                            in_dtype=in_dtype, ring_dtype=in_dtype, seed=560 + d_v + T)
+    err, worst_o, worst_c, n_flush = spec._run(cuda, w, T, 12, heads=[1, H - 2], seed=T)
+    assert err == 0 and n_flush > 0
+    assert worst_o <= spec.TOL and worst_c <= spec.TOL, (worst_o, worst_c)
