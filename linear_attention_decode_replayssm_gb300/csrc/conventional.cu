@@ -19,12 +19,9 @@ namespace rs {
 
 // A unit is RB = DV / NSPLIT state rows of one (row, head): the rows of the
 // update are independent once the row dots are known, so a 128 x 128 fp32
-// head is two 32 KiB units, the same shape as a 64 x 128 Mamba-2 head.  A
-// CTA takes HPC consecutive units, NT threads each, with a named barrier per
-// unit, so that small (fp16) units still put a fp32-sized block of state in
-// flight per CTA.
-template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT, int HPC>
-__global__ void __launch_bounds__(NT * HPC) conventional_kernel(const KArgs a) {
+// head is two 32 KiB units, the same shape as a 64 x 128 Mamba-2 head.
+template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT>
+__global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
   using V = CkVec<TC>;
   constexpr int RB = DV / NSPLIT;
   constexpr int E = V::E;
@@ -34,23 +31,11 @@ __global__ void __launch_bounds__(NT * HPC) conventional_kernel(const KArgs a) {
   static_assert(G <= 32 && 32 % G == 0, "a state row must fit in one warp");
   static_assert(NT % G == 0 && RB % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
 
-  __shared__ float sK_[HPC][DK], sQ_[HPC][DK], sV_[HPC][RB], sU_[HPC][RB], sC_[HPC][RB];
+  __shared__ float sK[DK], sQ[DK], sV[RB], sU[RB], sC[RB];
 
-  const int sub = HPC > 1 ? (int)threadIdx.x / NT : 0;
-  const int tid = (int)threadIdx.x - sub * NT, lane = tid & 31;
-  float *sK = sK_[sub], *sQ = sQ_[sub], *sV = sV_[sub], *sU = sU_[sub], *sC = sC_[sub];
-  // the unit's own barrier: units of one CTA never wait for each other
-  auto usync = [&]() {
-    if constexpr (HPC == 1) {
-      __syncthreads();
-    } else {
-      asm volatile("bar.sync %0, %1;" ::"r"(1 + sub), "n"(NT) : "memory");
-    }
-  };
-  const int u = blockIdx.x * HPC + sub;
-  if (u >= a.B * a.H * NSPLIT) return;
-  const int b = u / (a.H * NSPLIT);
-  const int rem = u - b * (a.H * NSPLIT);
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int b = blockIdx.x / (a.H * NSPLIT);
+  const int rem = blockIdx.x - b * (a.H * NSPLIT);
   const int h = rem / NSPLIT, row_off = (rem - h * NSPLIT) * RB;
   float *orow = a.out + (size_t)b * a.so + (size_t)h * DV + row_off;
   const int slot = __ldg(a.slot_idx + b);
@@ -89,7 +74,7 @@ __global__ void __launch_bounds__(NT * HPC) conventional_kernel(const KArgs a) {
   }
   const float a_in = __ldg(a.alpha + (size_t)b * a.H + h);
   const float alpha = DELTA ? expf(a_in) : a_in;
-  usync();
+  __syncthreads();
 
   float kv[E], qv[E];
 #pragma unroll
@@ -113,10 +98,10 @@ __global__ void __launch_bounds__(NT * HPC) conventional_kernel(const KArgs a) {
     }
     group_reduce<VPT, G>(part, lane);
     if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
-    usync();
+    __syncthreads();
     const float beta = __ldg(a.beta + (size_t)b * a.H + h);
     for (int i = tid; i < RB; i += NT) sU[i] = beta * (sV[i] - alpha * sC[i]);
-    usync();
+    __syncthreads();
   }
 
   const float *upd = DELTA ? sU : sV;
@@ -135,14 +120,13 @@ __global__ void __launch_bounds__(NT * HPC) conventional_kernel(const KArgs a) {
   }
   group_reduce<VPT, G>(part, lane);
   if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
-  usync();
+  __syncthreads();
   for (int i = tid; i < RB; i += NT) orow[i] = sC[i];
 }
 
-template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT = 1, int HPC = 1>
+template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT = 1>
 static cudaError_t launch_conv(const KArgs &a, cudaStream_t s) {
-  const size_t units = (size_t)a.B * a.H * NSPLIT;
-  conventional_kernel<DV, DK, TC, NT, DELTA, NSPLIT, HPC><<<(unsigned)((units + HPC - 1) / HPC), NT * HPC, 0, s>>>(a);
+  conventional_kernel<DV, DK, TC, NT, DELTA, NSPLIT><<<(unsigned)((size_t)a.B * a.H * NSPLIT), NT, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -154,7 +138,7 @@ static LaunchFn find_conv_t(int d_v, int d_k, int ckpt_dtype) {
     if (d_v == 128 && d_k == 128) return launch_conv<128, 128, float, 256, DELTA, 2>;
   } else if (ckpt_dtype == kF16) {
     if (d_v == 16 && d_k == 32) return launch_conv<16, 32, __half, 64, DELTA>;
-    if (d_v == 64 && d_k == 128) return launch_conv<64, 128, __half, 64, DELTA, 1, 2>;
+    if (d_v == 64 && d_k == 128) return launch_conv<64, 128, __half, 128, DELTA>;
     if (d_v == 128 && d_k == 128) return launch_conv<128, 128, __half, 256, DELTA>;
   }
   return nullptr;

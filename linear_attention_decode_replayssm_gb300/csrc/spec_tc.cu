@@ -370,6 +370,27 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
     // element split into two bf16 terms.
     const float gam = flush ? sWf[64] : 1.f;
     TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK);
+    // the fold's A operands of records j0 + t4 and j0 + t4 + 4 (weighted
+    // values of rows rA and rB, each split into two tf32 terms); past h they
+    // weigh 0 and read record 0
+    auto fold_a = [&](int j0, uint32_t (&ah)[4], uint32_t (&al)[4], int &ra, int &rb) {
+      const int ja = j0 + t4, jb = ja + 4;
+      ra = ja < hc ? ja : 0;
+      rb = jb < hc ? jb : 0;
+      const float wa = ja < hc ? sWf[ja] : 0.f, wb = jb < hc ? sWf[jb] : 0.f;
+      split_tf32(wa * bf16_at(sv, ra * DV + v_pos(ra, rA)), ah[0], al[0]);
+      split_tf32(wa * bf16_at(sv, ra * DV + v_pos(ra, rB)), ah[1], al[1]);
+      split_tf32(wb * bf16_at(sv, rb * DV + v_pos(rb, rA)), ah[2], al[2]);
+      split_tf32(wb * bf16_at(sv, rb * DV + v_pos(rb, rB)), ah[3], al[3]);
+    };
+    // the first 16 committed records' operands are formed once for all
+    // column blocks (a window of L <= 16 fits); later ones per block
+    uint32_t fh[2][4], fl[2][4];
+    int fra[2], frb[2];
+    if (flush) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) fold_a(8 * q, fh[q], fl[q], fra[q], frb[q]);
+    }
     float cacc[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) cacc[n][0] = cacc[n][1] = cacc[n][2] = cacc[n][3] = 0.f;
@@ -380,15 +401,20 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
         pa.x *= gam; pa.y *= gam; pa.z *= gam; pa.w *= gam;
         pb.x *= gam; pb.y *= gam; pb.z *= gam; pb.w *= gam;
         for (int j0 = 0; j0 < hc; j0 += 8) {
-          // records j0 + t and j0 + t + 4; past h they weigh 0 (and read record 0)
-          const int ja = j0 + t4, jb = ja + 4;
-          const int ra = ja < hc ? ja : 0, rb = jb < hc ? jb : 0;
-          const float wa = ja < hc ? sWf[ja] : 0.f, wb = jb < hc ? sWf[jb] : 0.f;
           uint32_t ah[4], al[4];
-          split_tf32(wa * bf16_at(sv, ra * DV + v_pos(ra, rA)), ah[0], al[0]);
-          split_tf32(wa * bf16_at(sv, ra * DV + v_pos(ra, rB)), ah[1], al[1]);
-          split_tf32(wb * bf16_at(sv, rb * DV + v_pos(rb, rA)), ah[2], al[2]);
-          split_tf32(wb * bf16_at(sv, rb * DV + v_pos(rb, rB)), ah[3], al[3]);
+          int ra, rb;
+          if (j0 < 16) {
+            const int q = j0 >> 3;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              ah[e] = q ? fh[1][e] : fh[0][e];
+              al[e] = q ? fl[1][e] : fl[0][e];
+            }
+            ra = q ? fra[1] : fra[0];
+            rb = q ? frb[1] : frb[0];
+          } else {
+            fold_a(j0, ah, al, ra, rb);
+          }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const int col = 16 * bk + 4 * (g8 >> 1) + (g8 & 1) + 2 * hf;  // column of tile index n = g8
