@@ -29,7 +29,8 @@ Modules
               it performs, in float64 arithmetic             (algorithm steps)
   spec        speculative verification with pointer commit (Mamba-2)
                                                              (algorithm steps)
-  storage     round-to-nearest-even casts to fp32 / fp16 / bf16
+  storage     round-to-nearest-even casts to fp32 / fp16 / bf16 / e4m3, and
+              the read copy's e4m3 rounding on a power-of-two row scale
   traffic     the byte and FLOP model the pages price the method with
 
 Every function states the passage it follows.  Parity status of each function
@@ -55,7 +56,7 @@ from .replay import (
     materialize,
     heads_from_groups,
 )
-from .storage import round_to, STORAGE_DTYPES
+from .storage import round_to, round_read_copy, round_rows_scaled, row_scale_exponent, STORAGE_DTYPES
 from . import spec, traffic
 
 __all__ = [
@@ -77,6 +78,9 @@ __all__ = [
     "materialize",
     "heads_from_groups",
     "round_to",
+    "round_read_copy",
+    "round_rows_scaled",
+    "row_scale_exponent",
     "STORAGE_DTYPES",
     "spec",
     "traffic",

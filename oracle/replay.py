@@ -66,7 +66,7 @@ from .recurrence import (
     mamba2_step,
     unroll,
 )
-from .storage import round_to
+from .storage import round_read_copy, round_to
 
 VARIANTS = ("mamba2", "gdn")
 
@@ -123,11 +123,13 @@ class ReplayState:
     def with_read_copy(self, lp_dtype):
         """Add the low-precision read copy of the two-precision checkpoint
         ([Ghana] §The precision argument, derived): the copy is cast from the
-        same values as the recurrence copy (here: the starting checkpoint)."""
+        same values as the recurrence copy (here: the starting checkpoint).
+        ``lp_dtype`` fp16 or bf16, or e4m3 on a power-of-two scale per state
+        row (``storage.round_read_copy``)."""
         if self.variant != "mamba2":
             raise NotImplementedError("two-precision checkpoint: Mamba-2 only")
         self.lp_dtype = lp_dtype
-        self.ckpt_lp = round_to(self.ckpt, lp_dtype)
+        self.ckpt_lp = round_read_copy(self.ckpt, lp_dtype)
         return self
 
     def reset_slot(self, s, ckpt0):
@@ -136,7 +138,7 @@ class ReplayState:
         from decode_step mod L, so recycled blocks need no zero-init)."""
         self.ckpt[s] = np.asarray(ckpt0, dtype=np.float64)
         if self.ckpt_lp is not None:
-            self.ckpt_lp[s] = round_to(ckpt0, self.lp_dtype)
+            self.ckpt_lp[s] = round_read_copy(ckpt0, self.lp_dtype)
 
 
 def _f64(x):
@@ -195,7 +197,7 @@ def replay_step(st, slot_idx, write_pos, is_flush, v, k, q, alpha, beta=None):
         if is_flush[b]:
             st.ckpt[s] = round_to(S_t, st.ckpt_dtype)
             if st.ckpt_lp is not None:  # both copies cast from the same unrounded matrix
-                st.ckpt_lp[s] = round_to(S_t, st.lp_dtype)
+                st.ckpt_lp[s] = round_read_copy(S_t, st.lp_dtype)
         else:
             st.ring_v[s, :, p] = round_to(new_v, st.ring_dtype)
             st.ring_k[s, :, p] = round_to(k[b], st.ring_dtype)

@@ -208,3 +208,28 @@ def test_two_precision_reading_the_recurrence_copy_is_caught(monkeypatch):
 
     monkeypatch.setattr(oracle, "replay_step", bad)
     assert _fails(pins.test_two_precision_read_error_is_one_rounding, "bf16")
+
+
+def test_e4m3_row_scale_off_by_one_is_caught(monkeypatch):
+    import oracle.storage
+
+    good = oracle.storage.row_scale_exponent
+
+    def bad(x):
+        return good(x) - 1  # one binade too fine: the row maximum saturates
+
+    monkeypatch.setattr(oracle.storage, "row_scale_exponent", bad)
+    monkeypatch.setattr(oracle, "row_scale_exponent", bad)
+    assert _fails(pins.test_e4m3_read_copy_row_scales)
+
+
+def test_e4m3_rounding_toward_zero_is_caught(monkeypatch):
+    import oracle.storage
+
+    def bad(x):
+        x = np.asarray(x, dtype=np.float64)
+        m, e = np.frexp(x)
+        return np.clip(np.ldexp(np.trunc(m * 16.0) / 16.0, e), -448.0, 448.0)  # truncates instead of rounding
+
+    monkeypatch.setattr(oracle.storage, "_round_e4m3", bad)
+    assert _fails(pins.test_round_e4m3_ties_saturation_and_library)

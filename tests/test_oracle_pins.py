@@ -118,6 +118,51 @@ def test_round_bf16_ties_and_library():
     np.testing.assert_array_equal(r(x.astype(np.float64), "bf16"), ref)
 
 
+def test_round_e4m3_ties_saturation_and_library():
+    r = oracle.round_to
+    assert r(1.0 + 2.0 ** -4, "e4m3") == 1.0                      # tie -> even
+    assert r(1.0 + 3 * 2.0 ** -4, "e4m3") == 1.25                 # tie -> even
+    assert r(1.0 + 2.0 ** -4 + 2.0 ** -30, "e4m3") == 1.125
+    assert r(0.3, "e4m3") == 0.3125
+    assert r(2.0 ** -9, "e4m3") == 2.0 ** -9                      # smallest subnormal
+    assert r(2.0 ** -10, "e4m3") == 0.0                           # half of it: tie -> 0
+    assert r(3 * 2.0 ** -10, "e4m3") == 2.0 ** -8                 # tie between 1 and 2 steps -> even
+    assert r(2.0 ** -6 + 2.0 ** -10, "e4m3") == 2.0 ** -6         # smallest normal, below half a step
+    assert r(448.0, "e4m3") == 448.0 and r(464.0, "e4m3") == 448.0  # largest finite; tie -> even
+    assert r(1e6, "e4m3") == 448.0 and r(-1e6, "e4m3") == -448.0  # saturation
+    assert np.isnan(r(np.nan, "e4m3"))
+    # against torch's float32 -> float8_e4m3fn conversion (nearest even) on
+    # values inside the finite range, normal and subnormal
+    torch = pytest.importorskip("torch")
+    rng = _rng(9)
+    x = np.concatenate([rng.standard_normal(20000) * 30.0, rng.standard_normal(20000) * 0.01]).astype(np.float32)
+    x = x[np.abs(x) <= 440.0]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(r(x.astype(np.float64), "e4m3"), ref)
+
+
+def test_e4m3_read_copy_row_scales():
+    """The E4M3 read copy scales each state row by a power of two so that its
+    largest element lands in (224, 448], then rounds once on that grid."""
+    e = oracle.row_scale_exponent
+    assert list(e(np.array([[1.0, -0.5], [448.0, 1.0], [-449.0, 0.0], [0.0, 0.0], [0.875, 0.1]]))) == [-8, 0, 1, 0, -9]
+    rng = _rng(4)
+    x = rng.standard_normal((50, 128)) * np.exp(rng.uniform(-12, 6, (50, 1)))
+    y = oracle.round_rows_scaled(x)
+    ex = e(x)[:, None]
+    amax = np.max(np.abs(x), axis=1, keepdims=True)
+    assert np.all(amax * 2.0 ** -ex > 224.0) and np.all(amax * 2.0 ** -ex <= 448.0)
+    # one rounding on the row's grid: within half a step of E4M3 at x / 2^e
+    xs = np.abs(x) * 2.0 ** -ex
+    step = np.where(xs < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(xs, 2.0 ** -6))) - 3))
+    assert np.all(np.abs(y - x) <= 0.5 * step * 2.0 ** ex * (1 + 1e-12))
+    # power-of-two scaling of a row commutes with the copy; a zero row stays zero
+    np.testing.assert_array_equal(oracle.round_rows_scaled(x * 2.0 ** 7), y * 2.0 ** 7)
+    assert np.all(oracle.round_rows_scaled(np.zeros((2, 8))) == 0)
+    assert oracle.round_read_copy(x, "e4m3") is not None
+    np.testing.assert_array_equal(oracle.round_read_copy(x, "f16"), oracle.round_to(x, "f16"))
+
+
 def test_round_f32_matches_cast():
     x = _rng(3).standard_normal(1000)
     np.testing.assert_array_equal(oracle.round_to(x, "f32"), x.astype(np.float32).astype(np.float64))
@@ -532,7 +577,7 @@ def _two_precision_run(lp_dtype, steps, alpha_lo, alpha_hi, L=4, H=2, dv=8, dk=1
         o_e = oracle.exact_step(ex, [0], v, k, q, a)
         gam = gam * a[0]
         if single is None:
-            eps = oracle.round_to(S_m, lp_dtype) - S_m
+            eps = oracle.round_read_copy(S_m, lp_dtype) - S_m
             predicted.append(gam[:, None] * np.einsum("hij,hj->hi", eps, q[0]))
         if fl[0]:
             S_m = ex.S[0].copy()
@@ -548,7 +593,7 @@ def test_two_precision_with_exact_read_copy_is_exact():
     assert rel_err(outs, exact) < 1e-12
 
 
-@pytest.mark.parametrize("lp", ["f16", "bf16"])
+@pytest.mark.parametrize("lp", ["f16", "bf16", "e4m3"])
 def test_two_precision_read_error_is_one_rounding(lp):
     """The pages' derivation: a non-flush step h records after the last flush
     errs by exactly gamma_h * eps_m * q, eps_m the read copy's rounding of the
