@@ -48,6 +48,11 @@ WORKLOADS = {
                               ring="bf16", lp="f16",
                               desc="Mamba-2 layer as mamba2_bs256 with a two-precision checkpoint: fp32 "
                                    "recurrence copy, fp16 read copy for non-flush rows"),
+    "mamba2_bs256_lp8": dict(variant="mamba2", B=256, H=128, d_v=64, d_k=128, L=16, ckpt="f32", inp="bf16",
+                             ring="bf16", lp="e4m3",
+                             desc="Mamba-2 layer as mamba2_bs256 with a two-precision checkpoint: fp32 "
+                                  "recurrence copy, E4M3 read copy (a power-of-two scale per state row) for "
+                                  "non-flush rows"),
     "mamba2_bs256_g8": dict(variant="mamba2", B=256, H=128, d_v=64, d_k=128, L=16, ckpt="f32", inp="bf16",
                             ring="bf16", groups=8,
                             desc="Mamba-2 layer as mamba2_bs256 with the model's own key layout: keys and queries "
@@ -339,7 +344,7 @@ class Layer:
 
         self.lib, self.spec, self.device = lib, spec, device
         B, H, dv, dk, L = (spec[k] for k in ("B", "H", "d_v", "d_k", "L"))
-        td = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+        td = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
         g = torch.Generator(device=device)
         g.manual_seed(seed)
         gdn = spec["variant"] == "gdn"
@@ -357,7 +362,12 @@ class Layer:
         sk = math.sqrt(dk)
         self.ckpt = (randn(B, H, dv, dk) / sk).to(td[spec["ckpt"]])
         self.state = self.ckpt.clone() if with_state else None  # for the conventional kernel
-        self.ckpt_lp = self.ckpt.to(td[spec["lp"]]) if spec.get("lp") else None  # two-precision read copy
+        self.ckpt_lp = self.ckpt_lp_scale = None  # two-precision read copy, cast by the library
+        if spec.get("lp"):
+            self.ckpt_lp = torch.empty(self.ckpt.shape, device=device, dtype=td[spec["lp"]])
+            if spec["lp"] == "e4m3":
+                self.ckpt_lp_scale = torch.empty(self.ckpt.shape[:3], device=device)
+            lib.replayssm_seed_read_copy(ckpt=self.ckpt, ckpt_lp=self.ckpt_lp, scale=self.ckpt_lp_scale)
         self.ring_v = (randn(B, H, L, dv) / sk).to(td[spec["ring"]])
         G = spec.get("groups", 0)
         KH = G or H  # key / query vectors per row
@@ -401,7 +411,8 @@ class Layer:
         if self.spec["variant"] == "gdn":
             self.lib.replayssm_decode_gdn(beta=x["beta"], **kw)
         else:
-            self.lib.replayssm_decode_mamba2(ckpt_lp=self.ckpt_lp, kq_scratch=self.kq, **kw)
+            self.lib.replayssm_decode_mamba2(ckpt_lp=self.ckpt_lp, ckpt_lp_scale=self.ckpt_lp_scale, kq_scratch=self.kq,
+                                             **kw)
 
     def conventional_step(self, t, stream=None):
         x = self.inputs[t % N_INPUT_SETS]
@@ -538,8 +549,8 @@ def measure_e2e(lib, torch, layer, steps, dist):
         if gdn:
             calls.append(lib.prepare_decode("replayssm_decode_gdn", beta=dv_["beta"], **kw))
         else:
-            calls.append(lib.prepare_decode("replayssm_decode_mamba2", ckpt_lp=layer.ckpt_lp, kq_scratch=layer.kq,
-                                            **kw))
+            calls.append(lib.prepare_decode("replayssm_decode_mamba2", ckpt_lp=layer.ckpt_lp,
+                                            ckpt_lp_scale=layer.ckpt_lp_scale, kq_scratch=layer.kq, **kw))
     d2h = o_h[0].numel() * 4
     up_s, comp, down_s = (torch.cuda.Stream(device=dev) for _ in range(3))
     up = [torch.cuda.Event() for _ in range(2)]     # a device buffer holds this step's inputs

@@ -68,7 +68,7 @@ extern "C" {
 /* Same type as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st *rs_stream_t;
 
-#define RS_ABI_VERSION 3
+#define RS_ABI_VERSION 4
 #define RS_MAX_L 64 /* largest supported buffer length */
 
 typedef enum {
@@ -79,7 +79,12 @@ typedef enum {
   RS_ECUDA = -4         /* the CUDA runtime reported an error at launch */
 } rs_status;
 
-typedef enum { RS_F32 = 0, RS_F16 = 1, RS_BF16 = 2 } rs_dtype;
+typedef enum {
+  RS_F32 = 0,
+  RS_F16 = 1,
+  RS_BF16 = 2,
+  RS_F8E4M3 = 3 /* read copy of a two-precision checkpoint only (see ckpt_lp) */
+} rs_dtype;
 
 typedef enum { RS_MAMBA2 = 0, RS_GDN = 1 } rs_variant;
 
@@ -146,11 +151,16 @@ typedef struct rs_step_args {
   int64_t stride_v_row, stride_k_row, stride_q_row, stride_out_row; /* elements */
   int32_t *dev_err; /* optional device int32, see rs_dev_error */
   /* Two-precision checkpoint (Mamba-2 only; NULL = one checkpoint copy):
-   * ckpt_lp [num_slots, H, d_v, d_k] of lp_dtype (RS_F16 or RS_BF16) is the
-   * read copy, ckpt (RS_F32) the recurrence copy.  A non-flush row reads
-   * only ckpt_lp; a flush row reads ckpt, and casts S_new into both copies,
-   * each rounded once (RN-even) from the same fp32 matrix.  The caller seeds
-   * ckpt_lp from the same state as ckpt when a request starts. */
+   * ckpt_lp [num_slots, H, d_v, d_k] of lp_dtype (RS_F16, RS_BF16 or
+   * RS_F8E4M3) is the read copy, ckpt (RS_F32) the recurrence copy.  A
+   * non-flush row reads only ckpt_lp; a flush row reads ckpt, and casts
+   * S_new into both copies, each rounded once (RN-even) from the same fp32
+   * matrix.  An RS_F8E4M3 copy (64 x 128 heads) holds each state row on a
+   * power-of-two scale: element (s, h, i, j) is its E4M3 code times
+   * ckpt_lp_scale[s, h, i], the smallest power of two 2^e with
+   * max_j |S[i][j]| <= 448 * 2^e.  The caller seeds ckpt_lp (and the scales)
+   * from the same state as ckpt when a request starts
+   * (replayssm_seed_read_copy). */
   void *ckpt_lp;
   int32_t lp_dtype;
   int32_t reserved2; /* must be 0 */
@@ -163,6 +173,9 @@ typedef struct rs_step_args {
   int32_t n_groups;
   int32_t reserved3; /* must be 0 */
   float *kq_scratch;
+  /* RS_F8E4M3 read copy: fp32 row scales [num_slots, H, d_v], 16-byte
+   * aligned; NULL for any other read copy */
+  float *ckpt_lp_scale;
 } rs_step_args;
 
 /* RS_ABI_VERSION of the loaded library. */
@@ -320,6 +333,23 @@ int replayssm_plan_spec(const int32_t *committed, int32_t B, int32_t L, int32_t 
 int replayssm_spec_commit(const int32_t *committed, const uint8_t *is_flush, const int32_t *accepted,
                           int32_t B, int32_t L, int32_t T, int32_t *committed_out, uint8_t *is_flush_out,
                           int32_t *dev_err, rs_stream_t stream);
+
+/*
+ * Seed the read copy of a two-precision checkpoint from its recurrence copy
+ * ([Ghana] §The precision argument: both copies are roundings of one fp32
+ * matrix), e.g. when a request starts: n_rows rows of d_k fp32 values at
+ * ckpt (a whole pool is num_slots * H * d_v rows; one slot's heads are H *
+ * d_v rows starting at slot * H * d_v) are each rounded once, to nearest
+ * even, to lp_dtype in ckpt_lp.  For RS_F8E4M3 each row is first scaled by
+ * 2^-e, e the smallest integer with max |row| <= 448 * 2^e (0 for a row of
+ * zeros), the E4M3 cast saturates, and 2^e goes to scale[row]; scale is
+ * unused (may be NULL) for RS_F16 and RS_BF16.  DEVICE pointers owned by the
+ * caller; ckpt and ckpt_lp 16-byte aligned, scale 4-byte aligned; d_k a
+ * multiple of 8, at most 1024.  Returns RS_EINVAL for a bad size, a null
+ * pointer or another dtype, RS_EALIGN, or RS_ECUDA.  Asynchronous on stream.
+ */
+int replayssm_seed_read_copy(const float *ckpt, int64_t n_rows, int32_t d_k, int32_t lp_dtype, void *ckpt_lp,
+                             float *scale, rs_stream_t stream);
 
 /* ReplaySSM Mamba-2 cached decode step, non-flush and flush rows in one
  * launch (beta unused). */

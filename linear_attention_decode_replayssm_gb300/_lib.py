@@ -17,10 +17,10 @@ import numpy as np
 from . import build as _build
 
 RS_OK, RS_EINVAL, RS_EUNSUPPORTED, RS_EALIGN, RS_ECUDA = 0, -1, -2, -3, -4
-RS_F32, RS_F16, RS_BF16 = 0, 1, 2
+RS_F32, RS_F16, RS_BF16, RS_F8E4M3 = 0, 1, 2, 3
 RS_MAMBA2, RS_GDN = 0, 1
 RS_DERR_SLOT, RS_DERR_WRITE_POS, RS_DERR_TIMEOUT, RS_DERR_DST, RS_DERR_ACCEPTED = 1, 2, 4, 8, 16
-RS_ABI_VERSION = 3
+RS_ABI_VERSION = 4
 RS_MAX_L = 64
 RS_NOALLOC_KQ_FLOATS = 1 << 20
 
@@ -34,6 +34,7 @@ EXPORTS = (
     "replayssm_spec_verify_mamba2",
     "replayssm_plan_spec",
     "replayssm_spec_commit",
+    "replayssm_seed_read_copy",
     "replayssm_decode_mamba2",
     "replayssm_decode_mamba2_noalloc",
     "replayssm_decode_gdn",
@@ -59,6 +60,7 @@ class StepArgs(ctypes.Structure):
         ("dev_err", ctypes.c_void_p),
         ("ckpt_lp", ctypes.c_void_p), ("lp_dtype", ctypes.c_int32), ("reserved2", ctypes.c_int32),
         ("n_groups", ctypes.c_int32), ("reserved3", ctypes.c_int32), ("kq_scratch", ctypes.c_void_p),
+        ("ckpt_lp_scale", ctypes.c_void_p),
     ]
 
 
@@ -127,6 +129,9 @@ def load():
         fn.argtypes = [P(StepArgs), ctypes.c_void_p]
     lib.conventional_decode.restype = ctypes.c_int
     lib.conventional_decode.argtypes = [P(StepArgs), ctypes.c_int, ctypes.c_void_p]
+    lib.replayssm_seed_read_copy.restype = ctypes.c_int
+    lib.replayssm_seed_read_copy.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.replayssm_status_string.restype = ctypes.c_char_p
     lib.replayssm_status_string.argtypes = [ctypes.c_int]
     got = lib.replayssm_abi_version()
@@ -211,7 +216,7 @@ def _torch():
 
 def _dtype_code(t):
     torch = _torch()
-    m = {torch.float32: RS_F32, torch.float16: RS_F16, torch.bfloat16: RS_BF16}
+    m = {torch.float32: RS_F32, torch.float16: RS_F16, torch.bfloat16: RS_BF16, torch.float8_e4m3fn: RS_F8E4M3}
     if t.dtype not in m:
         raise TypeError(f"unsupported dtype {t.dtype}")
     return m[t.dtype]
@@ -239,7 +244,7 @@ def _rows(t, name, H, d):
 
 def _fill(args, *, variant, ckpt, slot_idx, v, k, q, alpha, out, beta=None, ring_v=None, ring_k=None,
           ring_a=None, write_pos=None, is_flush=None, dev_err=None, ckpt_lp=None, kq_scratch=None,
-          library_scratch=False):
+          library_scratch=False, ckpt_lp_scale=None):
     torch = _torch()
     _need(ckpt, "ckpt", ndim=4)
     if not ckpt.is_contiguous():
@@ -327,6 +332,13 @@ def _fill(args, *, variant, ckpt, slot_idx, v, k, q, alpha, out, beta=None, ring
         args.ckpt_lp, args.lp_dtype = ckpt_lp.data_ptr(), _dtype_code(ckpt_lp)
     else:
         args.ckpt_lp, args.lp_dtype = None, 0
+    if ckpt_lp_scale is not None:
+        _need(ckpt_lp_scale, "ckpt_lp_scale", torch.float32)
+        if not ckpt_lp_scale.is_contiguous() or ckpt_lp_scale.shape != ckpt.shape[:3]:
+            raise ValueError("ckpt_lp_scale must be contiguous float32 [num_slots, H, d_v]")
+        args.ckpt_lp_scale = ckpt_lp_scale.data_ptr()
+    else:
+        args.ckpt_lp_scale = None
     return args
 
 
@@ -337,16 +349,41 @@ def _stream(stream):
 
 
 def replayssm_decode_mamba2(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos, is_flush, v, k, q, alpha,
-                            out, dev_err=None, stream=None, ckpt_lp=None, kq_scratch=None):
+                            out, dev_err=None, stream=None, ckpt_lp=None, kq_scratch=None, ckpt_lp_scale=None):
     """One ReplaySSM Mamba-2 decode step in place on ckpt and the rings; o in
-    ``out``.  ``ckpt_lp`` (fp16 or bf16, shape of ckpt) makes ckpt the
-    recurrence copy of a two-precision checkpoint and ckpt_lp its read copy.
-    k and q of shape [B, G, d_k] (G < H groups) select group-shared keys,
-    with ring_k [slots, G, L, d_k] and a float32 ``kq_scratch`` of B * G * L."""
+    ``out``.  ``ckpt_lp`` (fp16, bf16 or float8_e4m3fn, shape of ckpt) makes
+    ckpt the recurrence copy of a two-precision checkpoint and ckpt_lp its
+    read copy; an E4M3 copy takes its row scales in ``ckpt_lp_scale``
+    (float32 [slots, H, d_v]).  k and q of shape [B, G, d_k] (G < H groups)
+    select group-shared keys, with ring_k [slots, G, L, d_k] and a float32
+    ``kq_scratch`` of B * G * L."""
     args = _fill(StepArgs(), variant=RS_MAMBA2, ckpt=ckpt, slot_idx=slot_idx, v=v, k=k, q=q, alpha=alpha,
                  out=out, ring_v=ring_v, ring_k=ring_k, ring_a=ring_a, write_pos=write_pos,
-                 is_flush=is_flush, dev_err=dev_err, ckpt_lp=ckpt_lp, kq_scratch=kq_scratch)
+                 is_flush=is_flush, dev_err=dev_err, ckpt_lp=ckpt_lp, kq_scratch=kq_scratch,
+                 ckpt_lp_scale=ckpt_lp_scale)
     return _check(load().replayssm_decode_mamba2(ctypes.byref(args), _stream(stream)), "replayssm_decode_mamba2")
+
+
+def replayssm_seed_read_copy(*, ckpt, ckpt_lp, scale=None, stream=None):
+    """Cast the recurrence copy ``ckpt`` (float32, last dim d_k) into its read
+    copy ``ckpt_lp`` (same shape; fp16, bf16 or float8_e4m3fn, the last with
+    its row scales in ``scale``, float32 of shape ckpt.shape[:-1])."""
+    torch = _torch()
+    _need(ckpt, "ckpt", torch.float32)
+    _need(ckpt_lp, "ckpt_lp")
+    if not ckpt.is_contiguous() or not ckpt_lp.is_contiguous() or ckpt_lp.shape != ckpt.shape:
+        raise ValueError("ckpt and ckpt_lp must be contiguous with one shape")
+    d_k = ckpt.shape[-1]
+    n_rows = ckpt.numel() // d_k
+    lp = _dtype_code(ckpt_lp)
+    sp = None
+    if lp == RS_F8E4M3:
+        _need(scale, "scale", torch.float32)
+        if not scale.is_contiguous() or scale.shape != ckpt.shape[:-1]:
+            raise ValueError("scale must be contiguous float32 of shape ckpt.shape[:-1]")
+        sp = scale.data_ptr()
+    return _check(load().replayssm_seed_read_copy(ckpt.data_ptr(), n_rows, d_k, lp, ckpt_lp.data_ptr(), sp,
+                                                  _stream(stream)), "replayssm_seed_read_copy")
 
 
 def replayssm_decode_mamba2_noalloc(*, ckpt, ring_v, ring_k, ring_a, slot_idx, write_pos, is_flush, v, k, q,

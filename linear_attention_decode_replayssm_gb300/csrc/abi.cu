@@ -173,10 +173,16 @@ int validate(const rs_step_args *a, bool replay, bool gdn) {
     if (!aligned4(a->kq_scratch)) return RS_EALIGN;
   }
   if (a->ckpt_lp) {
-    // two-precision checkpoint: Mamba-2 replay, fp32 recurrence copy, 16-bit read copy
+    // two-precision checkpoint: Mamba-2 replay, fp32 recurrence copy, 16-bit
+    // or E4M3 (row-scaled) read copy
     if (!replay || gdn) return RS_EUNSUPPORTED;
-    if (a->ckpt_dtype != RS_F32 || (a->lp_dtype != RS_F16 && a->lp_dtype != RS_BF16)) return RS_EUNSUPPORTED;
+    if (a->ckpt_dtype != RS_F32 || (a->lp_dtype != RS_F16 && a->lp_dtype != RS_BF16 && a->lp_dtype != RS_F8E4M3))
+      return RS_EUNSUPPORTED;
     if (!aligned16(a->ckpt_lp)) return RS_EALIGN;
+    if ((a->lp_dtype == RS_F8E4M3) != (a->ckpt_lp_scale != nullptr)) return RS_EINVAL;  // scales with E4M3 only
+    if (a->ckpt_lp_scale && !aligned16(a->ckpt_lp_scale)) return RS_EALIGN;
+  } else if (a->ckpt_lp_scale) {
+    return RS_EINVAL;
   }
   return RS_OK;
 }
@@ -202,6 +208,7 @@ rs::KArgs to_kargs(const rs_step_args *a) {
   k.ring_k = a->ring_k;
   k.ring_a = a->ring_a;
   k.ckpt_lp = a->ckpt_lp;
+  k.lp_scale = a->ckpt_lp_scale;
   k.n_groups = a->n_groups;
   k.kq = a->kq_scratch;
   k.out = a->out;
@@ -329,6 +336,19 @@ int replayssm_spec_commit(const int32_t *committed, const uint8_t *is_flush, con
   if (!aligned4(committed) || !aligned4(accepted) || !aligned4(committed_out)) return RS_EALIGN;
   const cudaError_t e = rs::launch_spec_commit(committed, is_flush, accepted, B, L, T, committed_out,
                                                is_flush_out, dev_err, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RS_OK : RS_ECUDA;
+}
+
+int replayssm_seed_read_copy(const float *ckpt, int64_t n_rows, int32_t d_k, int32_t lp_dtype, void *ckpt_lp,
+                             float *scale, rs_stream_t stream) {
+  if (n_rows < 0 || d_k < 8 || d_k > 1024 || d_k % 8) return RS_EINVAL;
+  if (lp_dtype != RS_F16 && lp_dtype != RS_BF16 && lp_dtype != RS_F8E4M3) return RS_EINVAL;
+  if (n_rows == 0) return RS_OK;
+  if (!ckpt || !ckpt_lp || (lp_dtype == RS_F8E4M3 && !scale)) return RS_EINVAL;
+  if (!aligned16(ckpt) || !aligned16(ckpt_lp) || (scale && !aligned4(scale))) return RS_EALIGN;
+  if (n_rows > 0x7fffffffLL * 8) return RS_EINVAL;
+  const cudaError_t e = rs::launch_seed_read_copy(ckpt, n_rows, d_k, lp_dtype, ckpt_lp, scale,
+                                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? RS_OK : RS_ECUDA;
 }
 

@@ -13,6 +13,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,6 +22,7 @@ namespace rs {
 constexpr int kF32 = 0;
 constexpr int kF16 = 1;
 constexpr int kBF16 = 2;
+constexpr int kF8 = 3;  // E4M3, the read copy of a two-precision checkpoint
 
 // Kernel arguments, copied by value into the launch (mirrors rs_step_args).
 struct KArgs {
@@ -32,6 +34,7 @@ struct KArgs {
   const float *alpha, *beta;
   void *ckpt, *ring_v, *ring_k;
   void *ckpt_lp;  // read copy of a two-precision checkpoint, or nullptr
+  float *lp_scale;  // row scales of an E4M3 read copy [slots, H, d_v], or nullptr
   int n_groups;   // 0: a key per head; > 0: keys and queries shared by groups
   float *kq;      // [B, n_groups, L] scratch for the group dots k_j . q_t
   float *ring_a, *out;
@@ -473,6 +476,37 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, u
   const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
   hi = *reinterpret_cast<const uint32_t *>(&h);
   lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+}  // namespace rs
+
+namespace rs {
+
+// ---------------------------------------------------------------------------
+// E4M3 read copy: each state row on a power-of-two scale 2^e, e the smallest
+// integer with max |row| <= 448 * 2^e; codes rounded to nearest even with
+// saturation, column c of a row at byte c
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int e4m3_row_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int k;
+  const float m = frexpf(amax, &k);  // amax = m 2^k, 0.5 <= m < 1; 448 = 0.875 2^9
+  return m <= 0.875f ? k - 9 : k - 8;
+}
+
+// four consecutive columns times 2^-e as E4M3 codes, the first in the low byte
+__device__ __forceinline__ uint32_t e4m3_pack4(float a, float b, float c, float d, int e) {
+  const __nv_fp8x2_storage_t lo =
+      __nv_cvt_float2_to_fp8x2(make_float2(ldexpf(a, -e), ldexpf(b, -e)), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi =
+      __nv_cvt_float2_to_fp8x2(make_float2(ldexpf(c, -e), ldexpf(d, -e)), __NV_SATFINITE, __NV_E4M3);
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// two E4M3 codes (the low byte first) widened to fp32
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t w16) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w16 & 0xffffu), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
 }  // namespace rs

@@ -44,6 +44,11 @@ using RingHeadFn = uint32_t (*)(int nsr, int nsc);
 cudaError_t plan_rings(const void *kernel, int threads, size_t ck_bytes, size_t rec_bytes, RingHeadFn head,
                        int units, RingPlan *out);
 
+// The read copy of a two-precision checkpoint cast from its recurrence copy
+// (materialize.cu): n_rows rows of d_k fp32 values.
+cudaError_t launch_seed_read_copy(const float *ckpt, int64_t n_rows, int d_k, int lp_dtype, void *ckpt_lp, float *scale,
+                                  cudaStream_t s);
+
 // Raise a kernel's dynamic shared-memory limit (once per device and kernel)
 // when a launch needs more than the 48 KiB default.
 cudaError_t ensure_smem(const void *kernel, size_t bytes);

@@ -56,32 +56,39 @@ namespace rs {
 // there are more of them, and the checkpoint slots turn over at the speed of
 // the memory system rather than of the arithmetic.
 struct M2Rec {
-  uint32_t k, v, q, a, meta, scr, bytes;
+  uint32_t k, v, q, a, meta, scr, scl, bytes;
 };
 
-__host__ __device__ inline M2Rec m2_rec(int DV, int DK, int rec_es, int L) {
+// scl_bytes: row scales of an E4M3 read copy (0 for other kernels)
+__host__ __device__ inline M2Rec m2_rec(int DV, int DK, int rec_es, int L, int scl_bytes = 0) {
   M2Rec s;
   uint32_t o = 0;
   s.k = o;    o = align128(o + L * DK * rec_es);   // records 0..p, current token at p
   s.v = o;    o = align128(o + L * DV * rec_es);
   s.q = o;    o = align128(o + DK * rec_es);
   s.a = o;    o = align128(o + L * 4);             // decays of records 0..p
-  s.meta = o; o = align128(o + 16);                // slot, p, flush, status
+  s.meta = o; o = align128(o + 32);                // slot, p, flush, status, read-copy parts
   s.scr = o;  o = align128(o + (2 * L + 2 * DV + 4) * 4);  // w_j, k_j.q, row dots, gamma, window term
+  s.scl = o;  o = align128(o + scl_bytes);
   s.bytes = o;
   return s;
 }
 
-// barriers full/rec_empty[nsr], ck_empty[2 nsc] (a read-copy kernel splits
-// each checkpoint slot into two half-slots) and the abort flag
-__host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(8 * (2 * nsr + 2 * nsc) + 16); }
+// barriers full/rec_empty[nsr], ck_empty[NP nsc] (a read-copy kernel splits
+// each checkpoint slot into NP parts: two for a 16-bit read copy, four for
+// E4M3) and the abort flag
+template <int NP>
+__host__ __device__ inline uint32_t m2_head(int nsr, int nsc) { return align128(8 * (2 * nsr + NP * nsc) + 16); }
 // with a window warp: one more barrier per record slot (window terms ready)
-__host__ __device__ inline uint32_t m2_head_ww(int nsr, int nsc) { return align128(8 * (3 * nsr + 2 * nsc) + 16); }
+template <int NP>
+__host__ __device__ inline uint32_t m2_head_ww(int nsr, int nsc) { return align128(8 * (3 * nsr + NP * nsc) + 16); }
 
 
 // LMAX bounds the buffer length at compile time (L <= LMAX): loops over a
 // window's records unroll to a fixed count with predicated bodies.
-// TL is the read-copy type of a two-precision checkpoint (TL == TC: one copy).
+// TL is the read-copy type of a two-precision checkpoint (TL == TC: one copy):
+// fp16 or bf16, or E4M3 (__nv_fp8_e4m3) with a power-of-two scale per state
+// row in a.lp_scale.
 // GRP: group-shared keys and queries (k, q [B, G, d_k], ring_k [slots, G, L,
 // d_k]); the window's k_j . q_t were computed once per group by
 // mamba2_group_kq_kernel into a.kq, and non-flush units read those instead of
@@ -100,6 +107,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
     mamba2_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr bool TWO = !std::is_same<TC, TL>::value;
+  constexpr bool F8 = std::is_same<TL, __nv_fp8_e4m3>::value;
   constexpr int E = V::E;
   constexpr int NCH = DK / E;        // 16-byte chunks per state row
   constexpr int G = NCH / CPR;       // lanes per state row
@@ -112,7 +120,12 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
   constexpr int PROD = NGRP * NCW + (WW ? 1 : 0);  // warp index of the producer
   constexpr uint32_t CKB = DV * DK * (uint32_t)sizeof(TC);
   constexpr uint32_t CKB_LP = DV * DK * (uint32_t)sizeof(TL);
-  static_assert(!TWO || (E == 4 && sizeof(TL) == 2), "read copy: 16-bit elements under an fp32 checkpoint");
+  // a read-copy kernel's checkpoint slot holds NPART read copies, or one
+  // flush row's fp32 rows in NPART row blocks
+  constexpr int NPART = TWO ? (int)(CKB / CKB_LP) : 1;
+  constexpr int NPH = NPART > 2 ? NPART : 2;  // ck_empty barriers per slot in the head
+  static_assert(NPART <= 4, "at most four parts per checkpoint slot");
+  static_assert(!TWO || (E == 4 && (sizeof(TL) == 2 || F8)), "read copy: 16-bit or E4M3 under an fp32 checkpoint");
   // flush fold on the tensor cores: fp32 or fp16 checkpoint, one warp per 16
   // state rows
   constexpr bool MMAF = (std::is_same<TC, float>::value || std::is_same<TC, __half>::value) && DV == 16 * NCW &&
@@ -120,16 +133,17 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
   static_assert(G <= 32 && 32 % G == 0 && NCH % CPR == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && DV % RPP == 0 && VPT >= 1 && VPT <= G, "bad tiling");
   static_assert(DK % 8 == 0 && DV % 8 == 0, "head dims must be multiples of 8");
+  static_assert(!F8 || (MMAF && WW), "an E4M3 read copy runs with the window warp and the tensor-core fold");
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // per record slot: all bytes of a unit landed
   uint64_t *rec_empty = full + nsr;                     // per record slot: the unit is done
   uint64_t *ck_empty = rec_empty + nsr;                 // per checkpoint slot: consumers hold it in registers
-  uint64_t *ready = ck_empty + 2 * nsc;                 // per record slot: window terms written (WW)
+  uint64_t *ready = ck_empty + NPH * nsc;               // per record slot: window terms written (WW)
   int *s_abort = reinterpret_cast<int *>(ready + (WW ? nsr : 0));
   const int L = a.L;
-  const M2Rec lay = m2_rec(DV, DK, RES, L);
-  unsigned char *ck_slots = smem + (WW ? m2_head_ww(nsr, nsc) : m2_head(nsr, nsc));
+  const M2Rec lay = m2_rec(DV, DK, RES, L, F8 ? DV * 4 : 0);
+  unsigned char *ck_slots = smem + (WW ? m2_head_ww<NPH>(nsr, nsc) : m2_head<NPH>(nsr, nsc));
   unsigned char *rec_slots = ck_slots + (size_t)nsc * CKB;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -149,7 +163,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
       mbar_init(&rec_empty[s], NC + (WW ? 32 : 0));  // every thread of the consuming group (+ window warp)
       if (WW) mbar_init(&ready[s], 32);
     }
-    for (int c = 0; c < (TWO ? 2 * nsc : nsc); ++c) mbar_init(&ck_empty[c], NC);
+    for (int c = 0; c < NPART * nsc; ++c) mbar_init(&ck_empty[c], NC);
     *s_abort = 0;
     mbar_init_fence();
   }
@@ -173,11 +187,11 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
     int c_sl, c_wp, c_fl;
     int ps = 0, pc = 0;         // record and checkpoint slot of unit `it`
     uint32_t phs = 0, phc = 0;  // parity of it / nsr and it / nsc
-    // read-copy kernels: a ring of 2 nsc half-slots (CKB_LP bytes each); a
-    // non-flush row's read copy takes one, a flush row's fp32 rows take two
-    // (rows 0 .. DV/2 - 1, then the rest); per half-slot: used yet, and the
-    // parity of its use count
-    const int nhs = 2 * nsc;
+    // read-copy kernels: a ring of NPART nsc parts (CKB_LP bytes each); a
+    // non-flush row's read copy takes one, a flush row's fp32 rows take
+    // NPART (row blocks of DV / NPART rows, in order); per part: used yet,
+    // and the parity of its use count
+    const int nhs = NPART * nsc;
     int hc = 0;
     uint32_t hused = 0, hpar = 0;
     fetch(blockIdx.x, c_sl, c_wp, c_fl);
@@ -192,24 +206,28 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
         const int p = __shfl_sync(0xffffffffu, c_wp, j);
         const int fl = __shfl_sync(0xffffffffu, c_fl, j);
         const int s = ps, c = pc;
-        int h0 = -1, h1 = -1;  // half-slots of this unit (read-copy kernels)
+        int hp[4] = {-1, -1, -1, -1};  // parts of this unit (read-copy kernels)
         if constexpr (TWO) {
           if (slot >= 0 && slot < a.num_slots && p >= 0 && p < L) {
-            h0 = hc;
-            hc = hc + 1 == nhs ? 0 : hc + 1;
-            if (fl) {
-              h1 = hc;
-              hc = hc + 1 == nhs ? 0 : hc + 1;
+#pragma unroll
+            for (int k = 0; k < NPART; ++k) {
+              if (k == 0 || fl) {
+                hp[k] = hc;
+                hc = hc + 1 == nhs ? 0 : hc + 1;
+              }
             }
           }
         }
-        if (it >= nsr || (TWO ? h0 >= 0 : it >= nsc)) {
+        if (it >= nsr || (TWO ? hp[0] >= 0 : it >= nsc)) {
           int w = 1;
           if (lane == 0) {
             if (it >= nsr) w = mbar_wait(&rec_empty[s], phs ^ 1u) ? 1 : 0;
             if constexpr (TWO) {
-              if (w && h0 >= 0 && ((hused >> h0) & 1u)) w = mbar_wait(&ck_empty[h0], ((hpar >> h0) & 1u) ^ 1u) ? 1 : 0;
-              if (w && h1 >= 0 && ((hused >> h1) & 1u)) w = mbar_wait(&ck_empty[h1], ((hpar >> h1) & 1u) ^ 1u) ? 1 : 0;
+#pragma unroll
+              for (int k = 0; k < NPART; ++k) {
+                const int h = hp[k];
+                if (w && h >= 0 && ((hused >> h) & 1u)) w = mbar_wait(&ck_empty[h], ((hpar >> h) & 1u) ^ 1u) ? 1 : 0;
+              }
             } else {
               if (w && it >= nsc) w = mbar_wait(&ck_empty[c], phc ^ 1u) ? 1 : 0;
             }
@@ -223,13 +241,12 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
         }
         __syncwarp();
         if constexpr (TWO) {
-          if (h0 >= 0) {
-            hused |= 1u << h0;
-            hpar ^= 1u << h0;
-          }
-          if (h1 >= 0) {
-            hused |= 1u << h1;
-            hpar ^= 1u << h1;
+#pragma unroll
+          for (int k = 0; k < NPART; ++k) {
+            if (hp[k] >= 0) {
+              hused |= 1u << hp[k];
+              hpar ^= 1u << hp[k];
+            }
           }
         }
         const int b = u / a.H, h = u - (u / a.H) * a.H;
@@ -248,19 +265,22 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
           const size_t unit = (size_t)slot * a.H + h;
           if (lane == 0) {
             meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
-            meta[4] = h0; meta[5] = h1;
+            meta[4] = hp[0]; meta[5] = hp[1]; meta[6] = hp[2]; meta[7] = hp[3];
             const TC *ck32 = static_cast<const TC *>(a.ckpt) + unit * (DV * DK);
             if constexpr (TWO) {
               if (!fl) {
                 // a two-precision non-flush row reads only the read copy
                 mbar_expect_tx(&full[s], CKB_LP);
-                bulk_load(ck_slots + (size_t)h0 * CKB_LP, static_cast<const TL *>(a.ckpt_lp) + unit * (DV * DK),
-                          CKB_LP, &full[s], pol_stream);
+                bulk_load(ck_slots + (size_t)hp[0] * CKB_LP,
+                          static_cast<const unsigned char *>(a.ckpt_lp) + unit * (size_t)CKB_LP, CKB_LP, &full[s],
+                          pol_stream);
               } else {
-                static_assert(CKB == 2 * CKB_LP, "an fp32 checkpoint fills two half-slots");
+                static_assert(CKB == NPART * CKB_LP, "an fp32 checkpoint fills NPART parts");
                 mbar_expect_tx(&full[s], CKB);
-                bulk_load(ck_slots + (size_t)h0 * CKB_LP, ck32, CKB_LP, &full[s], pol_stream);
-                bulk_load(ck_slots + (size_t)h1 * CKB_LP, ck32 + (DV / 2) * DK, CKB_LP, &full[s], pol_stream);
+#pragma unroll
+                for (int k = 0; k < NPART; ++k)
+                  bulk_load(ck_slots + (size_t)hp[k] * CKB_LP, ck32 + k * (DV / NPART) * DK, CKB_LP, &full[s],
+                            pol_stream);
               }
             } else {
               mbar_expect_tx(&full[s], CKB);
@@ -311,9 +331,13 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
             if (jj < p) cp_async4(sa + jj, a.ring_a + unit * L + jj);
           }
           if (lane == 31) cp_async4(sa + p, a.alpha + (size_t)b * a.H + h);
+          if constexpr (F8) {
+            // a non-flush row's read copy comes with its row scales
+            if (!fl && lane < DV / 4) cp_async16(st + lay.scl + lane * 16, a.lp_scale + unit * DV + lane * 4);
+          }
         } else if (lane == 0) {
           meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
-          meta[4] = -1; meta[5] = -1;
+          meta[4] = -1; meta[5] = -1; meta[6] = -1; meta[7] = -1;
         }
         if (lane == 0) mbar_arrive(&full[s]);  // releases the meta words
         cp_async_arrive(&full[s]);
@@ -492,7 +516,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
     if (status != kStatusOk) {
       for (int i = ctid; i < DV; i += NC) orow[i] = 0.f;
       if (ctid == 0 && status != kStatusPad) report(a.dev_err, status == kStatusBadSlot ? 1 : 2);
-      if (!TWO) mbar_arrive(&ck_empty[c]);  // a read-copy kernel gave the unit no half-slot
+      if (!TWO) mbar_arrive(&ck_empty[c]);  // a read-copy kernel gave the unit no part
       mbar_arrive(&rec_empty[s]);
       continue;
     }
@@ -501,28 +525,33 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
     float *scr = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + lay.scr);
     float *sW = scr, *sS = scr + L, *sC = scr + 2 * L, *sGam = scr + 2 * L + DV, *sY = sGam + 4;
     const unsigned char *sk = st + lay.k, *sv = st + lay.v;
-    // the unit's checkpoint slot; a read-copy kernel names its half-slot(s)
-    // in the metadata: the read copy in one, or the fp32 rows 0 .. DV/2 - 1
-    // and DV/2 .. DV - 1 of a flush row in two
-    int hs0 = c, hs1 = -1;
+    // the unit's checkpoint slot; a read-copy kernel names its parts in the
+    // metadata: the read copy in one, or a flush row's fp32 row blocks of
+    // DV / NPART rows in NPART
+    int hs[4] = {c, -1, -1, -1};
     if constexpr (TWO) {
-      const int2 hm = *reinterpret_cast<const int2 *>(st + lay.meta + 16);
-      hs0 = hm.x;
-      hs1 = hm.y;
+      const int4 hm = *reinterpret_cast<const int4 *>(st + lay.meta + 16);
+      hs[0] = hm.x; hs[1] = hm.y; hs[2] = hm.z; hs[3] = hm.w;
     }
-    const unsigned char *ck_slot = ck_slots + (size_t)hs0 * (TWO ? CKB_LP : CKB);
+    const unsigned char *ck_slot = ck_slots + (size_t)hs[0] * (TWO ? CKB_LP : CKB);
     // fp32 state row r of a flush row
     auto ck_row = [&](int r) -> const unsigned char * {
       if constexpr (TWO) {
-        return r < DV / 2 ? ck_slot + (size_t)r * DK * sizeof(TC)
-                          : ck_slots + (size_t)hs1 * CKB_LP + (size_t)(r - DV / 2) * DK * sizeof(TC);
+        constexpr int RB = DV / NPART;  // rows per part
+        const int k = r / RB;
+        const int hk = k == 0 ? hs[0] : k == 1 ? hs[1] : k == 2 ? hs[2] : hs[3];
+        return ck_slots + (size_t)hk * CKB_LP + (size_t)(r - k * RB) * DK * sizeof(TC);
       } else {
         return ck_slot + (size_t)r * DK * sizeof(TC);
       }
     };
     auto release_ck = [&]() {
-      mbar_arrive(&ck_empty[hs0]);
-      if (TWO && hs1 >= 0) mbar_arrive(&ck_empty[hs1]);
+      mbar_arrive(&ck_empty[hs[0]]);
+      if constexpr (TWO) {
+#pragma unroll
+        for (int k = 1; k < NPART; ++k)
+          if (hs[k] >= 0) mbar_arrive(&ck_empty[hs[k]]);
+      }
     };
 
     // window weights w_j (suffix products of the decays) and gamma
@@ -547,130 +576,169 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
 
     float part[VPT];
     if (!flush) {
-      // take this thread's share of the checkpoint (the read copy of a
-      // two-precision checkpoint) into registers and hand the slot straight
-      // back to the producer
-      using Raw = typename std::conditional<TWO, uint2, uint4>::type;
-      Raw raw[VPT][CPR];
+      if constexpr (F8) {
+        // E4M3 read copy: a lane holds 16 codes (16 columns) of each of its
+        // rows, G8 lanes a row; the row's power-of-two scale is applied to
+        // the finished row dot
+        constexpr int G8 = DK / 16;       // lanes per state row
+        constexpr int RPP8 = NC / G8;     // rows per pass of the group
+        constexpr int VPT8 = DV / RPP8;   // rows per lane
+        static_assert(G8 <= 32 && 32 % G8 == 0 && DV % RPP8 == 0 && VPT8 >= 1 && VPT8 <= G8, "E4M3 tiling");
+        const int r8 = ctid / G8, c8 = ctid - (ctid / G8) * G8;
+        uint4 raw8[VPT8];
 #pragma unroll
-      for (int r = 0; r < VPT; ++r)
+        for (int r = 0; r < VPT8; ++r) raw8[r] = reinterpret_cast<const uint4 *>(ck_slot)[(r8 + r * RPP8) * G8 + c8];
+        release_ck();
+        float q16[16];
+        lds_cols<16>(st + lay.q, 16 * c8, RDT, q16);
+        float p8[VPT8];
 #pragma unroll
-        for (int i = 0; i < CPR; ++i)
-          raw[r][i] = reinterpret_cast<const Raw *>(ck_slot)[(row0 + r * RPP) * NCH + cv + G * i];
-      release_ck();
-      weights();
-      float qv[CPR][E];
+        for (int r = 0; r < VPT8; ++r) {
+          const uint32_t w4[4] = {raw8[r].x, raw8[r].y, raw8[r].z, raw8[r].w};
+          float acc = 0.f;
 #pragma unroll
-      for (int i = 0; i < CPR; ++i) lds_cols<E>(st + lay.q, (cv + G * i) * E, RDT, qv[i]);
-      // s_j = k_j . q: a warp takes records four at a time; each lane holds
-      // its 4-column chunk of q and accumulates four partial dots, and one
-      // transposed reduction finishes the chunk (group-shared keys: the
-      // producer brought the group's dots instead)
-      if constexpr (!GRP && !WW) {
-        constexpr int QPL = (DK + 127) / 128;  // 4-column chunks of q per lane
-        float qq[QPL][4];
-#pragma unroll
-        for (int i = 0; i < QPL; ++i) {
-          if (lane * 4 + i * 128 < DK) {
-            lds_cols<4>(st + lay.q, lane * 4 + i * 128, RDT, qq[i]);
-          } else {
-            qq[i][0] = qq[i][1] = qq[i][2] = qq[i][3] = 0.f;
+          for (int wi = 0; wi < 4; ++wi) {
+            const float2 lo = e4m3x2_to_f2(w4[wi]), hi = e4m3x2_to_f2(w4[wi] >> 16);
+            acc = fmaf(lo.x, q16[4 * wi], fmaf(lo.y, q16[4 * wi + 1], fmaf(hi.x, q16[4 * wi + 2], fmaf(hi.y, q16[4 * wi + 3], acc))));
           }
+          p8[r] = acc;
         }
-#pragma unroll
-        for (int ci = 0; ci < (LMAX / 4 + NCW - 1) / NCW; ++ci) {
-          const int ch = lw + ci * NCW;
-          if (ch * 4 > p) break;
-          float part4[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int j = ch * 4 + r;
-            float acc = 0.f;
-            if (j <= p) {
-#pragma unroll
-              for (int i = 0; i < QPL; ++i) {
-                const int cc = lane * 4 + i * 128;
-                if (cc < DK) {
-                  float kk[4];
-                  lds_cols<4>(sk, j * DK + cc, RDT, kk);
-                  acc = fmaf(kk[0], qq[i][0], fmaf(kk[1], qq[i][1], fmaf(kk[2], qq[i][2], fmaf(kk[3], qq[i][3], acc))));
-                }
-              }
-            }
-            part4[r] = acc;
-          }
-          group_reduce<4, 32>(part4, lane);
-          if (group_reduce_writer<4, 32>(lane)) {
-            const int j = ch * 4 + group_reduce_index<4, 32>(lane);
-            if (j <= p) sS[j] = part4[0];
-          }
-        }
-      }
-      // checkpoint GEMV partials from the stage
-#pragma unroll
-      for (int r = 0; r < VPT; ++r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < CPR; ++i) {
-          float f[E];
-          if constexpr (TWO) {
-            LpVec<TL>::unpack(raw[r][i], f);
-          } else {
-            V::unpack(raw[r][i], f);
-          }
-#pragma unroll
-          for (int e = 0; e < E; ++e) acc = fmaf(f[e], qv[i][e], acc);
-        }
-        part[r] = acc;
-      }
-      group_reduce<VPT, G>(part, lane);
-      if constexpr (WW) {
-        // o = gamma c + the window warp's sum_j w_j s_j v_j, by the lane that
-        // finished the row
+        group_reduce<VPT8, G8>(p8, lane);
         if (!window_ready()) {
           fail();
           break;
         }
-        if (group_reduce_writer<VPT, G>(lane)) {
-          const int row = row0 + group_reduce_index<VPT, G>(lane) * RPP;
-          orow[row] = fmaf(sGam[0], part[0], sY[row]);
+        if (group_reduce_writer<VPT8, G8>(lane)) {
+          const int row = r8 + group_reduce_index<VPT8, G8>(lane) * RPP8;
+          const float *scl = reinterpret_cast<const float *>(st + lay.scl);
+          orow[row] = fmaf(sGam[0] * scl[row], p8[0], sY[row]);
         }
       } else {
-        if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
-        gsync();
-      }
-
-      // o = gamma c + sum_j w_j s_j v_j, by one warp: a lane covers 8 output
-      // rows (one 16-byte load of a v record) for every OG-th record, then
-      // lanes sharing rows add up; the other warps append the record
-      if (!WW && lw == 0) {
-        constexpr int RG = DV / 8;   // 8-row groups
-        constexpr int OG = 32 / RG;  // record groups
-        static_assert(DV % 8 == 0 && 32 % RG == 0 && OG >= 1, "bad output layout");
-        const int rg = lane % RG, og = lane / RG;
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-        for (int i = 0; i < (LMAX + OG - 1) / OG; ++i) {
-          const int j = og + i * OG;
-          if (j <= p) {
-            const float cj = sW[j] * sS[j];
-            float vv[8];
-            lds_cols<8>(sv, j * DV + rg * 8, RDT, vv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(cj, vv[e], acc[e]);
+        // take this thread's share of the checkpoint (the read copy of a
+        // two-precision checkpoint) into registers and hand the slot straight
+        // back to the producer
+        using Raw = typename std::conditional<TWO, uint2, uint4>::type;
+        Raw raw[VPT][CPR];
+  #pragma unroll
+        for (int r = 0; r < VPT; ++r)
+  #pragma unroll
+          for (int i = 0; i < CPR; ++i)
+            raw[r][i] = reinterpret_cast<const Raw *>(ck_slot)[(row0 + r * RPP) * NCH + cv + G * i];
+        release_ck();
+        weights();
+        float qv[CPR][E];
+  #pragma unroll
+        for (int i = 0; i < CPR; ++i) lds_cols<E>(st + lay.q, (cv + G * i) * E, RDT, qv[i]);
+        // s_j = k_j . q: a warp takes records four at a time; each lane holds
+        // its 4-column chunk of q and accumulates four partial dots, and one
+        // transposed reduction finishes the chunk (group-shared keys: the
+        // producer brought the group's dots instead)
+        if constexpr (!GRP && !WW) {
+          constexpr int QPL = (DK + 127) / 128;  // 4-column chunks of q per lane
+          float qq[QPL][4];
+  #pragma unroll
+          for (int i = 0; i < QPL; ++i) {
+            if (lane * 4 + i * 128 < DK) {
+              lds_cols<4>(st + lay.q, lane * 4 + i * 128, RDT, qq[i]);
+            } else {
+              qq[i][0] = qq[i][1] = qq[i][2] = qq[i][3] = 0.f;
+            }
+          }
+  #pragma unroll
+          for (int ci = 0; ci < (LMAX / 4 + NCW - 1) / NCW; ++ci) {
+            const int ch = lw + ci * NCW;
+            if (ch * 4 > p) break;
+            float part4[4];
+  #pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int j = ch * 4 + r;
+              float acc = 0.f;
+              if (j <= p) {
+  #pragma unroll
+                for (int i = 0; i < QPL; ++i) {
+                  const int cc = lane * 4 + i * 128;
+                  if (cc < DK) {
+                    float kk[4];
+                    lds_cols<4>(sk, j * DK + cc, RDT, kk);
+                    acc = fmaf(kk[0], qq[i][0], fmaf(kk[1], qq[i][1], fmaf(kk[2], qq[i][2], fmaf(kk[3], qq[i][3], acc))));
+                  }
+                }
+              }
+              part4[r] = acc;
+            }
+            group_reduce<4, 32>(part4, lane);
+            if (group_reduce_writer<4, 32>(lane)) {
+              const int j = ch * 4 + group_reduce_index<4, 32>(lane);
+              if (j <= p) sS[j] = part4[0];
+            }
           }
         }
-#pragma unroll
-        for (int off = RG; off < 32; off <<= 1) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+        // checkpoint GEMV partials from the stage
+  #pragma unroll
+        for (int r = 0; r < VPT; ++r) {
+          float acc = 0.f;
+  #pragma unroll
+          for (int i = 0; i < CPR; ++i) {
+            float f[E];
+            if constexpr (TWO) {
+              LpVec<TL>::unpack(raw[r][i], f);
+            } else {
+              V::unpack(raw[r][i], f);
+            }
+  #pragma unroll
+            for (int e = 0; e < E; ++e) acc = fmaf(f[e], qv[i][e], acc);
+          }
+          part[r] = acc;
         }
-        if (og == 0) {
-          const float gam = sGam[0];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) orow[rg * 8 + e] = fmaf(gam, sC[rg * 8 + e], acc[e]);
+        group_reduce<VPT, G>(part, lane);
+        if constexpr (WW) {
+          // o = gamma c + the window warp's sum_j w_j s_j v_j, by the lane that
+          // finished the row
+          if (!window_ready()) {
+            fail();
+            break;
+          }
+          if (group_reduce_writer<VPT, G>(lane)) {
+            const int row = row0 + group_reduce_index<VPT, G>(lane) * RPP;
+            orow[row] = fmaf(sGam[0], part[0], sY[row]);
+          }
+        } else {
+          if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
+          gsync();
+        }
+
+        // o = gamma c + sum_j w_j s_j v_j, by one warp: a lane covers 8 output
+        // rows (one 16-byte load of a v record) for every OG-th record, then
+        // lanes sharing rows add up; the other warps append the record
+        if (!WW && lw == 0) {
+          constexpr int RG = DV / 8;   // 8-row groups
+          constexpr int OG = 32 / RG;  // record groups
+          static_assert(DV % 8 == 0 && 32 % RG == 0 && OG >= 1, "bad output layout");
+          const int rg = lane % RG, og = lane / RG;
+          float acc[8];
+  #pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  #pragma unroll
+          for (int i = 0; i < (LMAX + OG - 1) / OG; ++i) {
+            const int j = og + i * OG;
+            if (j <= p) {
+              const float cj = sW[j] * sS[j];
+              float vv[8];
+              lds_cols<8>(sv, j * DV + rg * 8, RDT, vv);
+  #pragma unroll
+              for (int e = 0; e < 8; ++e) acc[e] = fmaf(cj, vv[e], acc[e]);
+            }
+          }
+  #pragma unroll
+          for (int off = RG; off < 32; off <<= 1) {
+  #pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+          }
+          if (og == 0) {
+            const float gam = sGam[0];
+  #pragma unroll
+            for (int e = 0; e < 8; ++e) orow[rg * 8 + e] = fmaf(gam, sC[rg * 8 + e], acc[e]);
+          }
         }
       }
       // append the current record (k, v verbatim, alpha) at ring slot p; a
@@ -771,6 +839,27 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
       // store S_new (and its read copy), and o = S_new q from the same registers
       TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK);
       float oA = 0.f, oB = 0.f;
+      // an E4M3 read copy: the power-of-two scale of rows rA and rB from
+      // their maxima (the four lanes t4 of a row group hold all its columns)
+      int eA = 0, eB = 0;
+      if constexpr (F8) {
+        float mA = 0.f, mB = 0.f;
+#pragma unroll
+        for (int bk = 0; bk < NB; ++bk) {
+          mA = fmaxf(mA, fmaxf(fmaxf(fabsf(xa[bk].x), fabsf(xa[bk].y)), fmaxf(fabsf(xa[bk].z), fabsf(xa[bk].w))));
+          mB = fmaxf(mB, fmaxf(fmaxf(fabsf(xb[bk].x), fabsf(xb[bk].y)), fmaxf(fabsf(xb[bk].z), fabsf(xb[bk].w))));
+        }
+        mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, 1));
+        mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, 1));
+        mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, 2));
+        mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, 2));
+        eA = e4m3_row_exponent(mA);
+        eB = e4m3_row_exponent(mB);
+        if (t4 == 0) {
+          a.lp_scale[unit * DV + rA] = ldexpf(1.f, eA);
+          a.lp_scale[unit * DV + rB] = ldexpf(1.f, eB);
+        }
+      }
 #pragma unroll
       for (int bk = 0; bk < NB; ++bk) {
         const size_t offA = (size_t)rA * DK + 16 * bk + 4 * t4, offB = (size_t)rB * DK + 16 * bk + 4 * t4;
@@ -783,7 +872,11 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
           st_vec2(ckg + offA, LpVec<__half>::pack(fa));
           st_vec2(ckg + offB, LpVec<__half>::pack(fb));
         }
-        if constexpr (TWO) {
+        if constexpr (F8) {
+          unsigned char *lpg = static_cast<unsigned char *>(a.ckpt_lp) + unit * (DV * DK);
+          *reinterpret_cast<uint32_t *>(lpg + offA) = e4m3_pack4(fa[0], fa[1], fa[2], fa[3], eA);
+          *reinterpret_cast<uint32_t *>(lpg + offB) = e4m3_pack4(fb[0], fb[1], fb[2], fb[3], eB);
+        } else if constexpr (TWO) {
           TL *lpg = static_cast<TL *>(a.ckpt_lp) + unit * (DV * DK);
           st_vec2(lpg + offA, LpVec<TL>::pack(fa));
           st_vec2(lpg + offB, LpVec<TL>::pack(fb));
@@ -969,10 +1062,12 @@ static cudaError_t launch_mamba2_l(const KArgs &a, cudaStream_t s) {
   auto kern = mamba2_replay_kernel<DV, DK, TC, TL, RT, NCW, NGRP, LMAX, GRP, CPR, WW>;
   constexpr int threads = NGRP * NCW * 32 + (WW ? 64 : 32);
   const size_t ckb = (size_t)DV * DK * sizeof(TC);
-  const size_t rb = m2_rec(DV, DK, (int)sizeof(RT), a.L).bytes;
+  constexpr bool F8 = std::is_same<TL, __nv_fp8_e4m3>::value;
+  constexpr int NPH = !std::is_same<TC, TL>::value && sizeof(TC) / sizeof(TL) > 2 ? (int)(sizeof(TC) / sizeof(TL)) : 2;
+  const size_t rb = m2_rec(DV, DK, (int)sizeof(RT), a.L, F8 ? DV * 4 : 0).bytes;
   RingPlan plan;
-  cudaError_t e = plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, WW ? m2_head_ww : m2_head,
-                             a.B * a.H, &plan);
+  cudaError_t e = plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb,
+                             WW ? m2_head_ww<NPH> : m2_head<NPH>, a.B * a.H, &plan);
   if (e != cudaSuccess) return e;
   kern<<<plan.grid, threads, plan.smem, s>>>(a, plan.nsr, plan.nsc);
   return cudaGetLastError();

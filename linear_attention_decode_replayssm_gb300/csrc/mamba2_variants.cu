@@ -16,6 +16,9 @@ static LaunchFn read_copy_t(int d_v, int d_k, int lp_dtype) {
     if (d_v == 16 && d_k == 32) return launch_mamba2<16, 32, float, RT, 4, 1, __nv_bfloat16>;
     if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __nv_bfloat16, 4, false, true>;
     if (d_v == 128 && d_k == 128) return launch_mamba2<128, 128, float, RT, 8, 1, __nv_bfloat16>;
+  } else if (lp_dtype == kF8) {
+    // E4M3 with a power-of-two scale per state row
+    if (d_v == 64 && d_k == 128) return launch_mamba2<64, 128, float, RT, 4, 2, __nv_fp8_e4m3, 4, false, true>;
   }
   return nullptr;
 }
@@ -31,7 +34,7 @@ static LaunchFn grouped_t(int d_v, int d_k, int ckpt_dtype) {
   return nullptr;
 }
 
-// the fp32 checkpoint's read copy (lp_dtype fp16 or bf16)
+// the fp32 checkpoint's read copy (lp_dtype fp16, bf16 or E4M3)
 LaunchFn find_mamba2_read_copy(int d_v, int d_k, int lp_dtype, int in_dtype) {
   return in_dtype == kF32 ? read_copy_t<float>(d_v, d_k, lp_dtype) : read_copy_t<__nv_bfloat16>(d_v, d_k, lp_dtype);
 }

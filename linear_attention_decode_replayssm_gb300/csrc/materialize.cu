@@ -133,6 +133,46 @@ __global__ void __launch_bounds__(NT) materialize_kernel(const rs_materialize_ar
   for (int r = 0; r < VPT; ++r) st_vec(out + (size_t)(row0 + r * RPP) * DK + cv * E, V::pack(f[r]));
 }
 
+// The read copy of a two-precision checkpoint from its recurrence copy: one
+// warp per state row; E4M3 rows on their power-of-two scale.
+__global__ void __launch_bounds__(256) seed_read_copy_kernel(const float *ckpt, int64_t n_rows, int d_k, int lp_dtype,
+                                                             void *ckpt_lp, float *scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= n_rows) return;
+  const float *src = ckpt + row * d_k;
+  const int nq = d_k / 4;  // 4-column groups
+  if (lp_dtype == kF8) {
+    float amax = 0.f;
+    for (int c = lane; c < nq; c += 32) {
+      const float4 x = reinterpret_cast<const float4 *>(src)[c];
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const int e = e4m3_row_exponent(amax);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(ckpt_lp) + row * d_k);
+    for (int c = lane; c < nq; c += 32) {
+      const float4 x = reinterpret_cast<const float4 *>(src)[c];
+      dst[c] = e4m3_pack4(x.x, x.y, x.z, x.w, e);
+    }
+    if (lane == 0) scale[row] = ldexpf(1.f, e);
+  } else {
+    uint2 *dst = reinterpret_cast<uint2 *>(static_cast<unsigned char *>(ckpt_lp) + row * d_k * 2);
+    for (int c = lane; c < nq; c += 32) {
+      const float4 x = reinterpret_cast<const float4 *>(src)[c];
+      const float f[4] = {x.x, x.y, x.z, x.w};
+      dst[c] = lp_dtype == kF16 ? LpVec<__half>::pack(f) : LpVec<__nv_bfloat16>::pack(f);
+    }
+  }
+}
+
+cudaError_t launch_seed_read_copy(const float *ckpt, int64_t n_rows, int d_k, int lp_dtype, void *ckpt_lp, float *scale,
+                                  cudaStream_t s) {
+  seed_read_copy_kernel<<<(unsigned)((n_rows + 7) / 8), 256, 0, s>>>(ckpt, n_rows, d_k, lp_dtype, ckpt_lp, scale);
+  return cudaGetLastError();
+}
+
 template <int DV, int DK, typename TC, int NT, int NSPLIT = 1>
 static cudaError_t launch_mat(const rs_materialize_args &a, int gdn, cudaStream_t s) {
   materialize_kernel<DV, DK, TC, NT, NSPLIT><<<(unsigned)((size_t)a.B * a.H * NSPLIT), NT, 0, s>>>(a, gdn);

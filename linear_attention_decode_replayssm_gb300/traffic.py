@@ -16,7 +16,7 @@ per-head record of "ReplaySSM: an SSM decoder that writes its state once every
 
 import numpy as np
 
-ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
+ESIZE = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
 
 
 def step_bytes(*, variant, H, d_v, d_k, ckpt_dtype, in_dtype, ring_dtype, slot_idx, write_pos=None,
@@ -24,8 +24,8 @@ def step_bytes(*, variant, H, d_v, d_k, ckpt_dtype, in_dtype, ring_dtype, slot_i
     """Bytes one launch moves for the given per-row cursors (NumPy arrays [B]).
 
     With a two-precision checkpoint (``lp_dtype``), a non-flush row reads the
-    read copy instead of the checkpoint, and a flush row reads the checkpoint
-    and writes both copies.  With group-shared keys (``n_groups`` > 0) a row's
+    read copy instead of the checkpoint (with its row scales for E4M3), and a
+    flush row reads the checkpoint and writes both copies.  With group-shared keys (``n_groups`` > 0) a row's
     keys, queries and key records are counted once per group: a record is
     H (d_v + 1 decay) values plus G d_k keys (the group dots exchanged through
     the small scratch between the two kernels are not counted)."""
@@ -48,8 +48,10 @@ def step_bytes(*, variant, H, d_v, d_k, ckpt_dtype, in_dtype, ring_dtype, slot_i
     p = np.asarray(write_pos, dtype=np.int64)[live]
     fl = np.asarray(is_flush)[live] != 0
     n_fl, n_nf = int(fl.sum()), int((~fl).sum())
-    read_nf = state if lp_dtype is None else d_v * d_k * ESIZE[lp_dtype]
-    write_fl = state if lp_dtype is None else state + d_v * d_k * ESIZE[lp_dtype]
+    # an E4M3 read copy carries a 4-byte scale per state row
+    lp_copy = 0 if lp_dtype is None else d_v * d_k * ESIZE[lp_dtype] + (4 * d_v if lp_dtype == "e4m3" else 0)
+    read_nf = state if lp_dtype is None else lp_copy
+    write_fl = state if lp_dtype is None else state + lp_copy
     total += int(p.sum()) * rec_row
     total += n_fl * H * (state + write_fl) + n_nf * (H * read_nf + rec_row)
     return total

@@ -14,7 +14,7 @@ TORCH_DTYPES = {}
 def tdt(name):
     import torch
 
-    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[name]
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}[name]
 
 
 def dev(a, dtype, device="cuda"):
@@ -31,8 +31,14 @@ class GpuRun:
 
         self.lib, self.w, self.conventional = lib, w, conventional
         self.ckpt = dev(w.ckpt0 if ckpt0 is None else ckpt0, tdt(w.ckpt_dtype))
-        # two-precision checkpoint: the read copy starts as the checkpoint cast (RN-even)
-        self.ckpt_lp = None if lp_dtype is None else self.ckpt.to(tdt(lp_dtype))
+        # two-precision checkpoint: the read copy starts as the library's cast
+        # of the checkpoint (RN-even; E4M3 on a power-of-two scale per row)
+        self.ckpt_lp = self.ckpt_lp_scale = None
+        if lp_dtype is not None:
+            self.ckpt_lp = torch.empty(self.ckpt.shape, device="cuda", dtype=tdt(lp_dtype))
+            if lp_dtype == "e4m3":
+                self.ckpt_lp_scale = torch.empty(self.ckpt.shape[:3], device="cuda", dtype=torch.float32)
+            lib.replayssm_seed_read_copy(ckpt=self.ckpt, ckpt_lp=self.ckpt_lp, scale=self.ckpt_lp_scale)
         self.ring_v = dev(w.ring_v0, tdt(w.ring_dtype))
         self.ring_k = dev(w.ring_k0, tdt(w.ring_dtype))
         self.ring_a = dev(w.ring_a0, torch.float32)
@@ -41,6 +47,18 @@ class GpuRun:
         self.wp = torch.empty(w.B, device="cuda", dtype=torch.int32)
         self.fl = torch.empty(w.B, device="cuda", dtype=torch.uint8)
         self.dev_err = torch.zeros(1, device="cuda", dtype=torch.int32)
+
+    def read_copy(self, slots, heads):
+        """The read copy of the given slots and heads as float64 values (an
+        E4M3 copy's codes times its row scales)."""
+        import torch
+
+        sl = torch.as_tensor(np.asarray(slots), device="cuda")
+        hs = torch.as_tensor(np.asarray(heads), device="cuda")
+        x = self.ckpt_lp[sl][:, hs].double()
+        if self.ckpt_lp_scale is not None:
+            x = x * self.ckpt_lp_scale[sl][:, hs].double()[..., None]
+        return x.cpu().numpy()
 
     def tensors(self, x):
         import torch
@@ -70,7 +88,8 @@ class GpuRun:
             lib.replayssm_decode_mamba2(ckpt=self.ckpt, ring_v=self.ring_v, ring_k=self.ring_k,
                                         ring_a=self.ring_a, slot_idx=self.slot_idx, write_pos=self.wp,
                                         is_flush=self.fl, v=t["v"], k=t["k"], q=t["q"], alpha=t["alpha"],
-                                        out=out, dev_err=self.dev_err, ckpt_lp=self.ckpt_lp)
+                                        out=out, dev_err=self.dev_err, ckpt_lp=self.ckpt_lp,
+                                        ckpt_lp_scale=self.ckpt_lp_scale)
         else:
             lib.replayssm_decode_gdn(ckpt=self.ckpt, ring_v=self.ring_v, ring_k=self.ring_k, ring_a=self.ring_a,
                                      slot_idx=self.slot_idx, write_pos=self.wp, is_flush=self.fl, v=t["v"],

@@ -19,7 +19,8 @@ staggered cursors -- and every state precision the kernels take):
     64 (the compile-time window bounds 8, 16, 32 and 64), 128 x 128 and
     16 x 32 heads, bf16 and fp32 inputs; batch 512 at L 16 in fp32 and fp16;
   * the two-precision checkpoint with fp16 and bf16 read copies, both input
-    types and every head shape;
+    types and every head shape, and the E4M3 read copy (64 x 128 heads) at
+    L 16 / 32 / 64;
   * group-shared keys with fp32 and fp16 checkpoints;
   * Gated DeltaNet with fp32 and fp16 checkpoints, fp16 and fp32 rings, L 4 /
     16 / 32, and the batch-256 layer with fp32 rings against the exact
@@ -139,10 +140,12 @@ def test_mamba2_bs512(cuda, ckpt_dtype):
 # --------------------------------------------------------------------------
 # two-precision checkpoint
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("lp", ["f16", "bf16"])
-@pytest.mark.parametrize("d_v, d_k, H, L, in_dtype", [(64, 128, 32, 16, "bf16"), (64, 128, 32, 32, "bf16"),
-                                                       (64, 128, 32, 16, "f32"), (128, 128, 32, 16, "bf16"),
-                                                       (16, 32, 64, 16, "bf16")])
+@pytest.mark.parametrize("lp, d_v, d_k, H, L, in_dtype", [
+    (lp, *shape) for lp in ("f16", "bf16") for shape in
+    ((64, 128, 32, 16, "bf16"), (64, 128, 32, 32, "bf16"), (64, 128, 32, 16, "f32"), (128, 128, 32, 16, "bf16"),
+     (16, 32, 64, 16, "bf16"))] + [
+    ("e4m3", 64, 128, 32, 16, "bf16"), ("e4m3", 64, 128, 32, 32, "bf16"), ("e4m3", 64, 128, 32, 64, "bf16"),
+    ("e4m3", 64, 128, 32, 16, "f32")])
 def test_two_precision(cuda, lp, d_v, d_k, H, L, in_dtype):
     B = 40
     assert_many_units(B, H)

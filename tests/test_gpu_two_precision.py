@@ -44,7 +44,13 @@ def cuda(lib):
 
 
 def _half_ulp(x, lp):
-    """Half the spacing of ``lp`` numbers in the binade of each |x|."""
+    """Half the spacing of ``lp`` numbers in the binade of each |x| (E4M3: on
+    the row's power-of-two scale, rows along the last axis)."""
+    if lp == "e4m3":
+        e = oracle.row_scale_exponent(x)[..., None].astype(np.float64)
+        xs = np.abs(x) * 2.0 ** -e
+        step = np.where(xs < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(xs, 2.0 ** -6))) - 3))
+        return 0.5 * step * 2.0 ** e
     ax = np.abs(x)
     e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
     mant, emin = {"f16": (10, -14), "bf16": (7, -126)}[lp]
@@ -100,20 +106,20 @@ def _run(lib, w, lp, steps, heads=None):
             fs = w.slot_idx[fl_rows]
             fs_t = torch.as_tensor(fs, device="cuda")
             hp = g.ckpt[fs_t][:, hs_t].double().cpu().numpy()
-            lpv = g.ckpt_lp[fs_t][:, hs_t].double().cpu().numpy()
+            lpv = g.read_copy(fs, hs)
             S_new = o.ex.S[fs]
             worst_ck = max(worst_ck, rel_err(hp, S_new, nd=2))
             lim = _half_ulp(S_new, lp) + ARITH * _scale(S_new)
             assert np.all(np.abs(lpv - S_new) <= lim), "read copy is not a rounding of the new state"
             n_lp += lpv.size
-            n_lp_exact += int(np.sum(lpv == oracle.round_to(S_new, lp)))
+            n_lp_exact += int(np.sum(lpv == oracle.round_read_copy(S_new, lp)))
             for s in fs:
                 S_m[s] = o.ex.S[s].copy()
                 gam[s] = 1.0
     return g, dict(ck=worst_ck, excess=worst_excess, seen=seen, lp_exact=n_lp_exact / max(n_lp, 1), n_lp=n_lp)
 
 
-@pytest.mark.parametrize("lp", ["f16", "bf16"])
+@pytest.mark.parametrize("lp", ["f16", "bf16", "e4m3"])
 def test_two_precision_small(cuda, lp):
     """Padded rows, permuted slots, staggered cursors, 48 steps (3 windows)."""
     w = synth.make_workload("mamba2_bs256", B=7, H=3, steps=48, seed=21, pad_rows=1, num_slots=11,
@@ -126,19 +132,43 @@ def test_two_precision_small(cuda, lp):
     assert r["seen"] > 3 * TOL_F32, r  # the read copy's rounding shows in the outputs
 
 
+@pytest.mark.parametrize("lp", ["bf16", "e4m3"])
 @pytest.mark.parametrize("L", [4, 32])
-def test_two_precision_buffer_lengths(cuda, L):
+def test_two_precision_buffer_lengths(cuda, L, lp):
     w = synth.make_workload("mamba2_bs256", B=5, H=2, steps=2 * L + 3, seed=L, L=L)
-    g, r = _run(cuda, w, "bf16", 2 * L + 3)
+    g, r = _run(cuda, w, lp, 2 * L + 3)
     assert int(g.dev_err.item()) == 0
     assert r["lp_exact"] >= MIN_EXACT and r["ck"] <= TOL_F32 and r["excess"] <= TOL_F32, r
 
 
-def test_two_precision_bs256_full_size_sampled(cuda):
-    """The bench's layer (batch 256, 128 heads of 64 x 128, L 16, fp16 read
-    copy) for 32 steps in its launch configuration, two heads of every row
-    followed by the oracle."""
+@pytest.mark.parametrize("lp", ["f16", "e4m3"])
+def test_two_precision_bs256_full_size_sampled(cuda, lp):
+    """The bench's layer (batch 256, 128 heads of 64 x 128, L 16, fp16 or
+    E4M3 read copy) for 32 steps in its launch configuration, two heads of
+    every row followed by the oracle."""
     w = synth.make_workload("mamba2_bs256", steps=32, seed=2)
-    g, r = _run(cuda, w, "f16", 32, heads=[5, 100])
+    g, r = _run(cuda, w, lp, 32, heads=[5, 100])
     assert int(g.dev_err.item()) == 0
     assert r["lp_exact"] >= MIN_EXACT and r["ck"] <= TOL_F32 and r["excess"] <= TOL_F32, r
+
+
+@pytest.mark.parametrize("lp", ["f16", "bf16", "e4m3"])
+def test_seed_read_copy_is_the_oracle_rounding(cuda, lp):
+    """replayssm_seed_read_copy rounds each element of the fp32 recurrence
+    copy once: bit for bit the oracle's rounding (E4M3: with the same
+    power-of-two row scales)."""
+    import torch
+
+    w = synth.make_workload("mamba2_bs256", B=6, H=4, steps=1, seed=8)
+    ck = w.ckpt0.copy()
+    ck[0, 0, 3] = 0.0                      # a row of zeros
+    ck[1, 1, 5] *= 1e-6                    # a tiny row
+    ck[2, 2, 7] = 448.0 * 2.0 ** -5        # a maximum on a binade edge
+    g = GpuRun(cuda, w, ckpt0=ck, lp_dtype=lp)
+    torch.cuda.synchronize()
+    got = g.read_copy(np.arange(w.num_slots), np.arange(w.H))
+    want = oracle.round_read_copy(ck.astype(np.float64), lp)
+    np.testing.assert_array_equal(got, want)
+    if lp == "e4m3":
+        e = oracle.row_scale_exponent(ck.astype(np.float64))
+        np.testing.assert_array_equal(g.ckpt_lp_scale.double().cpu().numpy(), 2.0 ** e)
