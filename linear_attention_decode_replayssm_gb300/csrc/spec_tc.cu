@@ -43,10 +43,11 @@
 // Persistent and warp-specialised: a producer warp streams each unit's
 // checkpoint (one bulk copy) and its records, drafts and decays (per-lane
 // cp.async) into slot rings; groups of four consumer warps take alternate
-// units.  Within a group, per unit: warp 0 computes the causal decays W and D
-// (warp 1 the fold weights on a flush) while all four compute the dots, one
-// named barrier, then each warp forms its 16 state rows of all T outputs.
-// Every wait is bounded.
+// units.  Within a group, per unit: warp 1 computes the causal decays W and D
+// (warp 2 the fold weights on a flush) while the dots run on warp 0 (and on
+// the others for windows longer than 16 records), one named barrier, then
+// each warp forms its 16 state rows of all T outputs.  Every wait is
+// bounded.
 #include "common.cuh"
 #include "launch.h"
 
@@ -292,8 +293,9 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
       return *reinterpret_cast<const uint2 *>(sq + ((size_t)qi * DK + kq_pos(qi, 16 * bk + 4 * t4)) * RES);
     };
 
-    // ---- phase A: decays (warp 0), fold weights (warp 1), dots (all) ----
-    if (lw == 0) {
+    // ---- phase A: decays (warp 1), fold weights (warp 2), dots (warp 0
+    // first, the others for longer windows) ----
+    if (lw == 1) {
       // W_{j,0} and D_0 from one suffix scan over the first draft's window;
       // each later draft multiplies in its own decay
       float x0 = lane <= nb ? sa[r0 + lane] : 1.f;
@@ -320,7 +322,7 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
       // records of the last 16-tile past R weigh 0 for every draft
       for (int x = R + lane; x < (R + 15) / 16 * 16; x += 32)
         for (int i = 0; i < T; ++i) sWt[x * SP + i] = 0.f;
-    } else if (lw == 1 && flush) {
+    } else if (lw == 2 && flush) {
       // fold weights of the committed records, and their gamma
       float x0 = lane < hc ? sa[lane] : 1.f;
       float x1 = lane + 32 < hc ? sa[lane + 32] : 1.f;
@@ -333,8 +335,10 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
       if (lane == 0) sWf[64] = x0;
     }
     // Sd = K Q over the window's records, 16 records per tile, tiles shared
-    // round-robin by the group's warps; records past R read as 0
-    for (int rt = lw; rt * 16 < R; rt += NCW) {
+    // by the group's warps (warp 0 first: with a window of at most 16
+    // records the decays and the fold weights run beside it); records past
+    // R read as 0
+    for (int rt = (NCW - lw) % NCW; rt * 16 < R; rt += NCW) {
       const int ja = rt * 16 + g8, jb = ja + 8;  // window records of rows g8, g8 + 8
       float dacc[NT][4];
 #pragma unroll
