@@ -354,6 +354,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
+// Wait for the fill of a record slot with unit u: the phase of its full
+// barrier with parity `parity`.  When consumer groups take alternate units
+// and the slot count is not a multiple of the group count, a group can come
+// to a slot while the slot's previous fill (another group's unit) has not
+// landed yet; a parity wait then returns at once, on the phase before.  The
+// producer writes the unit index into the slot (*slot_unit) only after that
+// previous unit was released, before it completes the new phase, so a slot
+// that does not show u yet means the wait returned early: wait until it
+// does, then wait for the phase again.  false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_unit(uint64_t *bar, uint32_t parity, const int *slot_unit, int u) {
+  if (!mbar_wait(bar, parity)) return false;
+  if (*(const volatile int *)slot_unit == u) return true;
+  const unsigned long long t0 = global_ns();
+  while (*(const volatile int *)slot_unit != u) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return mbar_wait(bar, parity);
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` on the barrier's
 // transaction count.  Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar,

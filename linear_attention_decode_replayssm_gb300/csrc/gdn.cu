@@ -60,7 +60,7 @@ __host__ __device__ inline GdnRec gdn_rec(int RB, int DK, int res, int ies, int 
   s.d = o;    o = align128(o + L * RB * res);    // corrected values of this unit's rows
   s.vt = o;   o = align128(o + RB * ies);
   s.a = o;    o = align128(o + (L + 4) * 4);     // g_0..g_{p-1}; [L] = g_t, [L+1] = beta_t
-  s.meta = o; o = align128(o + 16);
+  s.meta = o; o = align128(o + 20);  // slot, p, flush, status, unit
   s.scr = o;  o = align128(o + (3 * L + 3 * RB + 4) * 4);  // G_j, weighted key dots, row window terms, d_t, scalars
   s.bytes = o;
   return s;
@@ -72,18 +72,20 @@ __host__ __device__ inline uint32_t gdn_head(int nsr, int nsc) { return align128
 // LMAX bounds the buffer length at compile time (L <= LMAX).
 // CPR: 16-byte checkpoint chunks a consumer lane holds per state row (chunks
 // cv, cv + G, ...), so the row reductions run over G = DK / (E CPR) lanes.
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int LMAX, int CPR>
-__global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
+// NGRP consumer groups of NCW warps take alternate units (a flush unit's
+// fold in one group overlaps the other group's units).
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int LMAX, int CPR, int NGRP>
+__global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr int RB = DV / NSPLIT;    // state rows per unit
   constexpr int E = V::E;
   constexpr int NCH = DK / E;        // 16-byte chunks per state row
   constexpr int G = NCH / CPR;       // lanes per state row
-  constexpr int NC = NCW * 32;       // consumer threads
+  constexpr int NC = NCW * 32;       // consumer threads per group
   constexpr int RPP = NC / G;        // state rows per pass
   constexpr int VPT = RB / RPP;      // state rows per consumer thread
-  constexpr int WIN = NCW;           // warp index of the window warp
-  constexpr int PROD = NCW + 1;      // warp index of the producer
+  constexpr int WIN = NGRP * NCW;    // warp index of the window warp
+  constexpr int PROD = WIN + 1;      // warp index of the producer
   constexpr int RPL = (RB + 31) / 32;  // state rows per window-warp lane
   constexpr uint32_t CKB = RB * DK * (uint32_t)sizeof(TC);
   static_assert(G <= 32 && 32 % G == 0 && NCH % CPR == 0, "a state row must fit in one warp");
@@ -119,9 +121,10 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
     for (int s = 0; s < nsr; ++s) {
       mbar_init(&full[s], 33);
       mbar_init(&ready[s], 32);           // the window warp's lanes
-      mbar_init(&rec_empty[s], NC + 32);  // every consumer thread and the window warp
+      mbar_init(&rec_empty[s], NC + 32);  // the consuming group's threads and the window warp
     }
     for (int c = 0; c < nsc; ++c) mbar_init(&ck_empty[c], NC);
+    for (int s = 0; s < nsr; ++s) reinterpret_cast<int *>(rec_slots + (size_t)s * lay.bytes + lay.meta)[4] = -1;
     *s_abort = 0;
     mbar_init_fence();
   }
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
         if (status == kStatusOk) {
           const size_t unit = (size_t)slot * a.H + h;
           if (lane == 0) {
-            meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
+            meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status; meta[4] = u;
             mbar_expect_tx(&full[s], CKB);
             bulk_load(ck_slots + (size_t)c * CKB,
                       static_cast<const TC *>(a.ckpt) + unit * (DV * DK) + (size_t)row_off * DK, CKB, &full[s],
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
           if (lane == 30) cp_async4(sa + L, a.alpha + (size_t)b * a.H + h);
           if (lane == 31) cp_async4(sa + L + 1, a.beta + (size_t)b * a.H + h);
         } else if (lane == 0) {
-          meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
+          meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status; meta[4] = u;
         }
         if (lane == 0) mbar_arrive(&full[s]);
         cp_async_arrive(&full[s]);
@@ -367,25 +370,30 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
   }
 
   // ------------------------------------------------------------------ consumers
-  // every consumer warp takes every unit; the lanes of a state row are in
-  // one warp, so the warps run independently of each other
-  const int row0 = tid / G, cv = tid - (tid / G) * G;
-  int s = 0, c = 0;
-  uint32_t ph = 0;
-  for (int it = 0;; ++it) {
-    if (it) {
-      if (++s == nsr) {
-        s = 0;
+  // group g takes the CTA's units g, g + NGRP, ...; the lanes of a state row
+  // are in one warp, so the warps run independently of each other
+  const int grp = warp / NCW, lw = warp - grp * NCW, ctid = tid - grp * NC;
+  const int row0 = ctid / G, cv = ctid - (ctid / G) * G;
+  int s = grp % nsr, c = grp % nsc;
+  uint32_t ph = (uint32_t)(grp / nsr) & 1u;
+  for (int it = grp;; it += NGRP) {
+    if (it != grp) {
+      // a plan may have fewer slots than groups: wrap as often as needed
+      s += NGRP;
+      while (s >= nsr) {
+        s -= nsr;
         ph ^= 1u;
       }
-      if (++c == nsc) c = 0;
+      c += NGRP;
+      while (c >= nsc) c -= nsc;
     }
     const int u = blockIdx.x + it * stride;
     if (u >= n_units) break;
     // the checkpoint and records have landed; the window warp's terms are
     // awaited only after the checkpoint pass, so its latency does not hold
     // the checkpoint slot
-    const bool w = mbar_wait(&full[s], ph);
+    const bool w = mbar_wait_unit(&full[s], ph,
+                                  reinterpret_cast<const int *>(rec_slots + (size_t)s * lay.bytes + lay.meta) + 4, u);
     if (!__all_sync(0xffffffffu, w) || *(volatile int *)s_abort) {
       fail();
       break;
@@ -399,8 +407,8 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
     const int h = rem / NSPLIT, half = rem - h * NSPLIT, row_off = half * RB;
     float *orow = a.out + (size_t)b * a.so + (size_t)h * DV + row_off;
     if (status != kStatusOk) {
-      for (int i = tid; i < RB; i += NC) orow[i] = 0.f;
-      if (tid == 0 && status != kStatusPad) report(a.dev_err, status == kStatusBadSlot ? 1 : 2);
+      for (int i = ctid; i < RB; i += NC) orow[i] = 0.f;
+      if (ctid == 0 && status != kStatusPad) report(a.dev_err, status == kStatusBadSlot ? 1 : 2);
       mbar_arrive(&ck_empty[c]);
       mbar_arrive(&rec_empty[s]);  // the window warp arrives on it too before the slot is reused
       continue;
@@ -472,7 +480,7 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
         else
           orow[rrow] = fmaf(alpha_t, A, d_pair * kq);
       }
-      if (warp == NCW - 1 && half == 0) {
+      if (lw == NCW - 1 && half == 0) {
         // append this token's key (rounded to the ring type) and gate, once per head
         for (int cc = lane; cc < DK / 8; cc += 32) {
           float f[8];
@@ -533,10 +541,10 @@ __global__ void __launch_bounds__(NCW * 32 + 64, 2) gdn_replay_kernel(const KArg
   }
 }
 
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int LMAX, int CPR>
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int LMAX, int CPR, int NGRP>
 static cudaError_t launch_gdn_l(const KArgs &a, cudaStream_t s) {
-  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT, LMAX, CPR>;
-  constexpr int threads = NCW * 32 + 64;
+  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT, LMAX, CPR, NGRP>;
+  constexpr int threads = NGRP * NCW * 32 + 64;
   const size_t ckb = (size_t)(DV / NSPLIT) * DK * sizeof(TC);
   const size_t rb = gdn_rec(DV / NSPLIT, DK, (int)sizeof(RT), (int)sizeof(IT), a.L).bytes;
   RingPlan plan;
@@ -548,10 +556,10 @@ static cudaError_t launch_gdn_l(const KArgs &a, cudaStream_t s) {
 }
 
 // the common short windows get a kernel unrolled for L <= 16
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int CPR = 1>
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int CPR = 1, int NGRP = 1>
 static cudaError_t launch_gdn(const KArgs &a, cudaStream_t s) {
-  return a.L <= 16 ? launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, 16, CPR>(a, s)
-                   : launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, RS_MAX_L, CPR>(a, s);
+  return a.L <= 16 ? launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, 16, CPR, NGRP>(a, s)
+                   : launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, RS_MAX_L, CPR, NGRP>(a, s);
 }
 
 template <typename TC, typename RT, typename IT>

@@ -67,7 +67,7 @@ __host__ __device__ inline M2Rec m2_rec(int DV, int DK, int rec_es, int L, int s
   s.v = o;    o = align128(o + L * DV * rec_es);
   s.q = o;    o = align128(o + DK * rec_es);
   s.a = o;    o = align128(o + L * 4);             // decays of records 0..p
-  s.meta = o; o = align128(o + 32);                // slot, p, flush, status, read-copy parts
+  s.meta = o; o = align128(o + 36);                // slot, p, flush, status, read-copy parts, unit
   s.scr = o;  o = align128(o + (2 * L + 2 * DV + 4) * 4);  // w_j, k_j.q, row dots, gamma, window term
   s.scl = o;  o = align128(o + scl_bytes);
   s.bytes = o;
@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
       if (WW) mbar_init(&ready[s], 32);
     }
     for (int c = 0; c < NPART * nsc; ++c) mbar_init(&ck_empty[c], NC);
+    for (int s = 0; s < nsr; ++s) reinterpret_cast<int *>(rec_slots + (size_t)s * lay.bytes + lay.meta)[8] = -1;
     *s_abort = 0;
     mbar_init_fence();
   }
@@ -266,6 +267,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
           if (lane == 0) {
             meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
             meta[4] = hp[0]; meta[5] = hp[1]; meta[6] = hp[2]; meta[7] = hp[3];
+            meta[8] = u;
             const TC *ck32 = static_cast<const TC *>(a.ckpt) + unit * (DV * DK);
             if constexpr (TWO) {
               if (!fl) {
@@ -338,6 +340,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
         } else if (lane == 0) {
           meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
           meta[4] = -1; meta[5] = -1; meta[6] = -1; meta[7] = -1;
+          meta[8] = u;
         }
         if (lane == 0) mbar_arrive(&full[s]);  // releases the meta words
         cp_async_arrive(&full[s]);
@@ -486,25 +489,27 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
       ++b;
     }
     if (it != grp) {
+      // a plan may have fewer slots than groups: wrap as often as needed
       s += NGRP;
-      if (s >= nsr) {
+      while (s >= nsr) {
         s -= nsr;
         ph ^= 1u;
       }
       c += NGRP;
-      if (c >= nsc) c -= nsc;
+      while (c >= nsc) c -= nsc;
     }
     const int u = blockIdx.x + it * stride;
     if (u >= n_units) break;
+    const int *slot_unit = reinterpret_cast<const int *>(rec_slots + (size_t)s * lay.bytes + lay.meta) + 8;
     if constexpr (WW) {
       // every warp waits for itself: no named barrier in this mode
-      const bool w = mbar_wait(&full[s], ph);
+      const bool w = mbar_wait_unit(&full[s], ph, slot_unit, u);
       if (!__all_sync(0xffffffffu, w) || *(volatile int *)s_abort) {
         fail();
         break;
       }
     } else {
-      if (lane == 0 && !mbar_wait(&full[s], ph)) *(volatile int *)s_abort = 1;
+      if (lane == 0 && !mbar_wait_unit(&full[s], ph, slot_unit, u)) *(volatile int *)s_abort = 1;
       gsync();
       if (*(volatile int *)s_abort) break;
     }

@@ -73,7 +73,7 @@ __host__ __device__ inline SpecTcRec spec_tc_rec(int DV, int DK, int L, int T) {
   o.v = x;    x = align128(x + R * DV * 2);
   o.q = x;    x = align128(x + T * DK * 2);
   o.a = x;    x = align128(x + R * 4);
-  o.meta = x; x = align128(x + 16);
+  o.meta = x; x = align128(x + 20);              // slot, h, flush, status, unit
   o.w = x;    x = align128(x + R16 * o.sp * 4);   // W_{j,i}, [j][i]
   o.d = x;    x = align128(x + T * 4);            // D_i
   o.wf = x;   x = align128(x + 65 * 4);           // fold weights and gamma
@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
       mbar_init(&rec_empty[s], NC);  // the consuming group
     }
     for (int c = 0; c < nsc; ++c) mbar_init(&ck_empty[c], NC);
+    for (int s = 0; s < nsr; ++s) reinterpret_cast<int *>(rec_slots + (size_t)s * lay.bytes + lay.meta)[4] = -1;
     *s_abort = 0;
     mbar_init_fence();
   }
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
       if (status == kStatusOk) {
         const size_t unit = (size_t)slot * a.H + h;
         if (lane == 0) {
-          meta[0] = slot; meta[1] = hc; meta[2] = fl; meta[3] = status;
+          meta[0] = slot; meta[1] = hc; meta[2] = fl; meta[3] = status; meta[4] = u;
           mbar_expect_tx(&full[ps], CKB);
           bulk_load(ck_slots + (size_t)pc * CKB, static_cast<const TC *>(a.ckpt) + unit * (DV * DK), CKB, &full[ps],
                     pol_stream);
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
         for (int j = lane; j < hc + T; j += 32)
           cp_async4(sa + j, j < hc ? a.ring_a + unit * L + j : a.alpha + (d0 + (j - hc) * dstep));
       } else if (lane == 0) {
-        meta[0] = slot; meta[1] = hc; meta[2] = fl; meta[3] = status;
+        meta[0] = slot; meta[1] = hc; meta[2] = fl; meta[3] = status; meta[4] = u;
       }
       if (lane == 0) mbar_arrive(&full[ps]);
       cp_async_arrive(&full[ps]);
@@ -238,18 +239,20 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
   uint32_t ph = (uint32_t)(grp / nsr) & 1u;
   for (int it = grp;; it += NGRP) {
     if (it != grp) {
+      // a plan may have fewer slots than groups: wrap as often as needed
       s += NGRP;
-      if (s >= nsr) {
+      while (s >= nsr) {
         s -= nsr;
         ph ^= 1u;
       }
       c += NGRP;
-      if (c >= nsc) c -= nsc;
+      while (c >= nsc) c -= nsc;
     }
     const int u = blockIdx.x + it * stride;
     if (u >= n_units) break;
     const int b = u / a.H, h = u - (u / a.H) * a.H;
-    const bool w = mbar_wait(&full[s], ph);
+    const bool w = mbar_wait_unit(&full[s], ph,
+                                  reinterpret_cast<const int *>(rec_slots + (size_t)s * lay.bytes + lay.meta) + 4, u);
     // every warp of the group leaves together: one warp's timeout stops all
     // of them at the barrier below
     if (!__all_sync(0xffffffffu, w)) fail();
