@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libreplayssm.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["abi.cu", "mamba2.cu", "mamba2_variants.cu", "mamba2_f32in.cu", "gdn.cu", "conventional.cu", "materialize.cu", "spec.cu", "spec_tc.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "mamba2.cu", "mamba2_variants.cu", "mamba2_f32in.cu", "gdn.cu", "conventional.cu", "materialize.cu", "materialize_pipe.cu", "spec.cu", "spec_tc.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "launch.h", "mamba2.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]

@@ -281,7 +281,8 @@ int replayssm_materialize(const rs_materialize_args *a, int variant, rs_stream_t
   if (a->L < 2 || a->L > RS_MAX_L) return RS_EINVAL;
   if (a->ckpt_dtype != RS_F32 && a->ckpt_dtype != RS_F16) return RS_EUNSUPPORTED;
   if (a->ring_dtype != RS_F32 && a->ring_dtype != RS_F16 && a->ring_dtype != RS_BF16) return RS_EUNSUPPORTED;
-  const rs::MatLaunchFn fn = rs::find_materialize(a->d_v, a->d_k, a->ckpt_dtype);
+  rs::MatLaunchFn fn = rs::find_mat_pipe(variant == RS_GDN, a->d_v, a->d_k, a->ckpt_dtype, a->ring_dtype);
+  if (!fn) fn = rs::find_materialize(a->d_v, a->d_k, a->ckpt_dtype);
   if (!fn) return RS_EUNSUPPORTED;
   if (a->B == 0) return RS_OK;
   if (!a->slot_idx || !a->held || !a->dst_idx || !a->ckpt || !a->ring_v || !a->ring_k || !a->ring_a || !a->dst)

@@ -21,6 +21,9 @@ LaunchFn find_conventional(int variant, int d_v, int d_k, int ckpt_dtype);
 // over decay products.
 using MatLaunchFn = cudaError_t (*)(const rs_materialize_args &, int gdn, cudaStream_t);
 MatLaunchFn find_materialize(int d_v, int d_k, int ckpt_dtype);
+// the pipelined materialisation (materialize_pipe.cu) for 64 x 128 Mamba-2
+// and 128 x 128 GDN heads, or nullptr where it is not built
+MatLaunchFn find_mat_pipe(int gdn, int d_v, int d_k, int ckpt_dtype, int ring_dtype);
 
 // Speculative verification (Mamba-2) and the device-side commit.
 using SpecLaunchFn = cudaError_t (*)(const rs_spec_args &, cudaStream_t);

@@ -302,40 +302,65 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
               static_cast<const unsigned char *>(a.v) + ((size_t)b * a.sv + (size_t)h * DV) * RES;
           const unsigned char *qin =
               static_cast<const unsigned char *>(a.q) + ((size_t)b * a.sq + (size_t)kh * DK) * RES;
-          if (!GRP || fl) {
-#pragma unroll
-            for (int i = 0; i < (LMAX * KC + 31) / 32; ++i) {
-              const int cc = lane + 32 * i;
-              if (cc < (p + 1) * KC)
-                cp_async16(st + lay.k + cc * 16, (cc < p * KC ? rk + cc * 16 : kin + (cc - p * KC) * 16));
-            }
+          if constexpr (!GRP && LMAX >= 32) {
+            // Long windows: the ring records, this token's k, v and q, the
+            // decays and an E4M3 copy's row scales as bulk copies, one piece
+            // per lane (measured faster than 16-byte cp.async pieces at
+            // L = 32, slower at L <= 16).  Decays past the last whole 16
+            // bytes of the ring row (at most three) and this token's decay
+            // go by cp.async.
+            float *sa = reinterpret_cast<float *>(st + lay.a);
+            const uint32_t rkb = (uint32_t)p * kb, rvb = (uint32_t)p * vb;
+            const bool a16 = (L & 3) == 0 && (reinterpret_cast<uintptr_t>(a.ring_a) & 15) == 0;
+            const int na = a16 ? (p & ~3) : 0;  // decays by bulk copy
+            const bool scl = F8 && !fl;
+            if (lane == 0) mbar_expect_tx(&full[s], rkb + rvb + 2 * kb + vb + na * 4 + (scl ? DV * 4 : 0));
+            __syncwarp();
+            if (lane == 1 && p > 0) bulk_load(st + lay.k, rk, rkb, &full[s], pol_stream);
+            if (lane == 2) bulk_load(st + lay.k + rkb, kin, kb, &full[s], pol_stream);
+            if (lane == 3 && p > 0) bulk_load(st + lay.v, rv, rvb, &full[s], pol_stream);
+            if (lane == 4) bulk_load(st + lay.v + rvb, vin, vb, &full[s], pol_stream);
+            if (lane == 5) bulk_load(st + lay.q, qin, kb, &full[s], pol_stream);
+            if (lane == 6 && na > 0) bulk_load(sa, a.ring_a + unit * L, na * 4, &full[s], pol_stream);
+            if (scl && lane == 7) bulk_load(st + lay.scl, a.lp_scale + unit * DV, DV * 4, &full[s], pol_stream);
+            for (int jj = na + lane; jj < p; jj += 32) cp_async4(sa + jj, a.ring_a + unit * L + jj);
+            if (lane == 31) cp_async4(sa + p, a.alpha + (size_t)b * a.H + h);
           } else {
-            // the group's k_j . q_t of the window, into the dots scratch of the slot
-            float *ss = reinterpret_cast<float *>(st + lay.scr) + L;
-            const float *kq = a.kq + ((size_t)b * a.n_groups + kh) * L;
+            if (!GRP || fl) {
+#pragma unroll
+              for (int i = 0; i < (LMAX * KC + 31) / 32; ++i) {
+                const int cc = lane + 32 * i;
+                if (cc < (p + 1) * KC)
+                  cp_async16(st + lay.k + cc * 16, (cc < p * KC ? rk + cc * 16 : kin + (cc - p * KC) * 16));
+              }
+            } else {
+              // the group's k_j . q_t of the window, into the dots scratch of the slot
+              float *ss = reinterpret_cast<float *>(st + lay.scr) + L;
+              const float *kq = a.kq + ((size_t)b * a.n_groups + kh) * L;
+#pragma unroll
+              for (int i = 0; i < (LMAX + 31) / 32; ++i) {
+                const int jj = lane + 32 * i;
+                if (jj <= p) cp_async4(ss + jj, kq + jj);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < (LMAX * VC + 31) / 32; ++i) {
+              const int cc = lane + 32 * i;
+              if (cc < (p + 1) * VC)
+                cp_async16(st + lay.v + cc * 16, (cc < p * VC ? rv + cc * 16 : vin + (cc - p * VC) * 16));
+            }
+            for (int cc = lane; cc < KC; cc += 32) cp_async16(st + lay.q + cc * 16, qin + cc * 16);
+            float *sa = reinterpret_cast<float *>(st + lay.a);
 #pragma unroll
             for (int i = 0; i < (LMAX + 31) / 32; ++i) {
               const int jj = lane + 32 * i;
-              if (jj <= p) cp_async4(ss + jj, kq + jj);
+              if (jj < p) cp_async4(sa + jj, a.ring_a + unit * L + jj);
             }
-          }
-#pragma unroll
-          for (int i = 0; i < (LMAX * VC + 31) / 32; ++i) {
-            const int cc = lane + 32 * i;
-            if (cc < (p + 1) * VC)
-              cp_async16(st + lay.v + cc * 16, (cc < p * VC ? rv + cc * 16 : vin + (cc - p * VC) * 16));
-          }
-          for (int cc = lane; cc < KC; cc += 32) cp_async16(st + lay.q + cc * 16, qin + cc * 16);
-          float *sa = reinterpret_cast<float *>(st + lay.a);
-#pragma unroll
-          for (int i = 0; i < (LMAX + 31) / 32; ++i) {
-            const int jj = lane + 32 * i;
-            if (jj < p) cp_async4(sa + jj, a.ring_a + unit * L + jj);
-          }
-          if (lane == 31) cp_async4(sa + p, a.alpha + (size_t)b * a.H + h);
-          if constexpr (F8) {
-            // a non-flush row's read copy comes with its row scales
-            if (!fl && lane < DV / 4) cp_async16(st + lay.scl + lane * 16, a.lp_scale + unit * DV + lane * 4);
+            if (lane == 31) cp_async4(sa + p, a.alpha + (size_t)b * a.H + h);
+            if constexpr (F8) {
+              // a non-flush row's read copy comes with its row scales
+              if (!fl && lane < DV / 4) cp_async16(st + lay.scl + lane * 16, a.lp_scale + unit * DV + lane * 4);
+            }
           }
         } else if (lane == 0) {
           meta[0] = slot; meta[1] = p; meta[2] = fl; meta[3] = status;
@@ -624,15 +649,15 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
         // back to the producer
         using Raw = typename std::conditional<TWO, uint2, uint4>::type;
         Raw raw[VPT][CPR];
-  #pragma unroll
+#pragma unroll
         for (int r = 0; r < VPT; ++r)
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < CPR; ++i)
             raw[r][i] = reinterpret_cast<const Raw *>(ck_slot)[(row0 + r * RPP) * NCH + cv + G * i];
         release_ck();
         weights();
         float qv[CPR][E];
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < CPR; ++i) lds_cols<E>(st + lay.q, (cv + G * i) * E, RDT, qv[i]);
         // s_j = k_j . q: a warp takes records four at a time; each lane holds
         // its 4-column chunk of q and accumulates four partial dots, and one
@@ -641,7 +666,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
         if constexpr (!GRP && !WW) {
           constexpr int QPL = (DK + 127) / 128;  // 4-column chunks of q per lane
           float qq[QPL][4];
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < QPL; ++i) {
             if (lane * 4 + i * 128 < DK) {
               lds_cols<4>(st + lay.q, lane * 4 + i * 128, RDT, qq[i]);
@@ -649,17 +674,17 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
               qq[i][0] = qq[i][1] = qq[i][2] = qq[i][3] = 0.f;
             }
           }
-  #pragma unroll
+#pragma unroll
           for (int ci = 0; ci < (LMAX / 4 + NCW - 1) / NCW; ++ci) {
             const int ch = lw + ci * NCW;
             if (ch * 4 > p) break;
             float part4[4];
-  #pragma unroll
+#pragma unroll
             for (int r = 0; r < 4; ++r) {
               const int j = ch * 4 + r;
               float acc = 0.f;
               if (j <= p) {
-  #pragma unroll
+#pragma unroll
                 for (int i = 0; i < QPL; ++i) {
                   const int cc = lane * 4 + i * 128;
                   if (cc < DK) {
@@ -679,10 +704,10 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
           }
         }
         // checkpoint GEMV partials from the stage
-  #pragma unroll
+#pragma unroll
         for (int r = 0; r < VPT; ++r) {
           float acc = 0.f;
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < CPR; ++i) {
             float f[E];
             if constexpr (TWO) {
@@ -690,7 +715,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
             } else {
               V::unpack(raw[r][i], f);
             }
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < E; ++e) acc = fmaf(f[e], qv[i][e], acc);
           }
           part[r] = acc;
@@ -721,27 +746,27 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
           static_assert(DV % 8 == 0 && 32 % RG == 0 && OG >= 1, "bad output layout");
           const int rg = lane % RG, og = lane / RG;
           float acc[8];
-  #pragma unroll
+#pragma unroll
           for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < (LMAX + OG - 1) / OG; ++i) {
             const int j = og + i * OG;
             if (j <= p) {
               const float cj = sW[j] * sS[j];
               float vv[8];
               lds_cols<8>(sv, j * DV + rg * 8, RDT, vv);
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 8; ++e) acc[e] = fmaf(cj, vv[e], acc[e]);
             }
           }
-  #pragma unroll
+#pragma unroll
           for (int off = RG; off < 32; off <<= 1) {
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
           }
           if (og == 0) {
             const float gam = sGam[0];
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 8; ++e) orow[rg * 8 + e] = fmaf(gam, sC[rg * 8 + e], acc[e]);
           }
         }

@@ -162,6 +162,42 @@ def test_materialize_fp16_checkpoint(cuda, variant, ring):
     assert rel_err(dst.double().cpu().numpy(), want, nd=2) <= TOL_F16_DST
 
 
+@pytest.mark.parametrize("variant, ring, ckpt", [("mamba2", "bf16", "f32"), ("mamba2", "f32", "f32"),
+                                                  ("mamba2", "bf16", "f16"), ("gdn", "f16", "f32"),
+                                                  ("gdn", "f32", "f32"), ("gdn", "f16", "f16")])
+def test_materialize_many_units(cuda, variant, ring, ckpt):
+    """More units than the launch has CTAs (each CTA takes several, its two
+    consumer groups alternating over the slot rings, a unit count that is
+    not a multiple of the groups or the grid), every held count from 0 to
+    L - 1, padded rows and a permuted destination: every element against
+    the oracle."""
+    import torch
+
+    lib = cuda
+    B, H = 97, 8
+    name = "mamba2_bs256" if variant == "mamba2" else "gdn_bs256"
+    kw = dict(in_dtype=ring) if variant == "mamba2" else {}  # Mamba-2 records are its inputs verbatim
+    held = (np.arange(B) % synth.SPECS[name]["L"]).astype(np.int32)
+    w = synth.make_workload(name, B=B, H=H, steps=1, seed=31, ckpt_dtype=ckpt, ring_dtype=ring, cursor0=held, **kw)
+    g = GpuRun(lib, w)
+    dst_idx = np.random.default_rng(6).permutation(B + 5)[:B].astype(np.int32)
+    dst_idx[[3, 50]] = -1  # skipped rows
+    dst = torch.full((B + 5, H, w.d_v, w.d_k), 5.0, device="cuda", dtype=tdt(ckpt))
+    before = [x.clone() for x in (g.ckpt, g.ring_v, g.ring_k, g.ring_a)]
+    _materialize(lib, g, w, held, dst, dst_idx)
+    assert int(g.dev_err.item()) == 0
+    for a_, b_ in zip(before, (g.ckpt, g.ring_v, g.ring_k, g.ring_a)):
+        assert _same_bits(a_, b_)
+    rs = oracle.ReplayState(w.variant, w.ckpt0.astype(np.float64), w.ring_v0.astype(np.float64),
+                            w.ring_k0.astype(np.float64), w.ring_a0.astype(np.float64))
+    want = oracle.materialize(rs, w.slot_idx, held, ckpt)
+    rows = np.flatnonzero(dst_idx >= 0)
+    got = dst[torch.as_tensor(dst_idx[rows].astype(np.int64), device="cuda")].double().cpu().numpy()
+    assert rel_err(got, want[rows], nd=2) <= (TOL_F16_DST if ckpt == "f16" else TOL_F32)
+    untouched = np.setdiff1d(np.arange(B + 5), dst_idx[rows])
+    assert bool((dst[torch.as_tensor(untouched, device="cuda")] == 5.0).all())
+
+
 def test_materialize_range_checks(cuda):
     """Out-of-range slot, destination or held count: the row is skipped, the
     matching bit is set, and nothing is written."""
