@@ -57,6 +57,9 @@ __host__ __device__ inline uint32_t mat_head(int nsr, int nsc) { return align128
 // RB state rows per unit (NSPLIT units per head), TC checkpoint type, RT ring
 // type, GDNW: log-gate weights (exp of suffix sums) instead of decay products
 template <int DV, int DK, int NSPLIT, typename TC, typename RT, bool GDNW>
+// One CTA per SM: the state held in accumulator layout and the split
+// operands fit in 112 registers without spilling; two CTAs per SM would
+// allow 96 (18 warps, five on one scheduler) and measured slower.
 __global__ void __maxnreg__(112) mat_pipe_kernel(const rs_materialize_args a, int nsr, int nsc) {
   constexpr int RB = DV / NSPLIT;
   constexpr int NCW = RB / 16;  // consumer warps per group: 16 rows each

@@ -18,6 +18,7 @@ staggered cursors -- and every state precision the kernels take):
   * Mamba-2, one checkpoint copy: 64 x 128 fp32 and fp16 at L 8 / 16 / 32 /
     64 (the compile-time window bounds 8, 16, 32 and 64), 128 x 128 and
     16 x 32 heads, bf16 and fp32 inputs; batch 512 at L 16 in fp32 and fp16;
+    an odd head count;
   * the two-precision checkpoint with fp16 and bf16 read copies, both input
     types and every head shape, and the E4M3 read copy (64 x 128 heads) at
     L 16 / 32 / 64;
@@ -82,14 +83,26 @@ def _mamba2_gates(r, ckpt_dtype):
 @pytest.mark.parametrize("ckpt_dtype", ["f32", "f16"])
 @pytest.mark.parametrize("L", [8, 16, 32, 64])
 def test_mamba2_64x128_window_bounds(cuda, L, ckpt_dtype):
-    # 48 rows x 32 heads = 1536 units; staggered cursors, padded rows and
+    # 80 rows x 32 heads = 2560 units; staggered cursors, padded rows and
     # permuted slots; every row flushes at least once
-    B, H = 48, 32
+    B, H = 80, 32
     assert_many_units(B, H)
-    w = synth.make_workload("mamba2_bs256", B=B, H=H, L=L, steps=L + 6, num_slots=56, permute_slots=True,
+    w = synth.make_workload("mamba2_bs256", B=B, H=H, L=L, steps=L + 6, num_slots=88, permute_slots=True,
                             pad_rows=3, ckpt_dtype=ckpt_dtype, seed=400 + L)
     r = par.run_parity(cuda, w, w.steps, heads=[0, 17, 31])
     _mamba2_gates(r, ckpt_dtype)
+
+
+@pytest.mark.parametrize("L", [8, 16])
+def test_mamba2_fp16_odd_heads(cuda, L):
+    # an odd head count (48 x 27 = 1296 units): no unit arithmetic may assume
+    # heads come in pairs
+    B, H = 48, 27
+    assert_many_units(B, H)
+    w = synth.make_workload("mamba2_bs256", B=B, H=H, L=L, steps=L + 6, pad_rows=2, ckpt_dtype="f16",
+                            seed=470 + L)
+    r = par.run_parity(cuda, w, w.steps, heads=[0, 13, 26])
+    _mamba2_gates(r, "f16")
 
 
 @pytest.mark.parametrize("ckpt_dtype", ["f32", "f16"])
