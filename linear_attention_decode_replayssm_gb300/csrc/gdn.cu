@@ -91,6 +91,10 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(con
   static_assert(G <= 32 && 32 % G == 0 && NCH % CPR == 0, "a state row must fit in one warp");
   static_assert(NC % G == 0 && RB % RPP == 0 && VPT >= 1 && 2 * VPT <= G, "bad tiling");
   static_assert(DK % 8 == 0 && RB % 8 == 0 && DK <= 128 && RB <= 32 * RPL, "bad head dims");
+  // flush on the tensor cores: 64-row units of an fp32 or fp16 checkpoint,
+  // each of the group's eight warps one 16-row tile of half the columns
+  constexpr bool MMAF = (sizeof(TC) == 4 || sizeof(TC) == 2) && RB == 64 && DK % 32 == 0 && (DK & (DK - 1)) == 0 &&
+                        NCW == 8;
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -412,6 +416,142 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(con
       mbar_arrive(&ck_empty[c]);
       mbar_arrive(&rec_empty[s]);  // the window warp arrives on it too before the slot is reused
       continue;
+    }
+    if constexpr (MMAF) {
+      if (flush) {
+        // Flush on the tensor cores.  Warp lw holds state rows rA = 16 (lw % 4)
+        // + g and rB = rA + 8 of the unit, columns 64 (lw / 4) + 16 bk + 4t ..
+        // + 3 in accumulator layout.  S_ckpt k_t and S_ckpt q_t of its rows
+        // come from the whole rows in the slot; then d_t, the output by the
+        // expansion o = alpha_t (Gamma S_ckpt q_t + window term) + d_t (k_t .
+        // q_t) (the unrounded S_new applied to q_t), and the fold S_new =
+        // alpha_t Gamma S_ckpt + sum_{j<p} alpha_t G_j d_j k_j^T + d_t k_t^T
+        // as a rank-(p+1) m16n8k8 tf32 product: each weighted value split into
+        // two tf32 terms (the current d_t unrounded), 16-bit keys exact, fp32
+        // keys split too.
+        constexpr int NBH = DK / 32;  // 16-column blocks of a half row
+        const int g8 = lane >> 2, t4 = lane & 3;
+        const int rA = 16 * (lw & 3) + g8, rB = rA + 8, cb = 64 * (lw >> 2);
+        const unsigned char *ck_slot = ck_slots + (size_t)c * CKB;
+        const unsigned char *skt = st + lay.kt, *sq = st + lay.q, *sk = st + lay.k, *sd = st + lay.d;
+        auto ld4 = [&](int r, int col) -> float4 {
+          if constexpr (sizeof(TC) == 4) {
+            return *reinterpret_cast<const float4 *>(ck_slot + ((size_t)r * DK + col) * 4);
+          } else {
+            float f[4];
+            LpVec<__half>::unpack(*reinterpret_cast<const uint2 *>(ck_slot + ((size_t)r * DK + col) * 2), f);
+            return make_float4(f[0], f[1], f[2], f[3]);
+          }
+        };
+        auto dot4 = [](const float4 &x, const float (&y)[4], float acc) {
+          return fmaf(x.x, y[0], fmaf(x.y, y[1], fmaf(x.z, y[2], fmaf(x.w, y[3], acc))));
+        };
+        float4 xa[NBH], xb[NBH];
+        float kA = 0.f, kB = 0.f, qA = 0.f, qB = 0.f;
+#pragma unroll
+        for (int bk = 0; bk < 2 * NBH; ++bk) {
+          const int col = (cb + 16 * bk + 4 * t4) & (DK - 1);  // own half first, then the other
+          const float4 ya = ld4(rA, col), yb = ld4(rB, col);
+          float k4[4], q4[4];
+          lds_cols<4>(skt, col, idt, k4);
+          lds_cols<4>(sq, col, idt, q4);
+          kA = dot4(ya, k4, kA); kB = dot4(yb, k4, kB);
+          qA = dot4(ya, q4, qA); qB = dot4(yb, q4, qB);
+          if (bk < NBH) {
+            xa[bk] = ya;
+            xb[bk] = yb;
+          }
+        }
+        mbar_arrive(&ck_empty[c]);
+        kA += __shfl_xor_sync(0xffffffffu, kA, 1); kA += __shfl_xor_sync(0xffffffffu, kA, 2);
+        kB += __shfl_xor_sync(0xffffffffu, kB, 1); kB += __shfl_xor_sync(0xffffffffu, kB, 2);
+        qA += __shfl_xor_sync(0xffffffffu, qA, 1); qA += __shfl_xor_sync(0xffffffffu, qA, 2);
+        qB += __shfl_xor_sync(0xffffffffu, qB, 1); qB += __shfl_xor_sync(0xffffffffu, qB, 2);
+        {
+          const bool wr = mbar_wait(&ready[s], ph);
+          if (!__all_sync(0xffffffffu, wr) || *(volatile int *)s_abort) {
+            fail();
+            break;
+          }
+        }
+        const float *sa = reinterpret_cast<const float *>(st + lay.a);
+        const float *scr = reinterpret_cast<const float *>(st + lay.scr);
+        const float *sW = scr, *sCk = scr + 3 * L, *sCq = sCk + RB, *sScal = sCk + 3 * RB;
+        const float gam = sScal[0], kq = sScal[1], alpha_t = sScal[2], beta_t = sa[L + 1];
+        // d_t of rows rA and rB: beta_t (v_t - alpha_t S_{t-1} k_t)
+        const float dA = beta_t * (lds_elem(st + lay.vt, rA, idt) - alpha_t * fmaf(gam, kA, sCk[rA]));
+        const float dB = beta_t * (lds_elem(st + lay.vt, rB, idt) - alpha_t * fmaf(gam, kB, sCk[rB]));
+        if (lw < 4 && t4 == 0) {
+          orow[rA] = fmaf(alpha_t, fmaf(gam, qA, sCq[rA]), dA * kq);
+          orow[rB] = fmaf(alpha_t, fmaf(gam, qB, sCq[rB]), dB * kq);
+        }
+        const float sc = alpha_t * gam;
+#pragma unroll
+        for (int bk = 0; bk < NBH; ++bk) {
+          xa[bk].x *= sc; xa[bk].y *= sc; xa[bk].z *= sc; xa[bk].w *= sc;
+          xb[bk].x *= sc; xb[bk].y *= sc; xb[bk].z *= sc; xb[bk].w *= sc;
+        }
+        for (int j0 = 0; j0 <= p; j0 += 8) {
+          // records j0 + t and j0 + t + 4: ring records below p (weight
+          // alpha_t G_j), this token at p (weight 1), none past p (weight 0,
+          // its key read from k_t so nothing stale enters)
+          const int ja = j0 + t4, jb = ja + 4;
+          auto val = [&](int j, int r, float d_cur) -> float {
+            if (j < p) return alpha_t * sW[j] * lds_elem(sd, j * RB + r, rdt);
+            return j == p ? d_cur : 0.f;
+          };
+          uint32_t ah[4], al[4];
+          split_tf32(val(ja, rA, dA), ah[0], al[0]);
+          split_tf32(val(ja, rB, dB), ah[1], al[1]);
+          split_tf32(val(jb, rA, dA), ah[2], al[2]);
+          split_tf32(val(jb, rB, dB), ah[3], al[3]);
+          auto key = [&](int j, int col) -> float {
+            return j < p ? lds_elem(sk, j * DK + col, rdt) : lds_elem(skt, col, idt);
+          };
+#pragma unroll
+          for (int bk = 0; bk < NBH; ++bk) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int col = cb + 16 * bk + 4 * (g8 >> 1) + (g8 & 1) + 2 * hf;  // column of tile index n = g
+              float d[4] = {hf ? xa[bk].z : xa[bk].x, hf ? xa[bk].w : xa[bk].y, hf ? xb[bk].z : xb[bk].x,
+                            hf ? xb[bk].w : xb[bk].y};
+              if constexpr (sizeof(RT) == 2 && sizeof(IT) == 2) {
+                const uint32_t bb[2] = {__float_as_uint(key(ja, col)), __float_as_uint(key(jb, col))};
+                mma_tf32(d, ah, bb);
+                mma_tf32(d, al, bb);
+              } else {
+                uint32_t bh[2], bl[2];
+                split_tf32(key(ja, col), bh[0], bl[0]);
+                split_tf32(key(jb, col), bh[1], bl[1]);
+                mma_tf32(d, ah, bh);
+                mma_tf32(d, al, bh);
+                mma_tf32(d, ah, bl);
+              }
+              if (hf) {
+                xa[bk].z = d[0]; xa[bk].w = d[1]; xb[bk].z = d[2]; xb[bk].w = d[3];
+              } else {
+                xa[bk].x = d[0]; xa[bk].y = d[1]; xb[bk].x = d[2]; xb[bk].y = d[3];
+              }
+            }
+          }
+        }
+        TC *ckg = static_cast<TC *>(a.ckpt) + ((size_t)slot * a.H + h) * (DV * DK) + (size_t)row_off * DK;
+#pragma unroll
+        for (int bk = 0; bk < NBH; ++bk) {
+          const size_t offA = (size_t)rA * DK + cb + 16 * bk + 4 * t4, offB = (size_t)rB * DK + cb + 16 * bk + 4 * t4;
+          const float fa[4] = {xa[bk].x, xa[bk].y, xa[bk].z, xa[bk].w};
+          const float fb[4] = {xb[bk].x, xb[bk].y, xb[bk].z, xb[bk].w};
+          if constexpr (sizeof(TC) == 4) {
+            st_vec(ckg + offA, V::pack(fa));
+            st_vec(ckg + offB, V::pack(fb));
+          } else {
+            st_vec2(ckg + offA, LpVec<__half>::pack(fa));
+            st_vec2(ckg + offB, LpVec<__half>::pack(fb));
+          }
+        }
+        mbar_arrive(&rec_empty[s]);
+        continue;
+      }
     }
     uint4 raw[VPT][CPR];
     {
