@@ -281,6 +281,26 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) 
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
 }
 
+// acc + lo(a) lo(b) + hi(a) hi(b), in that order: bf16 pairs multiplied on
+// the mixed-precision FMA (16-bit operands, fp32 addend and result, one
+// rounding), the same value as widening both to fp32 and using fmaf
+__device__ __forceinline__ float fma_bf16x2_acc(uint32_t a, uint32_t b, float acc) {
+  asm("{\n .reg .b16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
+      " fma.rn.f32.bf16 %0, a0, b0, %0;\n fma.rn.f32.bf16 %0, a1, b1, %0;\n}"
+      : "+f"(acc) : "r"(a), "r"(b));
+  return acc;
+}
+
+// a * b + c elementwise on fp32 pairs, one packed FMA (each component
+// rounded once, as fmaf)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 __device__ __forceinline__ void st_vec2(void *p, const uint2 &v) {
   asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }

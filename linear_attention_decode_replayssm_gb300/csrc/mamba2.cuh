@@ -443,6 +443,8 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
               } else {
                 q4[0] = q4[1] = q4[2] = q4[3] = 0.f;
               }
+              uint2 qw = make_uint2(0u, 0u);  // the chunk as bf16 pairs
+              if (RDT == kBF16 && col < DK) qw = *reinterpret_cast<const uint2 *>(st + lay.q + (size_t)col * 2);
 #pragma unroll 1
               for (int j0 = 0; j0 <= p; j0 += 8) {
                 float part[8];
@@ -451,9 +453,15 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
                   const int j = j0 + r;
                   float acc = 0.f;
                   if (j <= p && col < DK) {
-                    float kk[4];
-                    lds_cols<4>(sk, j * DK + col, RDT, kk);
-                    acc = fmaf(kk[0], q4[0], fmaf(kk[1], q4[1], fmaf(kk[2], q4[2], kk[3] * q4[3])));
+                    if constexpr (RDT == kBF16) {
+                      // bf16 keys and query on the mixed-precision FMA, no widening
+                      const uint2 kw = *reinterpret_cast<const uint2 *>(sk + ((size_t)j * DK + col) * 2);
+                      acc = fma_bf16x2_acc(kw.x, qw.x, fma_bf16x2_acc(kw.y, qw.y, 0.f));
+                    } else {
+                      float kk[4];
+                      lds_cols<4>(sk, j * DK + col, RDT, kk);
+                      acc = fmaf(kk[0], q4[0], fmaf(kk[1], q4[1], fmaf(kk[2], q4[2], kk[3] * q4[3])));
+                    }
                   }
                   part[r] = acc;
                 }
@@ -470,17 +478,32 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
             __syncwarp();
             // y = sum_{j <= p} c_j v_j for this lane's state rows
             if (lane * RPL < DV) {
-              float y[RPL];
-#pragma unroll
-              for (int e = 0; e < RPL; ++e) y[e] = 0.f;
+              if constexpr (RPL == 2 && RDT == kBF16) {
+                // the lane's two rows as one bf16 pair, both sums in one
+                // packed fp32 FMA
+                float2 y = make_float2(0.f, 0.f);
 #pragma unroll 4
-              for (int j = 0; j <= p; ++j) {
-                const float cj = sS[j];
+                for (int j = 0; j <= p; ++j) {
+                  const float cj = sS[j];
+                  const uint32_t w = reinterpret_cast<const uint32_t *>(sv)[(j * DV) / 2 + lane];
+                  y = ffma2(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)),
+                            make_float2(cj, cj), y);
+                }
+                sY[2 * lane] = y.x;
+                sY[2 * lane + 1] = y.y;
+              } else {
+                float y[RPL];
 #pragma unroll
-                for (int e = 0; e < RPL; ++e) y[e] = fmaf(cj, lds_elem(sv, j * DV + lane * RPL + e, RDT), y[e]);
+                for (int e = 0; e < RPL; ++e) y[e] = 0.f;
+#pragma unroll 4
+                for (int j = 0; j <= p; ++j) {
+                  const float cj = sS[j];
+#pragma unroll
+                  for (int e = 0; e < RPL; ++e) y[e] = fmaf(cj, lds_elem(sv, j * DV + lane * RPL + e, RDT), y[e]);
+                }
+#pragma unroll
+                for (int e = 0; e < RPL; ++e) sY[lane * RPL + e] = y[e];
               }
-#pragma unroll
-              for (int e = 0; e < RPL; ++e) sY[lane * RPL + e] = y[e];
             }
           }
           __syncwarp();
