@@ -61,7 +61,7 @@ cudaError_t dev_info(int dev, DevInfo *out) {
 }  // namespace
 
 cudaError_t plan_rings(const void *kernel, int threads, size_t ck_bytes, size_t rec_bytes, RingHeadFn head,
-                       int units, RingPlan *out) {
+                       int units, RingPlan *out, const int (*shapes)[3], int n_shapes) {
   static std::mutex mu;
   static std::map<std::tuple<int, const void *, size_t, size_t>, RingPlan> cache;
   int dev = 0;
@@ -86,9 +86,20 @@ cudaError_t plan_rings(const void *kernel, int threads, size_t ck_bytes, size_t 
     // preferred shapes, best first: two CTAs per SM each with two
     // checkpoint slots (two producers per SM keep bulk-copy issue off the
     // critical path), then one CTA per SM with fewer or more slots
-    static const int shapes[][3] = {{2, 2, 4}, {2, 2, 3}, {2, 2, 2}, {1, 4, 8}, {1, 3, 6}, {1, 2, 4}, {1, 2, 3}, {1, 1, 2}};
+    // (a shape whose CTAs per SM the kernel's registers and threads do not
+    // allow is skipped: it would run fewer CTAs with the smaller rings)
+    static const int defaults[][3] = {{2, 2, 4}, {2, 2, 3}, {2, 2, 2}, {1, 4, 8}, {1, 3, 6}, {1, 2, 4}, {1, 2, 3}, {1, 1, 2}};
+    if (!shapes) {
+      shapes = defaults;
+      n_shapes = (int)(sizeof(defaults) / sizeof(defaults[0]));
+    }
+    int fit_regs = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit_regs, kernel, threads, 0);
+    if (e != cudaSuccess) return e;
     int ctas = 0;
-    for (const auto &sh : shapes) {
+    for (int k = 0; k < n_shapes; ++k) {
+      const int *sh = shapes[k];
+      if (sh[0] > fit_regs) continue;
       const size_t budget = (size_t)std::min<long>(d.smem_sm / sh[0] - 1024, d.smem_block);
       if (need(sh[2], sh[1]) <= budget) {
         ctas = sh[0];

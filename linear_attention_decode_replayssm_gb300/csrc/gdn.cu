@@ -33,13 +33,14 @@
 // k_j . q_t (eight records per reduction) and the window terms
 // sum_j G_j (k_j . k_t) d_j and sum_j G_j (k_j . q_t) d_j of every state row;
 // it signals the consumers on a second barrier.
-// The consumer warps take the checkpoint into registers, free its slot at
-// once, and form S_ckpt k_t and S_ckpt q_t in one pass with one transposed
-// group reduction; the lanes that finish a row add the window terms, form
-// d_t and the output, or fold the window into the row on a flush.  A state
-// row never leaves its warp, so the consumer warps never wait for each
-// other.  All waits are bounded and report RS_DERR_TIMEOUT instead of
-// hanging.
+// Two groups of four consumer warps take alternate units.  On a non-flush
+// unit a group forms S_ckpt k_t and S_ckpt q_t in one pass over the slot
+// (freeing it after the pass) with one transposed group reduction; the lanes
+// that finish a row add the window terms and form d_t and the output.  On a
+// flush each warp takes 16 whole rows in tensor-core accumulator layout and
+// folds the window on the tensor cores.  A state row never leaves its warp,
+// so the consumer warps never wait for each other.  All waits are bounded
+// and report RS_DERR_TIMEOUT instead of hanging.
 #include "common.cuh"
 #include "launch.h"
 #include "replayssm.h"
@@ -73,9 +74,10 @@ __host__ __device__ inline uint32_t gdn_head(int nsr, int nsc) { return align128
 // CPR: 16-byte checkpoint chunks a consumer lane holds per state row (chunks
 // cv, cv + G, ...), so the row reductions run over G = DK / (E CPR) lanes.
 // NGRP consumer groups of NCW warps take alternate units (a flush unit's
-// fold in one group overlaps the other group's units).
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int LMAX, int CPR, int NGRP>
-__global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
+// fold in one group overlaps the other group's units); MINB CTAs per SM.
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int LMAX, int CPR, int NGRP,
+          int MINB>
+__global__ void __launch_bounds__(NGRP * NCW * 32 + 64, MINB) gdn_replay_kernel(const KArgs a, int nsr, int nsc) {
   using V = CkVec<TC>;
   constexpr int RB = DV / NSPLIT;    // state rows per unit
   constexpr int E = V::E;
@@ -92,9 +94,10 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(con
   static_assert(NC % G == 0 && RB % RPP == 0 && VPT >= 1 && 2 * VPT <= G, "bad tiling");
   static_assert(DK % 8 == 0 && RB % 8 == 0 && DK <= 128 && RB <= 32 * RPL, "bad head dims");
   // flush on the tensor cores: 64-row units of an fp32 or fp16 checkpoint,
-  // each of the group's eight warps one 16-row tile of half the columns
+  // each warp of the group one 16-row tile (of half the columns with eight
+  // warps, of all of them with four)
   constexpr bool MMAF = (sizeof(TC) == 4 || sizeof(TC) == 2) && RB == 64 && DK % 32 == 0 && (DK & (DK - 1)) == 0 &&
-                        NCW == 8;
+                        (NCW == 8 || NCW == 4);
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -420,8 +423,8 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(con
     if constexpr (MMAF) {
       if (flush) {
         // Flush on the tensor cores.  Warp lw holds state rows rA = 16 (lw % 4)
-        // + g and rB = rA + 8 of the unit, columns 64 (lw / 4) + 16 bk + 4t ..
-        // + 3 in accumulator layout.  S_ckpt k_t and S_ckpt q_t of its rows
+        // + g and rB = rA + 8 of the unit, columns (DK / CW) (lw / 4) + 16 bk +
+        // 4t .. + 3 in accumulator layout (CW = NCW / 4 warps share a row).  S_ckpt k_t and S_ckpt q_t of its rows
         // come from the whole rows in the slot; then d_t, the output by the
         // expansion o = alpha_t (Gamma S_ckpt q_t + window term) + d_t (k_t .
         // q_t) (the unrounded S_new applied to q_t), and the fold S_new =
@@ -429,9 +432,10 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(con
         // as a rank-(p+1) m16n8k8 tf32 product: each weighted value split into
         // two tf32 terms (the current d_t unrounded), 16-bit keys exact, fp32
         // keys split too.
-        constexpr int NBH = DK / 32;  // 16-column blocks of a half row
+        constexpr int CW = NCW / 4;        // warps per row
+        constexpr int NBH = DK / 16 / CW;  // 16-column blocks a warp holds
         const int g8 = lane >> 2, t4 = lane & 3;
-        const int rA = 16 * (lw & 3) + g8, rB = rA + 8, cb = 64 * (lw >> 2);
+        const int rA = 16 * (lw & 3) + g8, rB = rA + 8, cb = (DK / CW) * (lw >> 2);
         const unsigned char *ck_slot = ck_slots + (size_t)c * CKB;
         const unsigned char *skt = st + lay.kt, *sq = st + lay.q, *sk = st + lay.k, *sd = st + lay.d;
         auto ld4 = [&](int r, int col) -> float4 {
@@ -449,8 +453,8 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(con
         float4 xa[NBH], xb[NBH];
         float kA = 0.f, kB = 0.f, qA = 0.f, qB = 0.f;
 #pragma unroll
-        for (int bk = 0; bk < 2 * NBH; ++bk) {
-          const int col = (cb + 16 * bk + 4 * t4) & (DK - 1);  // own half first, then the other
+        for (int bk = 0; bk < DK / 16; ++bk) {
+          const int col = (cb + 16 * bk + 4 * t4) & (DK - 1);  // own columns first, then the rest
           const float4 ya = ld4(rA, col), yb = ld4(rB, col);
           float k4[4], q4[4];
           lds_cols<4>(skt, col, idt, k4);
@@ -553,15 +557,19 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(con
         continue;
       }
     }
-    uint4 raw[VPT][CPR];
-    {
-      const uint4 *ck = reinterpret_cast<const uint4 *>(ck_slots + (size_t)c * CKB);
+    // the checkpoint rows of this thread: held in registers for the fold of
+    // a CUDA-core flush; with the tensor-core flush (a branch of its own)
+    // they are read row by row as the products need them
+    constexpr int VH = MMAF ? 1 : VPT;
+    uint4 raw[VH][CPR];
+    const uint4 *ck = reinterpret_cast<const uint4 *>(ck_slots + (size_t)c * CKB);
+    if constexpr (!MMAF) {
 #pragma unroll
       for (int r = 0; r < VPT; ++r)
 #pragma unroll
         for (int i = 0; i < CPR; ++i) raw[r][i] = ck[(row0 + r * RPP) * NCH + cv + G * i];
+      mbar_arrive(&ck_empty[c]);
     }
-    mbar_arrive(&ck_empty[c]);
 
     const size_t unit = (size_t)slot * a.H + h;
     const float *sa = reinterpret_cast<const float *>(st + lay.a);
@@ -585,7 +593,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(con
 #pragma unroll
       for (int i = 0; i < CPR; ++i) {
         float f[E];
-        V::unpack(raw[r][i], f);
+        V::unpack(MMAF ? ck[(row0 + r * RPP) * NCH + cv + G * i] : raw[MMAF ? 0 : r][i], f);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           s0 = fmaf(f[e], ktc[i][e], s0);
@@ -595,6 +603,7 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(con
       part[r] = s0;
       part[VPT + r] = s1;
     }
+    if constexpr (MMAF) mbar_arrive(&ck_empty[c]);
     group_reduce<2 * VPT, G>(part, lane);
     {
       const bool wr = mbar_wait(&ready[s], ph);
@@ -681,33 +690,39 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, 2) gdn_replay_kernel(con
   }
 }
 
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int LMAX, int CPR, int NGRP>
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int LMAX, int CPR, int NGRP,
+          int MINB>
 static cudaError_t launch_gdn_l(const KArgs &a, cudaStream_t s) {
-  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT, LMAX, CPR, NGRP>;
+  auto kern = gdn_replay_kernel<DV, DK, TC, RT, IT, NCW, NSPLIT, LMAX, CPR, NGRP, MINB>;
   constexpr int threads = NGRP * NCW * 32 + 64;
   const size_t ckb = (size_t)(DV / NSPLIT) * DK * sizeof(TC);
   const size_t rb = gdn_rec(DV / NSPLIT, DK, (int)sizeof(RT), (int)sizeof(IT), a.L).bytes;
+  // one CTA per SM: a checkpoint slot per group, two record slots per group
+  static const int one_cta[][3] = {{1, NGRP, 2 * NGRP}, {1, 2, 4}, {1, 2, 3}, {1, 1, 2}};
   RingPlan plan;
-  cudaError_t e =
-      plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, gdn_head, a.B * a.H * NSPLIT, &plan);
+  cudaError_t e = plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, gdn_head, a.B * a.H * NSPLIT,
+                             &plan, MINB == 1 ? one_cta : nullptr, 4);
   if (e != cudaSuccess) return e;
   kern<<<plan.grid, threads, plan.smem, s>>>(a, plan.nsr, plan.nsc);
   return cudaGetLastError();
 }
 
 // the common short windows get a kernel unrolled for L <= 16
-template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int CPR = 1, int NGRP = 1>
+template <int DV, int DK, typename TC, typename RT, typename IT, int NCW, int NSPLIT, int CPR = 1, int NGRP = 1,
+          int MINB = 2>
 static cudaError_t launch_gdn(const KArgs &a, cudaStream_t s) {
-  return a.L <= 16 ? launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, 16, CPR, NGRP>(a, s)
-                   : launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, RS_MAX_L, CPR, NGRP>(a, s);
+  return a.L <= 16 ? launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, 16, CPR, NGRP, MINB>(a, s)
+                   : launch_gdn_l<DV, DK, TC, RT, IT, NCW, NSPLIT, RS_MAX_L, CPR, NGRP, MINB>(a, s);
 }
 
 template <typename TC, typename RT, typename IT>
 static LaunchFn find_gdn_t(int d_v, int d_k) {
   constexpr bool f32 = sizeof(TC) == 4;
   if (d_v == 16 && d_k == 32) return launch_gdn<16, 32, TC, RT, IT, f32 ? 4 : 2, 1>;
-  if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, TC, RT, IT, 8, 1>;
-  if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, TC, RT, IT, 8, 2, f32 ? 2 : 1>;
+  // 64-row units: two groups of four warps per CTA (measured 100.6 us against
+  // 105.7 for one group of eight at batch 256, 32 heads of 128 x 128)
+  if (d_v == 64 && d_k == 128) return launch_gdn<64, 128, TC, RT, IT, 4, 1, f32 ? 2 : 1, 2>;
+  if (d_v == 128 && d_k == 128) return launch_gdn<128, 128, TC, RT, IT, 4, 2, f32 ? 2 : 1, 2>;
   return nullptr;
 }
 

@@ -43,9 +43,11 @@ struct RingPlan {
   int nsr, nsc;
   size_t smem;
 };
+// `shapes` ({CTAs per SM, checkpoint slots, record slots}, best first)
+// replaces the default list when given.
 using RingHeadFn = uint32_t (*)(int nsr, int nsc);
 cudaError_t plan_rings(const void *kernel, int threads, size_t ck_bytes, size_t rec_bytes, RingHeadFn head,
-                       int units, RingPlan *out);
+                       int units, RingPlan *out, const int (*shapes)[3] = nullptr, int n_shapes = 0);
 
 // The read copy of a two-precision checkpoint cast from its recurrence copy
 // (materialize.cu): n_rows rows of d_k fp32 values.

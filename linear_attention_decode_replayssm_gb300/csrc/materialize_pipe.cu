@@ -15,7 +15,7 @@
 // the checkpoint and the held records, rounded once, with the memory shape
 // of a decode flush: a producer warp streams each unit's checkpoint rows
 // (one bulk copy) and its held records and decays (per-lane cp.async) into
-// slot rings; two groups of four consumer warps take alternate units, each
+// slot rings; groups of four consumer warps take the units in turn, each
 // warp 16 state rows in the accumulator layout of an m16n8k8 tile.  A warp
 // scans the decays itself (products for Mamba-2, sums of log-gates then exp
 // for GDN), folds the records on the tensor cores (each weighted value split
@@ -55,15 +55,16 @@ __host__ __device__ inline uint32_t mat_head(int nsr, int nsc) { return align128
 }  // namespace
 
 // RB state rows per unit (NSPLIT units per head), TC checkpoint type, RT ring
-// type, GDNW: log-gate weights (exp of suffix sums) instead of decay products
-template <int DV, int DK, int NSPLIT, typename TC, typename RT, bool GDNW>
+// type, GDNW: log-gate weights (exp of suffix sums) instead of decay products,
+// NGRP consumer groups of four warps
+template <int DV, int DK, int NSPLIT, typename TC, typename RT, bool GDNW, int NGRP>
 // One CTA per SM: the state held in accumulator layout and the split
-// operands fit in 112 registers without spilling; two CTAs per SM would
-// allow 96 (18 warps, five on one scheduler) and measured slower.
+// operands fit in 112 registers without spilling (two CTAs of two groups
+// would allow 96 -- 18 warps, five on one scheduler -- and measured slower);
+// three groups and the producer are 13 warps, at most four a scheduler.
 __global__ void __maxnreg__(112) mat_pipe_kernel(const rs_materialize_args a, int nsr, int nsc) {
   constexpr int RB = DV / NSPLIT;
   constexpr int NCW = RB / 16;  // consumer warps per group: 16 rows each
-  constexpr int NGRP = 2;
   constexpr int NC = NCW * 32;
   constexpr int PROD = NGRP * NCW;
   constexpr int NB = DK / 16;
@@ -343,17 +344,21 @@ __global__ void __maxnreg__(112) mat_pipe_kernel(const rs_materialize_args a, in
   if (tid == 0 && *(volatile int *)s_abort) report(a.dev_err, kDerrTimeout);
 }
 
-template <int DV, int DK, int NSPLIT, typename TC, typename RT, bool GDNW>
+template <int DV, int DK, int NSPLIT, typename TC, typename RT, bool GDNW, int NGRP = 3>
 static cudaError_t launch_mat_pipe(const rs_materialize_args &a, int gdn, cudaStream_t s) {
   (void)gdn;
-  auto kern = mat_pipe_kernel<DV, DK, NSPLIT, TC, RT, GDNW>;
+  auto kern = mat_pipe_kernel<DV, DK, NSPLIT, TC, RT, GDNW, NGRP>;
   constexpr int RB = DV / NSPLIT;
-  constexpr int threads = 2 * 4 * 32 + 32;
+  constexpr int threads = NGRP * 4 * 32 + 32;
   const size_t ckb = (size_t)RB * DK * sizeof(TC);
   const size_t rb = mat_rec(RB, DK, (int)sizeof(RT), a.L, 4).bytes;
+  // three checkpoint slots for the three groups: measured faster than both
+  // two and four (batch 256, 128 heads of 64 x 128: 346 us against 357 and
+  // 363)
+  static const int shapes[][3] = {{1, 3, 6}, {1, 2, 4}, {1, 2, 3}, {1, 1, 2}};
   RingPlan plan;
-  cudaError_t e =
-      plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, mat_head, a.B * a.H * NSPLIT, &plan);
+  cudaError_t e = plan_rings(reinterpret_cast<const void *>(kern), threads, ckb, rb, mat_head, a.B * a.H * NSPLIT,
+                             &plan, shapes, 4);
   if (e != cudaSuccess) return e;
   kern<<<plan.grid, threads, plan.smem, s>>>(a, plan.nsr, plan.nsc);
   return cudaGetLastError();
