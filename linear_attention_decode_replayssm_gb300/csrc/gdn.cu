@@ -318,14 +318,12 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + 64, MINB) gdn_replay_kernel(
                 for (int e = 0; e < 4; ++e) kk[e] = kt4[e];
               }
             }
-            float dk = 0.f, dq = 0.f;
+            // both dots of the record share its key: one packed FMA per element
+            float2 dkq = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              dk = fmaf(kk[e], kt4[e], dk);
-              dq = fmaf(kk[e], q4[e], dq);
-            }
-            part[r] = dk;
-            part[8 + r] = dq;
+            for (int e = 0; e < 4; ++e) dkq = ffma2(make_float2(kk[e], kk[e]), make_float2(kt4[e], q4[e]), dkq);
+            part[r] = dkq.x;
+            part[8 + r] = dkq.y;
           }
           group_reduce<16, 32>(part, lane);
           const int vi = group_reduce_index<16, 32>(lane);

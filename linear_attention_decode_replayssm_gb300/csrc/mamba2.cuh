@@ -726,22 +726,43 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
             }
           }
         }
-        // checkpoint GEMV partials from the stage
-#pragma unroll
-        for (int r = 0; r < VPT; ++r) {
-          float acc = 0.f;
-#pragma unroll
-          for (int i = 0; i < CPR; ++i) {
-            float f[E];
-            if constexpr (TWO) {
-              LpVec<TL>::unpack(raw[r][i], f);
-            } else {
-              V::unpack(raw[r][i], f);
-            }
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc = fmaf(f[e], qv[i][e], acc);
+        // checkpoint GEMV partials from the stage (two rows per packed FMA
+        // when a thread holds an even number of rows)
+        auto unpack_raw = [&](int r, int i, float (&f)[E]) {
+          if constexpr (TWO) {
+            LpVec<TL>::unpack(raw[r][i], f);
+          } else {
+            V::unpack(raw[r][i], f);
           }
-          part[r] = acc;
+        };
+        if constexpr (VPT % 2 == 0) {
+#pragma unroll
+          for (int r = 0; r < VPT; r += 2) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < CPR; ++i) {
+              float f0[E], f1[E];
+              unpack_raw(r, i, f0);
+              unpack_raw(r + 1, i, f1);
+#pragma unroll
+              for (int e = 0; e < E; ++e) acc = ffma2(make_float2(f0[e], f1[e]), make_float2(qv[i][e], qv[i][e]), acc);
+            }
+            part[r] = acc.x;
+            part[r + 1] = acc.y;
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < VPT; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPR; ++i) {
+              float f[E];
+              unpack_raw(r, i, f);
+#pragma unroll
+              for (int e = 0; e < E; ++e) acc = fmaf(f[e], qv[i][e], acc);
+            }
+            part[r] = acc;
+          }
         }
         group_reduce<VPT, G>(part, lane);
         if constexpr (WW) {
