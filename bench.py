@@ -502,8 +502,10 @@ def measure_e2e(lib, torch, layer, steps, dist):
     moves the buffer; the decode is launched through the C ABI with its
     arguments marshalled once per device buffer (``prepare_decode``); one D2H
     copy brings the output back and the host reads it.  Uploads, decodes and
-    downloads run on three streams with two device buffers, so step t+1's
-    upload and step t-1's download overlap step t's decode."""
+    downloads run on three streams with three device buffers, and the host
+    issues step t+2 before it waits for step t's output, so the next uploads
+    and the last download overlap a decode and the host's own work never sits
+    between two decodes."""
     dev = layer.device
     s = layer.spec
     B, H, dv, dk, L = (s[k] for k in ("B", "H", "d_v", "d_k", "L"))
@@ -537,11 +539,13 @@ def measure_e2e(lib, torch, layer, steps, dist):
                 hv[name].copy_(x[name])
         host_buf.append(hb)
         host.append((hv["wp"].numpy(), hv["fl"].numpy()))
-    dev_buf = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
-    outs = [torch.empty_like(layer.out) for _ in range(2)]
-    o_h = [torch.empty(layer.out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    NBUF = 3  # steps in flight
+    assert N_INPUT_SETS > NBUF  # a staging buffer is rewritten only after its upload is done
+    dev_buf = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(NBUF)]
+    outs = [torch.empty_like(layer.out) for _ in range(NBUF)]
+    o_h = [torch.empty(layer.out.shape, dtype=torch.float32).pin_memory() for _ in range(NBUF)]
     calls = []
-    for i in range(2):
+    for i in range(NBUF):
         dv_ = views(dev_buf[i])
         kw = dict(ckpt=layer.ckpt, ring_v=layer.ring_v, ring_k=layer.ring_k, ring_a=layer.ring_a,
                   slot_idx=layer.slot_idx, write_pos=dv_["wp"], is_flush=dv_["fl"], v=dv_["v"], k=dv_["k"],
@@ -553,13 +557,13 @@ def measure_e2e(lib, torch, layer, steps, dist):
                                             ckpt_lp_scale=layer.ckpt_lp_scale, kq_scratch=layer.kq, **kw))
     d2h = o_h[0].numel() * 4
     up_s, comp, down_s = (torch.cuda.Stream(device=dev) for _ in range(3))
-    up = [torch.cuda.Event() for _ in range(2)]     # a device buffer holds this step's inputs
-    used = [torch.cuda.Event() for _ in range(2)]   # the decode that read a device buffer is done
-    back = [torch.cuda.Event() for _ in range(2)]   # an output buffer has reached host memory
+    up = [torch.cuda.Event() for _ in range(NBUF)]     # a device buffer holds this step's inputs
+    used = [torch.cuda.Event() for _ in range(NBUF)]   # the decode that read a device buffer is done
+    back = [torch.cuda.Event() for _ in range(NBUF)]   # an output buffer has reached host memory
     ds = layer.decode_step0.copy()
 
     def launch(t):
-        i, hs = t % 2, t % N_INPUT_SETS
+        i, hs = t % NBUF, t % N_INPUT_SETS
         wp, fl = host[hs]
         lib.replayssm_plan_step(ds + t, L, write_pos=wp, is_flush=fl)
         up_s.wait_event(used[i])
@@ -576,14 +580,15 @@ def measure_e2e(lib, torch, layer, steps, dist):
         back[i].record(down_s)
 
     def read(t):
-        back[t % 2].synchronize()  # the host holds this step's output
-        return float(o_h[t % 2][0, 0, 0])
+        back[t % NBUF].synchronize()  # the host holds this step's output
+        return float(o_h[t % NBUF][0, 0, 0])
 
     def run(n):
-        launch(0)
+        for t in range(min(NBUF - 1, n)):
+            launch(t)
         for t in range(n):
-            if t + 1 < n:
-                launch(t + 1)
+            if t + NBUF - 1 < n:
+                launch(t + NBUF - 1)
             read(t)
 
     run(3)
