@@ -645,16 +645,26 @@ __global__ void __launch_bounds__(NGRP * NCW * 32 + (WW ? 64 : 32), 2)
         float q16[16];
         lds_cols<16>(st + lay.q, 16 * c8, RDT, q16);
         float p8[VPT8];
+        static_assert(VPT8 % 2 == 0, "two rows per packed FMA");
 #pragma unroll
-        for (int r = 0; r < VPT8; ++r) {
-          const uint32_t w4[4] = {raw8[r].x, raw8[r].y, raw8[r].z, raw8[r].w};
-          float acc = 0.f;
+        for (int r = 0; r < VPT8; r += 2) {
+          // rows r and r + 1 in one packed FMA per column (each row's order
+          // of accumulation: columns 3, 2, 1, 0 of every 4)
+          const uint32_t wa[4] = {raw8[r].x, raw8[r].y, raw8[r].z, raw8[r].w};
+          const uint32_t wb[4] = {raw8[r + 1].x, raw8[r + 1].y, raw8[r + 1].z, raw8[r + 1].w};
+          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
           for (int wi = 0; wi < 4; ++wi) {
-            const float2 lo = e4m3x2_to_f2(w4[wi]), hi = e4m3x2_to_f2(w4[wi] >> 16);
-            acc = fmaf(lo.x, q16[4 * wi], fmaf(lo.y, q16[4 * wi + 1], fmaf(hi.x, q16[4 * wi + 2], fmaf(hi.y, q16[4 * wi + 3], acc))));
+            const float2 loa = e4m3x2_to_f2(wa[wi]), hia = e4m3x2_to_f2(wa[wi] >> 16);
+            const float2 lob = e4m3x2_to_f2(wb[wi]), hib = e4m3x2_to_f2(wb[wi] >> 16);
+            const float *qq = q16 + 4 * wi;
+            acc = ffma2(make_float2(hia.y, hib.y), make_float2(qq[3], qq[3]), acc);
+            acc = ffma2(make_float2(hia.x, hib.x), make_float2(qq[2], qq[2]), acc);
+            acc = ffma2(make_float2(loa.y, lob.y), make_float2(qq[1], qq[1]), acc);
+            acc = ffma2(make_float2(loa.x, lob.x), make_float2(qq[0], qq[0]), acc);
           }
-          p8[r] = acc;
+          p8[r] = acc.x;
+          p8[r + 1] = acc.y;
         }
         group_reduce<VPT8, G8>(p8, lane);
         if (!window_ready()) {
