@@ -24,9 +24,10 @@
 //                                 most 2^-17), the bf16 queries exact;
 //   the window  Y = V^T (W o Sd)  (64 x records) by (records x T), the bf16
 //                                 values exact, the weighted dots split;
-//   the fold    S_new = gamma S + sum_{j<h} w_j v_j k_j^T on a flush, m16n8k8
-//                                 tf32 with the weighted values split into
-//                                 two tf32 terms (the bf16 keys are exact).
+//   the fold    S_new = gamma S + sum_{j<h} w_j v_j k_j^T on a flush, m16n8k16
+//                                 bf16 over 16 records a tile, the weighted
+//                                 values split into two bf16 terms (relative
+//                                 error at most 2^-17), the bf16 keys exact.
 // o = D o C + Y is then formed in registers: C and Y share the accumulator
 // layout (a warp's 16 state rows, lane 4g+t holding rows g and g+8 of drafts
 // 2t and 2t+1).  The state sits in accumulator layout too, each lane holding
@@ -377,27 +378,29 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
     // element split into two bf16 terms.
     const float gam = flush ? sWf[64] : 1.f;
     TC *ckg = static_cast<TC *>(a.ckpt) + unit * (DV * DK);
-    // the fold's A operands of records j0 + t4 and j0 + t4 + 4 (weighted
-    // values of rows rA and rB, each split into two tf32 terms); past h they
-    // weigh 0 and read record 0
-    auto fold_a = [&](int j0, uint32_t (&ah)[4], uint32_t (&al)[4], int &ra, int &rb) {
-      const int ja = j0 + t4, jb = ja + 4;
-      ra = ja < hc ? ja : 0;
-      rb = jb < hc ? jb : 0;
-      const float wa = ja < hc ? sWf[ja] : 0.f, wb = jb < hc ? sWf[jb] : 0.f;
-      split_tf32(wa * bf16_at(sv, ra * DV + v_pos(ra, rA)), ah[0], al[0]);
-      split_tf32(wa * bf16_at(sv, ra * DV + v_pos(ra, rB)), ah[1], al[1]);
-      split_tf32(wb * bf16_at(sv, rb * DV + v_pos(rb, rA)), ah[2], al[2]);
-      split_tf32(wb * bf16_at(sv, rb * DV + v_pos(rb, rB)), ah[3], al[3]);
+    // the fold's A operands for the 16 committed records from j0, records
+    // j0 + 2t + {0, 1} and j0 + 2t + 8 + {0, 1} of an m16n8k16 tile (weighted
+    // values of rows rA and rB, each split into two bf16 terms: relative error
+    // at most 2^-17, as for S Q); past h they weigh 0 and read record 0
+    auto fold_a = [&](int j0, uint32_t (&ah)[4], uint32_t (&al)[4], int (&rj)[4]) {
+      float w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j0 + 2 * t4 + (e & 1) + 8 * (e >> 1);
+        rj[e] = j < hc ? j : 0;
+        w[e] = j < hc ? sWf[j] : 0.f;
+      }
+      auto wv = [&](int e, int r) { return w[e] * bf16_at(sv, rj[e] * DV + v_pos(rj[e], r)); };
+      split_bf16x2(wv(0, rA), wv(1, rA), ah[0], al[0]);
+      split_bf16x2(wv(0, rB), wv(1, rB), ah[1], al[1]);
+      split_bf16x2(wv(2, rA), wv(3, rA), ah[2], al[2]);
+      split_bf16x2(wv(2, rB), wv(3, rB), ah[3], al[3]);
     };
     // the first 16 committed records' operands are formed once for all
     // column blocks (a window of L <= 16 fits); later ones per block
-    uint32_t fh[2][4], fl[2][4];
-    int fra[2], frb[2];
-    if (flush) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) fold_a(8 * q, fh[q], fl[q], fra[q], frb[q]);
-    }
+    uint32_t fh[4], fl[4];
+    int frj[4];
+    if (flush) fold_a(0, fh, fl, frj);
     float cacc[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) cacc[n][0] = cacc[n][1] = cacc[n][2] = cacc[n][3] = 0.f;
@@ -407,29 +410,29 @@ __global__ void __launch_bounds__(NGRP * (DV / 16) * 32 + 32, 2)
       if (flush) {
         pa.x *= gam; pa.y *= gam; pa.z *= gam; pa.w *= gam;
         pb.x *= gam; pb.y *= gam; pb.z *= gam; pb.w *= gam;
-        for (int j0 = 0; j0 < hc; j0 += 8) {
+        const uint16_t *sk16 = reinterpret_cast<const uint16_t *>(sk);
+        for (int j0 = 0; j0 < hc; j0 += 16) {
           uint32_t ah[4], al[4];
-          int ra, rb;
-          if (j0 < 16) {
-            const int q = j0 >> 3;
+          int rj[4];
+          if (j0 == 0) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              ah[e] = q ? fh[1][e] : fh[0][e];
-              al[e] = q ? fl[1][e] : fl[0][e];
+              ah[e] = fh[e];
+              al[e] = fl[e];
+              rj[e] = frj[e];
             }
-            ra = q ? fra[1] : fra[0];
-            rb = q ? frb[1] : frb[0];
           } else {
-            fold_a(j0, ah, al, ra, rb);
+            fold_a(j0, ah, al, rj);
           }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const int col = 16 * bk + 4 * (g8 >> 1) + (g8 & 1) + 2 * hf;  // column of tile index n = g8
             float d[4] = {hf ? pa.z : pa.x, hf ? pa.w : pa.y, hf ? pb.z : pb.x, hf ? pb.w : pb.y};
-            const uint32_t bb[2] = {__float_as_uint(bf16_at(sk, ra * DK + kq_pos(ra, col))),
-                                    __float_as_uint(bf16_at(sk, rb * DK + kq_pos(rb, col)))};
-            mma_tf32(d, ah, bb);
-            mma_tf32(d, al, bb);
+            // the bf16 keys of the tile's records at this column, exact
+            const uint32_t b0 = pack_bf16(sk16[rj[0] * DK + kq_pos(rj[0], col)], sk16[rj[1] * DK + kq_pos(rj[1], col)]);
+            const uint32_t b1 = pack_bf16(sk16[rj[2] * DK + kq_pos(rj[2], col)], sk16[rj[3] * DK + kq_pos(rj[3], col)]);
+            mma_bf16(d, ah, b0, b1);
+            mma_bf16(d, al, b0, b1);
             if (hf) {
               pa.z = d[0]; pa.w = d[1]; pb.z = d[2]; pb.w = d[3];
             } else {
