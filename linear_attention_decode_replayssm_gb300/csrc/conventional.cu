@@ -21,7 +21,7 @@ namespace rs {
 // update are independent once the row dots are known, so a 128 x 128 fp32
 // head is two 32 KiB units, the same shape as a 64 x 128 Mamba-2 head.
 template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT>
-__global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
+__device__ __forceinline__ void conventional_step(const KArgs &a) {
   using V = CkVec<TC>;
   constexpr int RB = DV / NSPLIT;
   constexpr int E = V::E;
@@ -82,18 +82,18 @@ __global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
     kv[e] = sK[cv * E + e];
     qv[e] = sQ[cv * E + e];
   }
-  float f[VPT][E];
-#pragma unroll
-  for (int r = 0; r < VPT; ++r) V::unpack(raw[r], f[r]);
-
+  // rows are widened as they are used (the packed rows stay in registers):
+  // fewer registers, more CTAs and bytes in flight per SM
   if (DELTA) {
     // u = beta (v - alpha S k): needs the full row dot S k first
     float part[VPT];
 #pragma unroll
     for (int r = 0; r < VPT; ++r) {
+      float fr[E];
+      V::unpack(raw[r], fr);
       float s = 0.f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) s = fmaf(f[r][e], kv[e], s);
+      for (int e = 0; e < E; ++e) s = fmaf(fr[e], kv[e], s);
       part[r] = s;
     }
     group_reduce<VPT, G>(part, lane);
@@ -109,14 +109,16 @@ __global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
 #pragma unroll
   for (int r = 0; r < VPT; ++r) {
     const float vv = upd[row0 + r * RPP];
+    float fr[E];
+    V::unpack(raw[r], fr);
     float s = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      f[r][e] = fmaf(alpha, f[r][e], vv * kv[e]);
-      s = fmaf(f[r][e], qv[e], s);
+      fr[e] = fmaf(alpha, fr[e], vv * kv[e]);
+      s = fmaf(fr[e], qv[e], s);
     }
     part[r] = s;
-    st_vec(st + (size_t)(row0 + r * RPP) * DK + cv * E, V::pack(f[r]));
+    st_vec(st + (size_t)(row0 + r * RPP) * DK + cv * E, V::pack(fr));
   }
   group_reduce<VPT, G>(part, lane);
   if (group_reduce_writer<VPT, G>(lane)) sC[row0 + group_reduce_index<VPT, G>(lane) * RPP] = part[0];
@@ -124,9 +126,24 @@ __global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
   for (int i = tid; i < RB; i += NT) orow[i] = sC[i];
 }
 
-template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT = 1>
+template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT>
+__global__ void __launch_bounds__(NT) conventional_kernel(const KArgs a) {
+  conventional_step<DV, DK, TC, NT, DELTA, NSPLIT>(a);
+}
+
+// the same step with registers bounded so that MINB CTAs fit on an SM
+template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT, int MINB>
+__global__ void __launch_bounds__(NT, MINB) conventional_kernel_bounded(const KArgs a) {
+  conventional_step<DV, DK, TC, NT, DELTA, NSPLIT>(a);
+}
+
+template <int DV, int DK, typename TC, int NT, bool DELTA, int NSPLIT = 1, int MINB = 0>
 static cudaError_t launch_conv(const KArgs &a, cudaStream_t s) {
-  conventional_kernel<DV, DK, TC, NT, DELTA, NSPLIT><<<(unsigned)((size_t)a.B * a.H * NSPLIT), NT, 0, s>>>(a);
+  const unsigned grid = (unsigned)((size_t)a.B * a.H * NSPLIT);
+  if constexpr (MINB > 0)
+    conventional_kernel_bounded<DV, DK, TC, NT, DELTA, NSPLIT, MINB><<<grid, NT, 0, s>>>(a);
+  else
+    conventional_kernel<DV, DK, TC, NT, DELTA, NSPLIT><<<grid, NT, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -138,7 +155,10 @@ static LaunchFn find_conv_t(int d_v, int d_k, int ckpt_dtype) {
     if (d_v == 128 && d_k == 128) return launch_conv<128, 128, float, 256, DELTA, 2>;
   } else if (ckpt_dtype == kF16) {
     if (d_v == 16 && d_k == 32) return launch_conv<16, 32, __half, 64, DELTA>;
-    if (d_v == 64 && d_k == 128) return launch_conv<64, 128, __half, 128, DELTA>;
+    // eight 16 KiB CTAs per SM keep enough bytes in flight (Mamba-2: 207 ->
+    // 172 us at batch 256 with the rows widened as used); the delta rule
+    // would spill at that bound
+    if (d_v == 64 && d_k == 128) return launch_conv<64, 128, __half, 128, DELTA, 1, DELTA ? 0 : 8>;
     if (d_v == 128 && d_k == 128) return launch_conv<128, 128, __half, 256, DELTA>;
   }
   return nullptr;
