@@ -1,4 +1,4 @@
-// Conventional load-update-store decode step (the baseline ReplaySSM is judged against).
+// Conventional load-update-store decode step (the baseline ReplaySSM is measured against).
 //
 // Sources:
 //   [Ghana] S. Ghana, "ReplaySSM: an SSM decoder that writes its state once
